@@ -1,0 +1,314 @@
+/*
+ * moe.h - C ABI of the B300 sparse Mixture-of-Experts FFN layer library.
+ *
+ * One MoE FFN layer forward pass, y = sum_i G(x)_i * E_i(x)
+ * ("Understanding Mixture of Experts", section "How MoE differs from the
+ * Transformer", layer equation), with SwiGLU experts E(x) = (silu(x W1) *
+ * (x W3)) W2 and three routing modes:
+ *   - token choice: each token takes its top-k experts by router score
+ *     (same page, section "Expert and Router", TopK(G(x), k));
+ *   - expert choice: each expert takes its top c = k*T/N tokens
+ *     ("MoE vs MoT: routing and inference cost", section "Mixture of Tokens");
+ *   - capacity-aware token drop: an expert over capacity C = gamma * N_bar
+ *     drops the candidates with the lowest gating score, optionally with m
+ *     extra local candidates per token ("Capacity-Aware Inference: Mitigating
+ *     the Straggler Effect in MoE", section 2, (1) Token Drop and (2) Expanded
+ *     Drop).
+ *
+ * Conventions for every call below:
+ *   - Pointers to tensors are DEVICE pointers unless a comment says host.
+ *     The caller allocates and owns every buffer, including the workspace;
+ *     the library never allocates, frees or synchronises inside these calls
+ *     (moe_get_device_status is the one call that synchronises a stream).
+ *   - `stream` is a cudaStream_t passed as void*; NULL is the legacy default
+ *     stream. All work is enqueued on it asynchronously, in call order.
+ *   - Tensors are dense row-major. Activations, weights and y have the
+ *     config's dtype (MOE_BF16 or MOE_F32); logits, scores and gates are fp32;
+ *     indices and counts are int32. Accumulation is always fp32.
+ *   - Base pointers of activation/weight tensors must be 16-byte aligned.
+ *     bf16 layers need d and f to be multiples of 64; fp32 layers need d to
+ *     be a multiple of 8.
+ *   - Return value: MOE_OK or a negative MOE_ERR_* code. Argument checks run
+ *     on the host before anything is enqueued; on failure no output is touched.
+ *     Conditions a kernel detects (a bounded wait that expired) are recorded in
+ *     a sticky status word in the workspace, read by moe_get_device_status.
+ *   - Inputs must be finite (no NaN/Inf); non-finite values give undefined
+ *     routing.
+ *
+ * Notation: T tokens, d model width, N routed experts, f expert hidden width,
+ * k experts per token, m expanded candidates, kc candidate slots per token
+ * (k + m, or N under expert choice), C capacity, P kept (token, expert) pairs,
+ * rows_max the upper bound of P that sizes the row buffers (moe_sizes).
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---- */
+#define MOE_OK                  0
+#define MOE_ERR_NULL           (-1)  /* a required pointer is NULL */
+#define MOE_ERR_SHAPE          (-2)  /* a size is out of range or inconsistent */
+#define MOE_ERR_ALIGN          (-3)  /* a pointer or row pitch breaks the 16-byte rule */
+#define MOE_ERR_WORKSPACE      (-4)  /* workspace smaller than moe_workspace_size */
+#define MOE_ERR_UNSUPPORTED    (-5)  /* valid but not implemented (see limits below) */
+#define MOE_ERR_LAUNCH         (-6)  /* the CUDA runtime refused a launch */
+#define MOE_ERR_DEVICE_TIMEOUT (-7)  /* a kernel's bounded wait expired (sticky, device) */
+#define MOE_ERR_DEVICE_BOUNDS  (-8)  /* a kernel saw an index outside its buffer (sticky) */
+
+/* ---- routing modes and dtypes ---- */
+#define MOE_TOKEN_CHOICE   0
+#define MOE_EXPERT_CHOICE  1
+#define MOE_CAPACITY_DROP  2
+
+#define MOE_F32  0
+#define MOE_BF16 1
+
+/* flags */
+#define MOE_LOGITS_GIVEN 1  /* router logits are an input; x and W_router are not read for routing */
+
+/* Limits: 1 <= N <= 256, 1 <= k <= N, k + m <= 32, expert choice N <= 256,
+ * T <= 24576 (per-expert candidate lists are held in shared memory),
+ * capacity-drop/expanded group_size divides N. */
+
+typedef struct moe_config {
+  int32_t T;          /* tokens in the batch */
+  int32_t d;          /* model width */
+  int32_t N;          /* routed experts */
+  int32_t f;          /* routed expert hidden width */
+  int32_t k;          /* experts per token (expert choice: c = floor(k*T/N)) */
+  int32_t mode;       /* MOE_TOKEN_CHOICE / MOE_EXPERT_CHOICE / MOE_CAPACITY_DROP */
+  double  gamma;      /* capacity factor; C = min(T, floor(gamma * k*T/N)); INFINITY = no limit */
+  int32_t m;          /* expanded drop: extra local candidates per token (0 = off) */
+  int32_t group_size; /* experts per device group for expanded drop */
+  int32_t renorm;     /* 1: gates divided by their sum over the token's candidates */
+  int32_t f_shared;   /* hidden width of the always-on shared expert (0 = none) */
+  int32_t dtype;      /* MOE_BF16 or MOE_F32 */
+  int32_t flags;      /* MOE_LOGITS_GIVEN */
+} moe_config;
+
+/* Derived sizes of a config (host values). */
+typedef struct moe_sizes_t {
+  int32_t kc;          /* candidate slots per token */
+  int32_t capacity;    /* C (capacity drop), c (expert choice) or T (token choice) */
+  int64_t rows_max;    /* upper bound of P: row capacity of xp/op/row_token/row_gate */
+  size_t  workspace;   /* bytes moe_layer_forward needs */
+  size_t  ffn_workspace; /* bytes moe_expert_ffn needs for rows_max rows */
+} moe_sizes_t;
+
+/* Number of doubles moe_layer_forward / moe_load_stats write to `stats`. */
+#define MOE_STATS_LEN 8
+/* stats[0] P kept pairs        stats[1] candidate pairs before selection
+ * stats[2] max kept per expert stats[3] mean kept per expert
+ * stats[4] max/mean kept (the straggler ratio of "Capacity-Aware Inference", section 1)
+ * stats[5] dropped fraction of candidate pairs
+ * stats[6] Switch balance term B = sum_i f_i * P_i ("MoE vs MoT", section
+ *          "MoE basic structure"), f_i = demand_i / sum(demand), P_i = mean_t p[t,i]
+ * stats[7] N * B (1 for a perfectly even router) */
+
+/* Fill `out` for `cfg`. Host only; no CUDA call. Returns MOE_ERR_* if the
+ * config is invalid or outside the limits. */
+int moe_sizes(const moe_config* cfg, moe_sizes_t* out);
+
+/* Bytes of workspace moe_layer_forward needs (0 if the config is invalid). */
+size_t moe_workspace_size(const moe_config* cfg);
+
+/* Bytes of workspace moe_expert_ffn needs for `rows_max` rows of hidden width f. */
+size_t moe_ffn_workspace_size(int64_t rows_max, int32_t f, int32_t dtype);
+
+/*
+ * Router: logits, softmax scores and each token's candidate experts.
+ * "Understanding Mixture of Experts", section "Expert and Router": the router
+ * decides which experts receive the token and G(x) weights them; TopK(G(x),k).
+ *
+ *   x        [T, d] dtype       (not read with MOE_LOGITS_GIVEN)
+ *   W_router [d, N] dtype       (not read with MOE_LOGITS_GIVEN)
+ *   bias     [N] fp32, nullable; added to the logits
+ *   logits   [T, N] fp32: output, or input with MOE_LOGITS_GIVEN
+ *   scores   [T, N] fp32 nullable: p = softmax over experts of each row,
+ *            by the fixed fp32 sequence max / subtract / Cody-Waite exp /
+ *            left-to-right sum / correctly rounded divide, so every decision
+ *            taken from it is reproducible bit for bit
+ *   cand_idx [T, kc] int32: token choice / capacity drop: the top-k experts
+ *            by logit, best first, ties to the lower expert; then (m > 0) the
+ *            m highest-logit experts of the token's home group not already
+ *            chosen; empty slots hold -1. Unused (nullable) under expert choice.
+ *   cand_gate[T, kc] fp32: gate of each slot, p or (renorm) p divided by the
+ *            left-to-right sum of the token's slot probabilities. Under expert
+ *            choice kc = N and cand_gate receives the scores p.
+ *   home_group [T] int32 nullable: device group of each token for expanded
+ *            drop; NULL = contiguous shards, group floor(t*G/T), G = N/group_size.
+ */
+int moe_route(const moe_config* cfg, const void* x, const void* W_router, const float* bias,
+              float* logits, float* scores, int32_t* cand_idx, float* cand_gate,
+              const int32_t* home_group, void* stream);
+
+/*
+ * Per-expert selection over the candidates (one thread block per expert).
+ * "Capacity-Aware Inference", section 2 (1) Token Drop: expert e keeps at most
+ * C of its candidates, those with the highest gate (ties: the lower token),
+ * and drops the rest. Under expert choice every token is a candidate of every
+ * expert with gate p[t, e] and exactly c = min(T, floor(k*T/N)) are kept
+ * ("MoE vs MoT", section "Mixture of Tokens"). Under token choice nothing is
+ * dropped and only the ranks below are produced.
+ *
+ *   cand_idx  [T, kc] int32 (ignored under expert choice)
+ *   cand_gate [T, kc] fp32
+ *   slot      [T, kc] int32 out: for a kept slot, its rank among expert e's
+ *             kept tokens in ascending token order; -1 for a dropped or empty slot
+ *   keep      [T, kc] uint8 out, nullable: 1 kept, 0 not
+ *   demand    [N] int32 out: candidates per expert before selection
+ *   kept      [N] int32 out: pairs per expert after selection
+ */
+int moe_capacity_drop(const moe_config* cfg, const int32_t* cand_idx, const float* cand_gate,
+                      int32_t* slot, uint8_t* keep, int32_t* demand, int32_t* kept, void* stream);
+
+/*
+ * Histogram -> prefix sum -> permute: the kept pairs in expert-contiguous row
+ * order, and the token rows gathered into it (the dispatch step that the
+ * all-to-all of "MoE vs MoT", section "MoE basic structure", performs across
+ * devices; here within one GPU).
+ *
+ *   x              [T, d] dtype
+ *   cand_idx, cand_gate, slot   as produced above ([T, kc])
+ *   kept           [N] int32
+ *   expert_offsets [N + 1] int32 out: exclusive prefix sum of kept; [N] = P
+ *   row_token      [rows_max] int32 out: token of each row (rows < P)
+ *   row_gate       [rows_max] fp32 out: gate of each row
+ *   tok_rows       [T, kc] int32 out: rows of each token in ascending expert
+ *                  order (= ascending row), padded with -1
+ *   xp             [rows_max, d] dtype out: xp[r] = x[row_token[r]]
+ * Rows inside an expert are in ascending token order. Rows >= P are not written.
+ */
+int moe_dispatch(const moe_config* cfg, const void* x, const int32_t* cand_idx,
+                 const float* cand_gate, const int32_t* slot, const int32_t* kept,
+                 int32_t* expert_offsets, int32_t* row_token, float* row_gate,
+                 int32_t* tok_rows, void* xp, void* stream);
+
+/*
+ * Grouped SwiGLU experts over expert-contiguous rows ("MoE vs MoT", section
+ * "MoE basic structure": the FFN is replicated N times; section "measured
+ * figures": grouped GEMM for the experts).
+ * For every segment s in [0, n_segments), rows r in
+ * [offsets[s], offsets[s+1]):  h = silu(xp[r] W1[s]) * (xp[r] W3[s]) stored in
+ * dtype, then op[r] = h W2[s] stored in dtype.
+ *
+ *   d, dtype     from cfg (the other cfg fields are not read)
+ *   xp           [rows_max, d] dtype
+ *   offsets      [n_segments + 1] int32, device-resident, non-decreasing,
+ *                offsets[0] = 0, offsets[n_segments] <= rows_max
+ *   f            hidden width of these experts
+ *   W1, W3       [n_segments, d, f] dtype;  W2 [n_segments, f, d] dtype
+ *   op           [rows_max, d] dtype out (rows >= offsets[n_segments] untouched)
+ *   ws           >= moe_ffn_workspace_size(rows_max, f, dtype) bytes
+ * bf16 runs on the tcgen05 tensor cores (fp32 accumulate in tensor memory);
+ * fp32 runs on the fp32 FMA pipes.
+ */
+int moe_expert_ffn(const moe_config* cfg, const void* xp, const int32_t* offsets,
+                   int32_t n_segments, int64_t rows_max, int32_t f,
+                   const void* W1, const void* W3, const void* W2, void* op,
+                   void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * One grouped GEMM, out[r] = A[r] B[s] for rows r of segment s, the second
+ * half of the expert FFN on its own. A [rows_max, K], B [n_segments, K, n_out],
+ * out [rows_max, n_out], all dtype; K and n_out multiples of 64 (bf16).
+ * ws >= moe_ffn_workspace_size(0, 0, dtype) bytes (status word only).
+ */
+int moe_grouped_gemm(int32_t dtype, const void* A, const int32_t* offsets, int32_t n_segments,
+                     int64_t rows_max, int32_t K, int32_t n_out, const void* B, void* out,
+                     void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Gate-weighted combine, the sum of the layer equation ("Understanding
+ * Mixture of Experts", y = sum_i G(x)_i E_i(x)):
+ *   y[t] = sum over r in tok_rows[t] (ascending) of row_gate[r] * op[r]
+ *          + shared_out[t]
+ * summed in fp32 and rounded once to dtype. A token with no row outputs
+ * shared_out[t] (or 0).
+ *   op [rows_max, d], row_gate [rows_max] fp32, tok_rows [T, kc] int32,
+ *   shared_out [T, d] nullable, y [T, d] out.
+ */
+int moe_combine(const moe_config* cfg, const void* op, const float* row_gate,
+                const int32_t* tok_rows, const void* shared_out, void* y, void* stream);
+
+/*
+ * Load statistics of one routed batch into stats[MOE_STATS_LEN] (device
+ * doubles; layout above). scores [T, N] are the router probabilities.
+ */
+int moe_load_stats(const moe_config* cfg, const int32_t* demand, const int32_t* kept,
+                   const float* scores, double* stats, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * The whole layer: route -> select -> dispatch -> expert FFN (+ shared
+ * expert, "How to design inference cost with MoE routing", section "how
+ * routing allocates the compute budget": an always-on expert that every token
+ * passes through, gate 1) -> combine -> statistics, all enqueued on `stream`
+ * with no host synchronisation.
+ *
+ *   x [T, d]; W_router [d, N]; bias [N] fp32 nullable
+ *   W1, W3 [N, d, f]; W2 [N, f, d]
+ *   Ws1, Ws3 [d, f_shared]; Ws2 [f_shared, d]   (read only when f_shared > 0)
+ *   home_group [T] int32 nullable (expanded drop)
+ *   logits [T, N] fp32 nullable: input with MOE_LOGITS_GIVEN (required then);
+ *          otherwise, when non-NULL, receives a copy of the logits
+ *   y [T, d] out; stats [MOE_STATS_LEN] doubles nullable
+ *   ws >= moe_workspace_size(cfg) bytes; intermediates stay readable there
+ *   through moe_workspace_views until the next call that uses ws.
+ */
+int moe_layer_forward(const moe_config* cfg, const void* x, const void* W_router,
+                      const float* bias, const void* W1, const void* W3, const void* W2,
+                      const void* Ws1, const void* Ws3, const void* Ws2,
+                      const int32_t* home_group, float* logits, void* y, double* stats,
+                      void* ws, size_t ws_bytes, void* stream);
+
+/* Device pointers to the intermediates moe_layer_forward leaves in ws. */
+typedef struct moe_views_t {
+  int32_t* status;         /* [1] sticky device status */
+  float*   logits;         /* [T, N] */
+  float*   scores;         /* [T, N] */
+  int32_t* cand_idx;       /* [T, kc] */
+  float*   cand_gate;      /* [T, kc] */
+  int32_t* slot;           /* [T, kc] */
+  uint8_t* keep;           /* [T, kc] */
+  int32_t* demand;         /* [N] */
+  int32_t* kept;           /* [N] */
+  int32_t* expert_offsets; /* [N + 1] */
+  int32_t* row_token;      /* [rows_max] */
+  float*   row_gate;       /* [rows_max] */
+  int32_t* tok_rows;       /* [T, kc] */
+  void*    xp;             /* [rows_max, d] */
+  void*    op;             /* [rows_max, d] */
+  void*    shared_out;     /* [T, d] or NULL */
+} moe_views_t;
+
+/* Carve `ws` into the views above. Host only; no CUDA call. */
+int moe_workspace_views(const moe_config* cfg, void* ws, moe_views_t* out);
+
+/* Enqueue a read of the sticky device status word at ws and synchronise
+ * `stream`; *out_host receives MOE_OK or the first MOE_ERR_DEVICE_* recorded.
+ * `ws` is any workspace passed to the calls above. The status word is the
+ * first 4 bytes of the workspace: zero the workspace, or call
+ * moe_clear_device_status, before its first use. */
+int moe_get_device_status(const void* ws, void* stream, int32_t* out_host);
+
+/* Enqueue a reset of the sticky device status word at ws to MOE_OK. */
+int moe_clear_device_status(void* ws, void* stream);
+
+/* Static description of a status code. */
+const char* moe_status_string(int status);
+
+/* Release host-side caches. Tensor-map descriptors are currently encoded on
+ * every call, so there is nothing to release; the entry point is kept so a
+ * caller need not change when a cache is added. */
+void moe_release_caches(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_B300_H */

@@ -1,0 +1,129 @@
+// Gate-weighted combine, the sum of the layer equation
+// y = sum_i G(x)_i E_i(x) ("Understanding Mixture of Experts", section "How
+// MoE differs from the Transformer").
+//
+// One warp per token; the token's rows (ascending expert) and gates are staged
+// in shared memory, then each lane walks 16-byte column vectors: for every row
+// an FMA into fp32 accumulators in a fixed order (ascending expert, shared
+// expert last), one rounding to the output dtype at the end.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kCombThreads = 256;
+constexpr int kCombWarps = kCombThreads / 32;
+constexpr int kCombMaxRows = 256;
+
+template <typename E> struct Pack;  // 16 bytes of E <-> fp32
+template <> struct Pack<__nv_bfloat16> {
+  static constexpr int n = 8;
+  static __device__ __forceinline__ void unpack(const uint4& q, float* v) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(h[i]);
+      v[2 * i] = f.x;
+      v[2 * i + 1] = f.y;
+    }
+  }
+  static __device__ __forceinline__ uint4 pack(const float* v) {
+    uint4 q;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&q);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    return q;
+  }
+};
+template <> struct Pack<float> {
+  static constexpr int n = 4;
+  static __device__ __forceinline__ void unpack(const uint4& q, float* v) {
+    v[0] = __uint_as_float(q.x); v[1] = __uint_as_float(q.y);
+    v[2] = __uint_as_float(q.z); v[3] = __uint_as_float(q.w);
+  }
+  static __device__ __forceinline__ uint4 pack(const float* v) {
+    return make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
+                      __float_as_uint(v[3]));
+  }
+};
+
+template <typename E>
+__global__ void __launch_bounds__(kCombThreads) combine_kernel(
+    const E* __restrict__ op, const float* __restrict__ row_gate,
+    const int32_t* __restrict__ tok_rows, const E* __restrict__ shared_out, E* __restrict__ y,
+    int T, int d, int kc, int rows_max) {
+  constexpr int V = Pack<E>::n;
+  __shared__ int s_row[kCombWarps][kCombMaxRows];
+  __shared__ float s_gate[kCombWarps][kCombMaxRows];
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  const int nvec = d / V;
+  const int warps_total = kCombWarps * gridDim.x;
+  for (int t = blockIdx.x * kCombWarps + wib; t < T; t += warps_total) {
+    int nrows = 0;
+    for (int base = 0; base < kc; base += 32) {
+      const int j = base + lane;
+      const int r = (j < kc) ? tok_rows[static_cast<size_t>(t) * kc + j] : -1;
+      const bool ok = r >= 0 && r < rows_max;
+      const unsigned b = __ballot_sync(0xffffffffu, ok);
+      if (ok) {  // kept in list order (ascending rows)
+        const int pos = nrows + __popc(b & ((1u << lane) - 1u));
+        s_row[wib][pos] = r;
+        s_gate[wib][pos] = row_gate[r];
+      }
+      nrows += __popc(b);
+    }
+    __syncwarp();
+    const uint4* sh = shared_out ? reinterpret_cast<const uint4*>(shared_out + static_cast<size_t>(t) * d)
+                                 : nullptr;
+    uint4* dst = reinterpret_cast<uint4*>(y + static_cast<size_t>(t) * d);
+    for (int c = lane; c < nvec; c += 32) {
+      float acc[V];
+#pragma unroll
+      for (int i = 0; i < V; ++i) acc[i] = 0.f;
+      for (int r = 0; r < nrows; ++r) {
+        const uint4 q = __ldg(reinterpret_cast<const uint4*>(op + static_cast<size_t>(s_row[wib][r]) * d) + c);
+        float v[V];
+        Pack<E>::unpack(q, v);
+        const float g = s_gate[wib][r];
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc[i] = fmaf(g, v[i], acc[i]);
+      }
+      if (sh) {
+        float v[V];
+        Pack<E>::unpack(__ldg(sh + c), v);
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc[i] += v[i];
+      }
+      dst[c] = Pack<E>::pack(acc);
+    }
+    __syncwarp();
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(int dtype, const void* op, const float* row_gate,
+                           const int32_t* tok_rows, const void* shared_out, void* y, int T,
+                           int d, int kc, int64_t rows_max, cudaStream_t s) {
+  const int rmax = rows_max > 0x7fffffff ? 0x7fffffff : static_cast<int>(rows_max);
+  if (T == 0) return cudaSuccess;
+  int blocks = (T + kCombWarps - 1) / kCombWarps;
+  const int cap = device_sm_count() * 8;
+  if (blocks > cap) blocks = cap;
+  if (dtype == 1) {
+    combine_kernel<__nv_bfloat16><<<blocks, kCombThreads, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(op), row_gate, tok_rows,
+        static_cast<const __nv_bfloat16*>(shared_out), static_cast<__nv_bfloat16*>(y), T, d, kc, rmax);
+  } else {
+    combine_kernel<float><<<blocks, kCombThreads, 0, s>>>(
+        static_cast<const float*>(op), row_gate, tok_rows, static_cast<const float*>(shared_out),
+        static_cast<float*>(y), T, d, kc, rmax);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,430 @@
+// C ABI of the MoE layer library: argument checks, workspace layout and the
+// launch sequence. Every check runs on the host before anything is enqueued.
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <cuda_runtime.h>
+
+#include "../../include/moe.h"
+#include "internal.h"
+
+namespace moe {
+
+int device_sm_count() {
+  static int counts[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (counts[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    counts[dev] = n;
+  }
+  return counts[dev];
+}
+
+namespace {
+
+__global__ void write_pair_kernel(int32_t* p, int32_t a, int32_t b) {
+  p[0] = a;
+  p[1] = b;
+}
+__global__ void clear_status_kernel(int32_t* status) { *status = 0; }
+
+struct Derived {
+  int kc = 0;
+  int cap = 0;            // C, c or T
+  int64_t rows_max = 0;
+  int sx = 0;             // bytes per activation element
+  bool ec = false;
+};
+
+constexpr int kMaxN = 256;
+constexpr int kMaxSlots = 32;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int validate(const moe_config* c, Derived* dv) {
+  if (!c) return MOE_ERR_NULL;
+  if (c->T < 0 || c->d <= 0 || c->N <= 0 || c->f <= 0 || c->k <= 0) return MOE_ERR_SHAPE;
+  if (c->mode != MOE_TOKEN_CHOICE && c->mode != MOE_EXPERT_CHOICE && c->mode != MOE_CAPACITY_DROP)
+    return MOE_ERR_SHAPE;
+  if (c->dtype != MOE_BF16 && c->dtype != MOE_F32) return MOE_ERR_SHAPE;
+  if (c->k > c->N || c->m < 0 || c->f_shared < 0) return MOE_ERR_SHAPE;
+  if (std::isnan(c->gamma) || c->gamma < 0) return MOE_ERR_SHAPE;
+  if (c->m > 0 && (c->group_size <= 0 || c->N % c->group_size != 0)) return MOE_ERR_SHAPE;
+  if (c->N > kMaxN) return MOE_ERR_UNSUPPORTED;
+  if (c->T > select_max_tokens()) return MOE_ERR_UNSUPPORTED;
+  const bool ec = c->mode == MOE_EXPERT_CHOICE;
+  if (ec && c->m != 0) return MOE_ERR_SHAPE;
+  if (!ec && c->k + c->m > kMaxSlots) return MOE_ERR_UNSUPPORTED;
+  if (c->dtype == MOE_BF16) {
+    if (c->d % 64 || c->f % 64 || c->f_shared % 64) return MOE_ERR_SHAPE;
+  } else {
+    if (c->d % 8) return MOE_ERR_SHAPE;
+  }
+  Derived d;
+  d.ec = ec;
+  d.kc = ec ? c->N : c->k + c->m;
+  d.sx = c->dtype == MOE_BF16 ? 2 : 4;
+  const int64_t T = c->T, N = c->N;
+  if (ec) {
+    d.cap = static_cast<int>(std::min<int64_t>(T, (static_cast<int64_t>(c->k) * T) / N));
+    d.rows_max = N * d.cap;
+  } else if (c->mode == MOE_CAPACITY_DROP && !std::isinf(c->gamma)) {
+    const double nbar = static_cast<double>(static_cast<int64_t>(c->k) * T) / static_cast<double>(N);
+    const double cf = std::floor(c->gamma * nbar);
+    d.cap = cf >= static_cast<double>(T) ? static_cast<int>(T) : static_cast<int>(cf);
+    d.rows_max = std::min<int64_t>(T * d.kc, N * d.cap);
+  } else {
+    d.cap = static_cast<int>(T);
+    d.rows_max = T * d.kc;
+  }
+  if (dv) *dv = d;
+  return MOE_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct Layout {
+  size_t status, logits, scores, cand_idx, cand_gate, slot, keep, demand, kept, offsets,
+      shared_offsets, row_token, row_gate, tok_rows, xp, hp, op, shared_out, stats_partial, total;
+};
+
+Layout layout(const moe_config& c, const Derived& d) {
+  Layout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align256(off + bytes);
+    return o;
+  };
+  const size_t T = c.T, N = c.N, kc = d.kc, R = d.rows_max, dd = c.d;
+  L.status = take(256);
+  L.logits = take(T * N * 4);
+  L.scores = take(T * N * 4);
+  L.cand_idx = take(T * kc * 4);
+  L.cand_gate = take(T * kc * 4);
+  L.slot = take(T * kc * 4);
+  L.keep = take(T * kc);
+  L.demand = take(N * 4);
+  L.kept = take(N * 4);
+  L.offsets = take((N + 1) * 4);
+  L.shared_offsets = take(2 * 4);
+  L.row_token = take(R * 4);
+  L.row_gate = take(R * 4);
+  L.tok_rows = take(T * kc * 4);
+  L.xp = take(R * dd * d.sx);
+  const size_t hp_rows = std::max(R * static_cast<size_t>(c.f), T * static_cast<size_t>(c.f_shared));
+  L.hp = take(hp_rows * d.sx);
+  L.op = take(R * dd * d.sx);
+  L.shared_out = take(c.f_shared > 0 ? T * dd * d.sx : 0);
+  L.stats_partial = take(stats_partial_doubles(c.T, c.N) * 8);
+  L.total = off;
+  return L;
+}
+
+template <typename P>
+P* at(void* ws, size_t off) {
+  return reinterpret_cast<P*>(static_cast<unsigned char*>(ws) + off);
+}
+
+int status_from(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH; }
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+// FFN over expert-contiguous rows; hp is scratch of rows_max * f elements.
+int run_ffn(int dtype, const void* xp, const int32_t* offsets, int S, int64_t rows_max, int d,
+            int f, const void* W1, const void* W3, const void* W2, void* hp, void* op,
+            int32_t* status, cudaStream_t s) {
+  cudaError_t e;
+  if (dtype == MOE_BF16) {
+    e = launch_grouped_gemm_tc_bf16(xp, offsets, S, rows_max, d, f, W1, W3, hp, true, status, s);
+    if (e != cudaSuccess) return MOE_ERR_LAUNCH;
+    e = launch_grouped_gemm_tc_bf16(hp, offsets, S, rows_max, f, d, W2, nullptr, op, false, status, s);
+  } else {
+    e = launch_grouped_gemm_simt_f32(static_cast<const float*>(xp), offsets, S, rows_max, d, f,
+                                     static_cast<const float*>(W1), static_cast<const float*>(W3),
+                                     static_cast<float*>(hp), true, s);
+    if (e != cudaSuccess) return MOE_ERR_LAUNCH;
+    e = launch_grouped_gemm_simt_f32(static_cast<const float*>(hp), offsets, S, rows_max, f, d,
+                                     static_cast<const float*>(W2), nullptr,
+                                     static_cast<float*>(op), false, s);
+  }
+  return status_from(e);
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_sizes(const moe_config* cfg, moe_sizes_t* out) {
+  if (!out) return MOE_ERR_NULL;
+  Derived d;
+  const int st = validate(cfg, &d);
+  if (st != MOE_OK) return st;
+  out->kc = d.kc;
+  out->capacity = d.cap;
+  out->rows_max = d.rows_max;
+  out->workspace = layout(*cfg, d).total;
+  out->ffn_workspace = moe_ffn_workspace_size(d.rows_max, cfg->f, cfg->dtype);
+  return MOE_OK;
+}
+
+size_t moe_workspace_size(const moe_config* cfg) {
+  Derived d;
+  if (validate(cfg, &d) != MOE_OK) return 0;
+  return layout(*cfg, d).total;
+}
+
+size_t moe_ffn_workspace_size(int64_t rows_max, int32_t f, int32_t dtype) {
+  if (rows_max < 0 || f < 0) return 0;
+  const size_t sx = dtype == MOE_BF16 ? 2 : 4;
+  return 256 + align256(static_cast<size_t>(rows_max) * static_cast<size_t>(f) * sx);
+}
+
+int moe_route(const moe_config* cfg, const void* x, const void* W_router, const float* bias,
+              float* logits, float* scores, int32_t* cand_idx, float* cand_gate,
+              const int32_t* home_group, void* stream) {
+  Derived d;
+  int st = validate(cfg, &d);
+  if (st != MOE_OK) return st;
+  const bool given = (cfg->flags & MOE_LOGITS_GIVEN) != 0;
+  if (!logits || !cand_gate || (!d.ec && !cand_idx)) return MOE_ERR_NULL;
+  if (!given && (!x || !W_router)) return MOE_ERR_NULL;
+  if (!given && (!aligned16(x) || !aligned16(W_router))) return MOE_ERR_ALIGN;
+  cudaStream_t s = as_stream(stream);
+  if (!given) {
+    if (launch_router_logits(cfg->dtype, x, W_router, bias, logits, cfg->T, cfg->d, cfg->N, s) !=
+        cudaSuccess)
+      return MOE_ERR_LAUNCH;
+  }
+  return status_from(launch_route_tokens(logits, scores, cand_idx, cand_gate, home_group, cfg->T,
+                                         cfg->N, cfg->k, cfg->m, cfg->group_size, cfg->renorm,
+                                         d.ec ? 1 : 0, s));
+}
+
+int moe_capacity_drop(const moe_config* cfg, const int32_t* cand_idx, const float* cand_gate,
+                      int32_t* slot, uint8_t* keep, int32_t* demand, int32_t* kept, void* stream) {
+  Derived d;
+  int st = validate(cfg, &d);
+  if (st != MOE_OK) return st;
+  if (!cand_gate || !slot || !demand || !kept || (!d.ec && !cand_idx)) return MOE_ERR_NULL;
+  return status_from(launch_select(cand_idx, cand_gate, cfg->T, d.kc, cfg->N, d.ec ? 1 : 0, d.cap,
+                                   slot, keep, demand, kept, as_stream(stream)));
+}
+
+int moe_dispatch(const moe_config* cfg, const void* x, const int32_t* cand_idx,
+                 const float* cand_gate, const int32_t* slot, const int32_t* kept,
+                 int32_t* expert_offsets, int32_t* row_token, float* row_gate, int32_t* tok_rows,
+                 void* xp, void* stream) {
+  Derived d;
+  int st = validate(cfg, &d);
+  if (st != MOE_OK) return st;
+  if (!x || !cand_gate || !slot || !kept || !expert_offsets || !row_token || !row_gate ||
+      !tok_rows || !xp || (!d.ec && !cand_idx))
+    return MOE_ERR_NULL;
+  if (!aligned16(x) || !aligned16(xp)) return MOE_ERR_ALIGN;
+  return status_from(launch_dispatch(cfg->dtype, x, cand_idx, cand_gate, slot, kept, cfg->T,
+                                     cfg->d, cfg->N, d.kc, d.ec ? 1 : 0, d.rows_max, expert_offsets, row_token,
+                                     row_gate, tok_rows, xp, as_stream(stream)));
+}
+
+int moe_expert_ffn(const moe_config* cfg, const void* xp, const int32_t* offsets,
+                   int32_t n_segments, int64_t rows_max, int32_t f, const void* W1,
+                   const void* W3, const void* W2, void* op, void* ws, size_t ws_bytes,
+                   void* stream) {
+  if (!cfg) return MOE_ERR_NULL;
+  if (cfg->dtype != MOE_BF16 && cfg->dtype != MOE_F32) return MOE_ERR_SHAPE;
+  if (cfg->d <= 0 || f <= 0 || n_segments < 0 || rows_max < 0) return MOE_ERR_SHAPE;
+  if (cfg->dtype == MOE_BF16 && (cfg->d % 64 || f % 64)) return MOE_ERR_SHAPE;
+  if (n_segments > kMaxN) return MOE_ERR_UNSUPPORTED;
+  if (!xp || !offsets || !W1 || !W3 || !W2 || !op || !ws) return MOE_ERR_NULL;
+  if (!aligned16(xp) || !aligned16(W1) || !aligned16(W3) || !aligned16(W2) || !aligned16(op) ||
+      !aligned16(ws))
+    return MOE_ERR_ALIGN;
+  if (ws_bytes < moe_ffn_workspace_size(rows_max, f, cfg->dtype)) return MOE_ERR_WORKSPACE;
+  int32_t* status = static_cast<int32_t*>(ws);
+  void* hp = static_cast<unsigned char*>(ws) + 256;
+  return run_ffn(cfg->dtype, xp, offsets, n_segments, rows_max, cfg->d, f, W1, W3, W2, hp, op,
+                 status, as_stream(stream));
+}
+
+int moe_grouped_gemm(int32_t dtype, const void* A, const int32_t* offsets, int32_t n_segments,
+                     int64_t rows_max, int32_t K, int32_t n_out, const void* B, void* out,
+                     void* ws, size_t ws_bytes, void* stream) {
+  if (dtype != MOE_BF16 && dtype != MOE_F32) return MOE_ERR_SHAPE;
+  if (K <= 0 || n_out <= 0 || n_segments < 0 || rows_max < 0) return MOE_ERR_SHAPE;
+  if (dtype == MOE_BF16 && (K % 64 || n_out % 64)) return MOE_ERR_SHAPE;
+  if (n_segments > kMaxN) return MOE_ERR_UNSUPPORTED;
+  if (!A || !offsets || !B || !out || !ws) return MOE_ERR_NULL;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(out) || !aligned16(ws)) return MOE_ERR_ALIGN;
+  if (ws_bytes < moe_ffn_workspace_size(0, 0, dtype)) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = as_stream(stream);
+  cudaError_t e;
+  if (dtype == MOE_BF16)
+    e = launch_grouped_gemm_tc_bf16(A, offsets, n_segments, rows_max, K, n_out, B, nullptr, out,
+                                    false, static_cast<int32_t*>(ws), s);
+  else
+    e = launch_grouped_gemm_simt_f32(static_cast<const float*>(A), offsets, n_segments, rows_max,
+                                     K, n_out, static_cast<const float*>(B), nullptr,
+                                     static_cast<float*>(out), false, s);
+  return status_from(e);
+}
+
+int moe_combine(const moe_config* cfg, const void* op, const float* row_gate,
+                const int32_t* tok_rows, const void* shared_out, void* y, void* stream) {
+  Derived d;
+  int st = validate(cfg, &d);
+  if (st != MOE_OK) return st;
+  if (!op || !row_gate || !tok_rows || !y) return MOE_ERR_NULL;
+  if (!aligned16(op) || !aligned16(y) || (shared_out && !aligned16(shared_out)))
+    return MOE_ERR_ALIGN;
+  return status_from(launch_combine(cfg->dtype, op, row_gate, tok_rows, shared_out, y, cfg->T,
+                                    cfg->d, d.kc, d.rows_max, as_stream(stream)));
+}
+
+int moe_load_stats(const moe_config* cfg, const int32_t* demand, const int32_t* kept,
+                   const float* scores, double* stats, void* ws, size_t ws_bytes, void* stream) {
+  Derived d;
+  int st = validate(cfg, &d);
+  if (st != MOE_OK) return st;
+  if (!demand || !kept || !scores || !stats || !ws) return MOE_ERR_NULL;
+  if (ws_bytes < stats_partial_doubles(cfg->T, cfg->N) * 8) return MOE_ERR_WORKSPACE;
+  return status_from(launch_stats(demand, kept, scores, cfg->T, cfg->N, static_cast<double*>(ws),
+                                  stats, as_stream(stream)));
+}
+
+int moe_layer_forward(const moe_config* cfg, const void* x, const void* W_router,
+                      const float* bias, const void* W1, const void* W3, const void* W2,
+                      const void* Ws1, const void* Ws3, const void* Ws2,
+                      const int32_t* home_group, float* logits, void* y, double* stats, void* ws,
+                      size_t ws_bytes, void* stream) {
+  Derived d;
+  int st = validate(cfg, &d);
+  if (st != MOE_OK) return st;
+  const moe_config& c = *cfg;
+  const bool given = (c.flags & MOE_LOGITS_GIVEN) != 0;
+  if (!x || !W1 || !W3 || !W2 || !y || !ws) return MOE_ERR_NULL;
+  if (given ? !logits : !W_router) return MOE_ERR_NULL;
+  if (c.f_shared > 0 && (!Ws1 || !Ws3 || !Ws2)) return MOE_ERR_NULL;
+  if (!aligned16(x) || !aligned16(W1) || !aligned16(W3) || !aligned16(W2) || !aligned16(y) ||
+      (reinterpret_cast<uintptr_t>(ws) & 255u) || (!given && !aligned16(W_router)))
+    return MOE_ERR_ALIGN;
+  if (c.f_shared > 0 && (!aligned16(Ws1) || !aligned16(Ws3) || !aligned16(Ws2))) return MOE_ERR_ALIGN;
+  const Layout L = layout(c, d);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+
+  cudaStream_t s = as_stream(stream);
+  int32_t* status = at<int32_t>(ws, L.status);
+  float* Lg = given ? logits : (logits ? logits : at<float>(ws, L.logits));
+  float* scores = at<float>(ws, L.scores);
+  int32_t* cand_idx = at<int32_t>(ws, L.cand_idx);
+  float* cand_gate = at<float>(ws, L.cand_gate);
+  int32_t* slot = at<int32_t>(ws, L.slot);
+  uint8_t* keep = at<uint8_t>(ws, L.keep);
+  int32_t* demand = at<int32_t>(ws, L.demand);
+  int32_t* kept = at<int32_t>(ws, L.kept);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* row_token = at<int32_t>(ws, L.row_token);
+  float* row_gate = at<float>(ws, L.row_gate);
+  int32_t* tok_rows = at<int32_t>(ws, L.tok_rows);
+  void* xp = at<void>(ws, L.xp);
+  void* hp = at<void>(ws, L.hp);
+  void* op = at<void>(ws, L.op);
+  void* ys = c.f_shared > 0 ? at<void>(ws, L.shared_out) : nullptr;
+
+  if (!given && launch_router_logits(c.dtype, x, W_router, bias, Lg, c.T, c.d, c.N, s) != cudaSuccess)
+    return MOE_ERR_LAUNCH;
+  if (launch_route_tokens(Lg, scores, cand_idx, cand_gate, home_group, c.T, c.N, c.k, c.m,
+                          c.group_size, c.renorm, d.ec ? 1 : 0, s) != cudaSuccess)
+    return MOE_ERR_LAUNCH;
+  if (launch_select(cand_idx, cand_gate, c.T, d.kc, c.N, d.ec ? 1 : 0, d.cap, slot, keep, demand,
+                    kept, s) != cudaSuccess)
+    return MOE_ERR_LAUNCH;
+  if (launch_dispatch(c.dtype, x, cand_idx, cand_gate, slot, kept, c.T, c.d, c.N, d.kc,
+                      d.ec ? 1 : 0, d.rows_max, offsets, row_token, row_gate, tok_rows, xp,
+                      s) != cudaSuccess)
+    return MOE_ERR_LAUNCH;
+  st = run_ffn(c.dtype, xp, offsets, c.N, d.rows_max, c.d, c.f, W1, W3, W2, hp, op, status, s);
+  if (st != MOE_OK) return st;
+  if (c.f_shared > 0 && c.T > 0) {
+    int32_t* soff = at<int32_t>(ws, L.shared_offsets);
+    write_pair_kernel<<<1, 1, 0, s>>>(soff, 0, c.T);
+    st = run_ffn(c.dtype, x, soff, 1, c.T, c.d, c.f_shared, Ws1, Ws3, Ws2, hp, ys, status, s);
+    if (st != MOE_OK) return st;
+  }
+  if (launch_combine(c.dtype, op, row_gate, tok_rows, ys, y, c.T, c.d, d.kc, d.rows_max, s) !=
+      cudaSuccess)
+    return MOE_ERR_LAUNCH;
+  if (stats) {
+    if (launch_stats(demand, kept, scores, c.T, c.N, at<double>(ws, L.stats_partial), stats, s) !=
+        cudaSuccess)
+      return MOE_ERR_LAUNCH;
+  }
+  return MOE_OK;
+}
+
+int moe_workspace_views(const moe_config* cfg, void* ws, moe_views_t* out) {
+  Derived d;
+  int st = validate(cfg, &d);
+  if (st != MOE_OK) return st;
+  if (!ws || !out) return MOE_ERR_NULL;
+  const Layout L = layout(*cfg, d);
+  out->status = at<int32_t>(ws, L.status);
+  out->logits = at<float>(ws, L.logits);
+  out->scores = at<float>(ws, L.scores);
+  out->cand_idx = at<int32_t>(ws, L.cand_idx);
+  out->cand_gate = at<float>(ws, L.cand_gate);
+  out->slot = at<int32_t>(ws, L.slot);
+  out->keep = at<uint8_t>(ws, L.keep);
+  out->demand = at<int32_t>(ws, L.demand);
+  out->kept = at<int32_t>(ws, L.kept);
+  out->expert_offsets = at<int32_t>(ws, L.offsets);
+  out->row_token = at<int32_t>(ws, L.row_token);
+  out->row_gate = at<float>(ws, L.row_gate);
+  out->tok_rows = at<int32_t>(ws, L.tok_rows);
+  out->xp = at<void>(ws, L.xp);
+  out->op = at<void>(ws, L.op);
+  out->shared_out = cfg->f_shared > 0 ? at<void>(ws, L.shared_out) : nullptr;
+  return MOE_OK;
+}
+
+int moe_get_device_status(const void* ws, void* stream, int32_t* out_host) {
+  if (!ws || !out_host) return MOE_ERR_NULL;
+  cudaStream_t s = as_stream(stream);
+  int32_t v = MOE_OK;
+  cudaError_t e = cudaMemcpyAsync(&v, ws, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) *out_host = v;
+  return status_from(e);
+}
+
+int moe_clear_device_status(void* ws, void* stream) {
+  if (!ws) return MOE_ERR_NULL;
+  clear_status_kernel<<<1, 1, 0, as_stream(stream)>>>(static_cast<int32_t*>(ws));
+  return status_from(cudaGetLastError());
+}
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_NULL: return "a required pointer is NULL";
+    case MOE_ERR_SHAPE: return "a size is out of range or inconsistent";
+    case MOE_ERR_ALIGN: return "a pointer breaks the 16-byte alignment rule";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_UNSUPPORTED: return "configuration outside the implemented limits";
+    case MOE_ERR_LAUNCH: return "the CUDA runtime refused a launch";
+    case MOE_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait expired";
+    case MOE_ERR_DEVICE_BOUNDS: return "a kernel saw an index outside its buffer";
+    default: return "unknown status";
+  }
+}
+
+void moe_release_caches(void) {}  // tensor maps are encoded per call; nothing is cached
+
+}  // extern "C"

@@ -1,0 +1,132 @@
+"""The C ABI library: loads, exports every entry point of include/moe.h, sizes
+its buffers as the capacity formulas say, and rejects bad arguments on the
+host before any CUDA call (so these run without a GPU)."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+import moe_workloads as W
+import oracle as O
+import routing_capacity_drop_router_b300 as M
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|void|const char\*)\s+(moe_\w+)\s*\(", src,
+                                 flags=re.M)))
+
+
+def test_library_exports_every_declared_entry_point():
+    names = _declared_functions()
+    assert len(names) >= 16
+    lib = M.lib()
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(M.SIGNATURES), "binding and header disagree"
+
+
+def test_struct_layout_matches_header():
+    assert ctypes.sizeof(M.moe_config) == 56
+    assert M.moe_config.gamma.offset == 24
+    assert ctypes.sizeof(M.moe_sizes_t) == 32
+    assert ctypes.sizeof(M.moe_views_t) == 16 * 8
+
+
+@pytest.mark.parametrize("w", list(W.ALL.values()), ids=list(W.ALL))
+def test_sizes_follow_capacity_formulas(w):
+    s = M.sizes(M.config_from_workload(w))
+    if w.mode == W.EXPERT_CHOICE:
+        c = O.ec_capacity(w.k, w.T, w.N)
+        assert (s.kc, s.capacity, s.rows_max) == (w.N, c, w.N * c)
+    elif w.mode == W.CAPACITY_DROP:
+        C = O.capacity(w.gamma, w.k, w.T, w.N)
+        assert (s.kc, s.capacity) == (w.k + w.m, C)
+        assert s.rows_max == min(w.T * (w.k + w.m), w.N * C)
+    else:
+        assert (s.kc, s.capacity, s.rows_max) == (w.k + w.m, w.T, w.T * (w.k + w.m))
+    assert s.workspace > 0 and M.workspace_size(M.config_from_workload(w)) == s.workspace
+
+
+def test_workload_capacities_match_the_pages_formulas():
+    assert M.sizes(M.config_from_workload(W.mixtral(1.0))).capacity == 1024
+    assert M.sizes(M.config_from_workload(W.mixtral(1.5))).capacity == 1536
+    assert M.sizes(M.config_from_workload(W.FINE_BF16)).capacity == 960
+    assert M.sizes(M.config_from_workload(W.EC_BF16)).capacity == 256
+
+
+def _cfg(**kw):
+    base = dict(T=64, d=128, N=8, f=128, k=2)
+    base.update(kw)
+    return M.make_config(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(N=0), M.MOE_ERR_SHAPE),
+    (dict(k=9), M.MOE_ERR_SHAPE),
+    (dict(d=100), M.MOE_ERR_SHAPE),               # bf16 needs d % 64 == 0
+    (dict(f=96), M.MOE_ERR_SHAPE),
+    (dict(N=300, k=2), M.MOE_ERR_UNSUPPORTED),
+    (dict(T=100000), M.MOE_ERR_UNSUPPORTED),
+    (dict(N=64, k=20, m=20, group_size=8), M.MOE_ERR_UNSUPPORTED),
+    (dict(gamma=float("nan"), mode="capacity_drop"), M.MOE_ERR_SHAPE),
+    (dict(gamma=-1.0, mode="capacity_drop"), M.MOE_ERR_SHAPE),
+    (dict(m=2, group_size=3), M.MOE_ERR_SHAPE),
+    (dict(mode=7), M.MOE_ERR_SHAPE),
+    (dict(dtype=5), M.MOE_ERR_SHAPE),
+])
+def test_invalid_configs_are_rejected(kw, code):
+    cfg = _cfg(**kw)
+    out = M.moe_sizes_t()
+    assert M.lib().moe_sizes(ctypes.byref(cfg), ctypes.byref(out)) == code
+    assert M.lib().moe_workspace_size(ctypes.byref(cfg)) == 0
+
+
+def test_null_pointers_rejected_before_any_launch():
+    lib = M.lib()
+    cfg = _cfg()
+    r = ctypes.byref(cfg)
+    assert lib.moe_route(r, None, None, None, None, None, None, None, None, None) == M.MOE_ERR_NULL
+    assert lib.moe_capacity_drop(r, None, None, None, None, None, None, None) == M.MOE_ERR_NULL
+    assert lib.moe_dispatch(r, *([None] * 10), None) == M.MOE_ERR_NULL
+    assert lib.moe_combine(r, None, None, None, None, None, None) == M.MOE_ERR_NULL
+    assert lib.moe_layer_forward(r, *([None] * 14), 0, None) == M.MOE_ERR_NULL
+    assert lib.moe_expert_ffn(r, None, None, 8, 64, 128, None, None, None, None, None, 0,
+                              None) == M.MOE_ERR_NULL
+    assert lib.moe_load_stats(r, None, None, None, None, None, 0, None) == M.MOE_ERR_NULL
+    assert lib.moe_get_device_status(None, None, None) == M.MOE_ERR_NULL
+    assert lib.moe_route(None, *([None] * 9)) == M.MOE_ERR_NULL
+
+
+def test_misaligned_and_small_workspace_rejected_before_any_launch():
+    lib = M.lib()
+    cfg = _cfg()
+    r = ctypes.byref(cfg)
+    fake = 0x10000  # never dereferenced: the checks fail first
+    ptrs = [fake] * 6
+    # x misaligned
+    assert lib.moe_layer_forward(r, fake + 2, fake, None, fake, fake, fake, None, None, None, None,
+                                 None, fake, None, fake, 1 << 40, None) == M.MOE_ERR_ALIGN
+    # workspace below moe_workspace_size
+    need = lib.moe_workspace_size(r)
+    assert lib.moe_layer_forward(r, fake, fake, None, fake, fake, fake, None, None, None, None,
+                                 None, fake, None, fake, need - 1, None) == M.MOE_ERR_WORKSPACE
+    # given logits flag without logits
+    cfg2 = _cfg(logits_given=True)
+    assert lib.moe_layer_forward(ctypes.byref(cfg2), fake, None, None, fake, fake, fake, None, None,
+                                 None, None, None, fake, None, fake, need, None) == M.MOE_ERR_NULL
+    assert lib.moe_expert_ffn(r, fake, fake, 8, 64, 128, *ptrs[:4], fake, 10, None) == \
+        M.MOE_ERR_WORKSPACE
+    assert lib.moe_grouped_gemm(M.MOE_BF16, fake, fake, 8, 64, 100, 128, fake, fake, fake, 1 << 20,
+                                None) == M.MOE_ERR_SHAPE
+
+
+def test_status_strings():
+    for code in range(-8, 1):
+        assert M.status_string(code) and M.status_string(code) != "unknown status"
+    assert M.status_string(-99) == "unknown status"

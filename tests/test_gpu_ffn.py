@@ -1,0 +1,109 @@
+"""GPU grouped expert GEMMs: the tcgen05 bf16 kernels against torch matmul and
+the oracle's SwiGLU expert, the fp32 FMA kernels against the oracle at 1e-5,
+over ragged segments (empty, one-row, several 128-row tiles, partial n-tiles)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from tests import gpu_util as G
+
+M = G.M
+pytestmark = pytest.mark.gpu
+
+
+def _segments(sizes):
+    off = np.zeros(len(sizes) + 1, dtype=np.int32)
+    off[1:] = np.cumsum(sizes)
+    return off
+
+
+def _rand(shape, seed, scale=1.0, dtype=torch.bfloat16):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(shape, generator=g) * scale).to(dtype)
+
+
+@pytest.mark.parametrize("sizes,K,n_out", [
+    ([130, 0, 170, 1, 249], 256, 320),
+    ([128], 128, 256),
+    ([3, 500, 64, 0, 0, 257], 512, 512),
+    ([1000], 1024, 192),
+])
+def test_grouped_gemm_bf16_against_torch(sizes, K, n_out):
+    S = len(sizes)
+    off = _segments(sizes)
+    P = int(off[-1])
+    rows_max = P + 37
+    A = _rand((rows_max, K), 1)
+    B = _rand((S, K, n_out), 2, K ** -0.5)
+    dev = torch.device("cuda")
+    out = torch.full((rows_max, n_out), 7.0, dtype=torch.bfloat16, device=dev)
+    ws = torch.zeros(M.ffn_workspace_size(0, 0, "bf16"), dtype=torch.uint8, device=dev)
+    M.moe_grouped_gemm("bf16", A.cuda(), torch.from_numpy(off).cuda(), S, rows_max, K, n_out,
+                       B.cuda(), out, ws)
+    torch.cuda.synchronize()
+    assert M.moe_get_device_status(ws) == M.MOE_OK
+    got = out.float().cpu()
+    for s in range(S):
+        a, b = int(off[s]), int(off[s + 1])
+        if a == b:
+            continue
+        ref = A[a:b].double() @ B[s].double()
+        G.assert_output_close(got[a:b].numpy(), ref.numpy(), "bf16", f"segment {s}")
+    assert torch.all(got[P:] == 7.0), "rows past the last segment were written"
+
+
+@pytest.mark.parametrize("sizes,d,f", [
+    ([130, 0, 170, 1, 249], 256, 384),
+    ([300, 300], 320, 128),
+    ([77], 2048, 1408),
+])
+def test_expert_ffn_bf16_against_oracle(sizes, d, f):
+    S = len(sizes)
+    off = _segments(sizes)
+    P = int(off[-1])
+    rows_max = P + 5
+    xp = _rand((rows_max, d), 3)
+    W1 = _rand((S, d, f), 4, d ** -0.5)
+    W3 = _rand((S, d, f), 5, d ** -0.5)
+    W2 = _rand((S, f, d), 6, f ** -0.5)
+    cfg = M.make_config(T=1, d=d, N=S, f=f, k=1, dtype="bf16")
+    dev = torch.device("cuda")
+    op = torch.zeros((rows_max, d), dtype=torch.bfloat16, device=dev)
+    ws = torch.zeros(M.ffn_workspace_size(rows_max, f, "bf16"), dtype=torch.uint8, device=dev)
+    M.moe_expert_ffn(cfg, xp.cuda(), torch.from_numpy(off).cuda(), S, rows_max, f, W1.cuda(),
+                     W3.cuda(), W2.cuda(), op, ws)
+    torch.cuda.synchronize()
+    assert M.moe_get_device_status(ws) == M.MOE_OK
+    got = op.float().cpu().numpy()
+    for s in range(S):
+        a, b = int(off[s]), int(off[s + 1])
+        if a == b:
+            continue
+        ref = O.swiglu(G.np32(xp[a:b]), G.np32(W1[s]), G.np32(W3[s]), G.np32(W2[s]), "bf16")
+        G.assert_output_close(got[a:b], ref, "bf16", f"segment {s}")
+
+
+@pytest.mark.parametrize("sizes,d,f", [([100, 0, 37, 64], 128, 256), ([5], 64, 200)])
+def test_expert_ffn_f32_against_oracle(sizes, d, f):
+    S = len(sizes)
+    off = _segments(sizes)
+    P = int(off[-1])
+    xp = _rand((P, d), 7, dtype=torch.float32)
+    W1 = _rand((S, d, f), 8, d ** -0.5, torch.float32)
+    W3 = _rand((S, d, f), 9, d ** -0.5, torch.float32)
+    W2 = _rand((S, f, d), 10, f ** -0.5, torch.float32)
+    cfg = M.make_config(T=1, d=d, N=S, f=f, k=1, dtype="f32")
+    dev = torch.device("cuda")
+    op = torch.zeros((P, d), dtype=torch.float32, device=dev)
+    ws = torch.zeros(M.ffn_workspace_size(P, f, "f32"), dtype=torch.uint8, device=dev)
+    M.moe_expert_ffn(cfg, xp.cuda(), torch.from_numpy(off).cuda(), S, P, f, W1.cuda(), W3.cuda(),
+                     W2.cuda(), op, ws)
+    torch.cuda.synchronize()
+    got = op.cpu().numpy()
+    for s in range(S):
+        a, b = int(off[s]), int(off[s + 1])
+        if a == b:
+            continue
+        ref = O.swiglu(xp[a:b].numpy(), W1[s].numpy(), W3[s].numpy(), W2[s].numpy(), "f32")
+        G.assert_output_close(got[a:b], ref, "f32", f"segment {s}")

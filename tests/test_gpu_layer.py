@@ -1,0 +1,110 @@
+"""Whole-layer GPU parity (moe_layer_forward) against the oracle.
+
+Small shapes run every token through the oracle; they span several 128-row
+tiles with ragged tails. The benchmark workloads run at full size with the
+oracle computing a sample of tokens (a token's output depends only on its own
+routing, which the oracle computes for the whole batch), in the launch
+configuration the benchmark times."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import moe_workloads as W
+import oracle as O
+from tests import gpu_util as G
+
+pytestmark = pytest.mark.gpu
+
+SMALL = [
+    W.Workload("small_tc", T=600, d=256, N=8, f=384, k=2),
+    W.Workload("small_drop_renorm", T=600, d=256, N=8, f=384, k=2, mode=W.CAPACITY_DROP,
+               gamma=1.0, renorm=True, zipf_s=1.2),
+    W.Workload("small_ec", T=640, d=192, N=8, f=256, k=2, mode=W.EXPERT_CHOICE),
+    W.Workload("small_expanded_shared", T=500, d=128, N=16, f=128, k=3, mode=W.CAPACITY_DROP,
+               gamma=1.25, m=2, group_size=4, f_shared=192, zipf_s=1.0),
+    W.Workload("small_f32", T=300, d=64, N=4, f=96, k=2, dtype="f32", mode=W.CAPACITY_DROP,
+               gamma=1.0),
+]
+
+
+def _check_layer(w, inp, tokens=None):
+    # 1) both sides given the oracle's fp32 logits: routing identical, y within tolerance
+    L = O.router_logits(G.np32(inp["x"]), G.np32(inp["W_r"]), G.np32(inp["bias"]))
+    ref = G.oracle_layer(w, inp, logits=L, tokens=tokens)
+    got = G.layer_gpu(w, inp, logits=L, want_views=True)
+    assert np.array_equal(got["kept"], ref["kept"])
+    assert np.array_equal(got["keep"].astype(bool), ref["keep"])
+    rows = ref["tokens"]
+    G.assert_output_close(got["y"][rows], ref["y"], w.dtype)
+    s = O.load_stats(ref["demand"], ref["kept"], ref["p"])
+    want = [s["P"], s["demand_total"], s["max_kept"], s["mean_kept"], s["max_over_mean"],
+            s["drop_fraction"], s["balance"], s["balance_times_N"]]
+    assert np.allclose(got["stats"], want, rtol=1e-5, atol=1e-9)
+    return L, ref, got
+
+
+def _check_own_logits(w, inp, L, ref, tokens=None):
+    # 2) the GPU computes its own logits: within the fp32 bound of the oracle's;
+    # tokens whose routing is unchanged match the oracle's output
+    got = G.layer_gpu(w, inp, want_views=True)
+    bound = G.logit_bound(G.np32(inp["x"]), G.np32(inp["W_r"]), L)
+    assert np.all(np.abs(got["logits"].astype(np.float64) - L) <= bound)
+    rows = ref["tokens"]
+    same = np.all(got["keep"].astype(bool)[rows] == ref["keep"][rows], axis=1)
+    if w.mode != W.EXPERT_CHOICE:
+        same &= np.all(got["cand_idx"][rows] == ref["idx"][rows], axis=1)
+    assert same.mean() >= 0.99, f"{(~same).sum()} of {len(rows)} tokens routed differently"
+    G.assert_output_close(got["y"][rows][same], ref["y"][same], w.dtype)
+
+
+@pytest.mark.parametrize("w", SMALL, ids=[w.name for w in SMALL])
+def test_small_layer_parity(w):
+    inp = W.make_inputs(w)
+    L, ref, _ = _check_layer(w, inp)
+    _check_own_logits(w, inp, L, ref)
+
+
+def test_tiny_fp32_workload_full():
+    w = W.TINY_F32
+    inp = W.make_inputs(w)
+    L, ref, _ = _check_layer(w, inp)
+    _check_own_logits(w, inp, L, ref)
+
+
+def test_capacity_zero_outputs_zero():
+    w = W.Workload("zero_cap", T=200, d=128, N=8, f=128, k=2, mode=W.CAPACITY_DROP, gamma=0.0)
+    inp = W.make_inputs(w)
+    got = G.layer_gpu(w, inp)
+    assert np.all(got["y"] == 0)
+    assert got["stats"][0] == 0 and got["stats"][5] == 1.0
+
+
+def test_gamma_inf_equals_token_choice_bitwise():
+    w_tc = W.Workload("tc", T=400, d=128, N=8, f=128, k=2, renorm=True)
+    w_drop = w_tc.replace(name="drop_inf", mode=W.CAPACITY_DROP, gamma=math.inf)
+    inp = W.make_inputs(w_tc)
+    a = G.layer_gpu(w_tc, inp)
+    b = G.layer_gpu(w_drop, inp)
+    assert np.array_equal(a["y"], b["y"])
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,sample", [
+    ("expert_choice_bf16", None),
+    ("decode_bf16", None),
+    ("mixtral_bf16_gamma1", 48),
+    ("mixtral_bf16", 32),
+    ("finegrained_bf16", 64),
+    ("finegrained_bf16_expanded", 64),
+])
+def test_benchmark_workloads_full_size(name, sample):
+    w = W.ALL[name]
+    inp = W.make_inputs(w)
+    tokens = None
+    if sample is not None:
+        rng = np.random.default_rng(0)
+        tokens = np.sort(rng.choice(w.T, size=sample, replace=False))
+    L, ref, _ = _check_layer(w, inp, tokens=tokens)
+    _check_own_logits(w, inp, L, ref, tokens=tokens)

@@ -1,0 +1,101 @@
+"""GPU routing parity: scores, top-k / expanded candidates, gates, per-expert
+selection (capacity drop, expert choice), offsets, row maps and token rows
+must equal the oracle's bit for bit when both get the same fp32 logits; the
+GPU's own router logits must sit within the fp32 accumulation bound."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import moe_workloads as W
+import oracle as O
+from tests import gpu_util as G
+
+pytestmark = pytest.mark.gpu
+
+
+def _logits_of(w):
+    inp = W.make_inputs(w, with_experts=False)
+    L = O.router_logits(G.np32(inp["x"]), G.np32(inp["W_r"]), G.np32(inp["bias"]))
+    return inp, L
+
+
+@pytest.mark.parametrize("name", list(W.ALL))
+def test_routing_bit_exact_on_every_workload(name):
+    w = W.ALL[name]
+    inp, L = _logits_of(w)
+    g = G.gpu_routing(w, torch.from_numpy(L), x=inp["x"])
+    G.compare_routing(w, g, L)
+    # the gather: every used row of xp is its token's row of x, bitwise
+    P = int(g["expert_offsets"][-1])
+    xp = g["xp"][:P]
+    assert torch.equal(xp, inp["x"][torch.from_numpy(g["row_token"][:P]).long()])
+
+
+SMALL = [
+    W.Workload("tc_ties", T=1000, d=64, N=16, f=64, k=4),
+    W.Workload("drop_ties", T=1000, d=64, N=16, f=64, k=4, mode=W.CAPACITY_DROP, gamma=1.0),
+    W.Workload("drop_renorm_ties", T=777, d=64, N=8, f=64, k=2, mode=W.CAPACITY_DROP,
+               gamma=0.75, renorm=True),
+    W.Workload("ec_ties", T=999, d=64, N=16, f=64, k=3, mode=W.EXPERT_CHOICE),
+    W.Workload("expanded_ties", T=1001, d=64, N=32, f=64, k=3, mode=W.CAPACITY_DROP, gamma=1.0,
+               m=3, group_size=4),
+    W.Workload("drop_zero_capacity", T=100, d=64, N=8, f=64, k=2, mode=W.CAPACITY_DROP, gamma=0.0),
+    W.Workload("ec_c_equals_T", T=64, d=64, N=4, f=64, k=4, mode=W.EXPERT_CHOICE),
+    W.Workload("one_expert", T=300, d=64, N=1, f=64, k=1),
+    W.Workload("many_experts", T=513, d=64, N=256, f=64, k=8, mode=W.CAPACITY_DROP, gamma=1.0),
+    W.Workload("ec_many_experts", T=300, d=64, N=64, f=64, k=2, mode=W.EXPERT_CHOICE),
+]
+
+
+@pytest.mark.parametrize("w", SMALL, ids=[w.name for w in SMALL])
+@pytest.mark.parametrize("quantum", [None, 0.25])
+def test_routing_bit_exact_with_ties_and_ragged_sizes(w, quantum):
+    L = W.random_logits(w.T, w.N, seed=3, scale=2.0, quantum=quantum)
+    g = G.gpu_routing(w, L)
+    G.compare_routing(w, g, L.numpy())
+
+
+def test_all_equal_logits_and_signed_zeros():
+    w = W.Workload("flat", T=257, d=64, N=8, f=64, k=3, mode=W.CAPACITY_DROP, gamma=1.0)
+    L = torch.zeros((w.T, w.N))
+    L[::2, ::3] = -0.0
+    g = G.gpu_routing(w, L)
+    G.compare_routing(w, g, L.numpy())
+    assert (g["cand_idx"] == np.array([0, 1, 2])).all()
+
+
+def test_given_home_groups():
+    w = W.Workload("home", T=300, d=64, N=16, f=64, k=2, mode=W.CAPACITY_DROP, gamma=1.0, m=2,
+                   group_size=4)
+    L = W.random_logits(w.T, w.N, seed=5)
+    hg = torch.from_numpy(np.random.default_rng(5).integers(0, 4, size=w.T).astype(np.int32))
+    g = G.gpu_routing(w, L, home_group=hg)
+    G.compare_routing(w, g, L.numpy(), home_group=hg.numpy())
+
+
+def test_empty_batch():
+    w = W.Workload("empty", T=0, d=64, N=8, f=64, k=2, mode=W.CAPACITY_DROP, gamma=1.0)
+    g = G.gpu_routing(w, torch.zeros((0, 8)))
+    assert (g["demand"] == 0).all() and (g["kept"] == 0).all()
+    assert (g["expert_offsets"] == 0).all()
+
+
+@pytest.mark.parametrize("name", ["tiny_fp32", "expert_choice_bf16", "mixtral_bf16",
+                                  "finegrained_bf16", "decode_bf16"])
+def test_router_logits_within_fp32_bound(name):
+    w = W.ALL[name]
+    inp, L = _logits_of(w)
+    cfg = G.M.config_from_workload(w)
+    sz = G.M.sizes(cfg)
+    dev = torch.device("cuda")
+    Lg = torch.empty((w.T, w.N), dtype=torch.float32, device=dev)
+    idx = torch.empty((w.T, sz.kc), dtype=torch.int32, device=dev)
+    gate = torch.empty((w.T, sz.kc), dtype=torch.float32, device=dev)
+    G.M.moe_route(cfg, G.cuda(inp["x"]), G.cuda(inp["W_r"]), G.cuda(inp["bias"]), Lg, None,
+                  None if w.mode == W.EXPERT_CHOICE else idx, gate)
+    torch.cuda.synchronize()
+    diff = np.abs(Lg.cpu().numpy().astype(np.float64) - L.astype(np.float64))
+    bound = G.logit_bound(G.np32(inp["x"]), G.np32(inp["W_r"]), L)
+    assert np.all(diff <= bound), float((diff / bound).max())
