@@ -162,7 +162,8 @@ int moe_route(const moe_config* cfg, const void* x, const void* W_router, const 
  *   slot      [T, kc] int32 out: for a kept slot, its rank among expert e's
  *             kept tokens in ascending token order; -1 for a dropped or empty slot
  *   keep      [T, kc] uint8 out, nullable: 1 kept, 0 not
- *   demand    [N] int32 out: candidates per expert before selection
+ *   demand    [N] int32 out: candidates per expert before selection (expert
+ *             choice: the c tokens the expert takes, since nothing is dropped)
  *   kept      [N] int32 out: pairs per expert after selection
  */
 int moe_capacity_drop(const moe_config* cfg, const int32_t* cand_idx, const float* cand_gate,

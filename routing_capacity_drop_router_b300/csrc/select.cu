@@ -186,8 +186,10 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
     }
   }
   if (threadIdx.x == 0) {
-    demand[e] = n_all;
-    kept[e] = n < cap ? n : (cap > 0 ? cap : 0);
+    const int k_e = n < cap ? n : (cap > 0 ? cap : 0);
+    // expert choice drops nothing: an expert's demand is the c tokens it takes
+    demand[e] = expert_choice ? k_e : n_all;
+    kept[e] = k_e;
   }
 }
 
