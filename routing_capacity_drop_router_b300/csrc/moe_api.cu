@@ -45,6 +45,10 @@ constexpr int kMaxSlots = 32;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// A buffer of `count` elements must be present unless it is empty (framework
+// tensors of size zero carry a NULL data pointer).
+bool have(const void* p, int64_t count) { return p != nullptr || count == 0; }
+
 int validate(const moe_config* c, Derived* dv) {
   if (!c) return MOE_ERR_NULL;
   if (c->T < 0 || c->d <= 0 || c->N <= 0 || c->f <= 0 || c->k <= 0) return MOE_ERR_SHAPE;
@@ -194,8 +198,10 @@ int moe_route(const moe_config* cfg, const void* x, const void* W_router, const 
   int st = validate(cfg, &d);
   if (st != MOE_OK) return st;
   const bool given = (cfg->flags & MOE_LOGITS_GIVEN) != 0;
-  if (!logits || !cand_gate || (!d.ec && !cand_idx)) return MOE_ERR_NULL;
-  if (!given && (!x || !W_router)) return MOE_ERR_NULL;
+  const int64_t T = cfg->T;
+  if (!have(logits, T) || !have(cand_gate, T) || (!d.ec && !have(cand_idx, T)))
+    return MOE_ERR_NULL;
+  if (!given && (!have(x, T) || !W_router)) return MOE_ERR_NULL;
   if (!given && (!aligned16(x) || !aligned16(W_router))) return MOE_ERR_ALIGN;
   cudaStream_t s = as_stream(stream);
   if (!given) {
@@ -213,7 +219,9 @@ int moe_capacity_drop(const moe_config* cfg, const int32_t* cand_idx, const floa
   Derived d;
   int st = validate(cfg, &d);
   if (st != MOE_OK) return st;
-  if (!cand_gate || !slot || !demand || !kept || (!d.ec && !cand_idx)) return MOE_ERR_NULL;
+  const int64_t T = cfg->T;
+  if (!have(cand_gate, T) || !have(slot, T) || !demand || !kept || (!d.ec && !have(cand_idx, T)))
+    return MOE_ERR_NULL;
   return status_from(launch_select(cand_idx, cand_gate, cfg->T, d.kc, cfg->N, d.ec ? 1 : 0, d.cap,
                                    slot, keep, demand, kept, as_stream(stream)));
 }
@@ -225,8 +233,10 @@ int moe_dispatch(const moe_config* cfg, const void* x, const int32_t* cand_idx,
   Derived d;
   int st = validate(cfg, &d);
   if (st != MOE_OK) return st;
-  if (!x || !cand_gate || !slot || !kept || !expert_offsets || !row_token || !row_gate ||
-      !tok_rows || !xp || (!d.ec && !cand_idx))
+  const int64_t T = cfg->T, R = d.rows_max;
+  if (!have(x, T) || !have(cand_gate, T) || !have(slot, T) || !kept || !expert_offsets ||
+      !have(row_token, R) || !have(row_gate, R) || !have(tok_rows, T) || !have(xp, R) ||
+      (!d.ec && !have(cand_idx, T)))
     return MOE_ERR_NULL;
   if (!aligned16(x) || !aligned16(xp)) return MOE_ERR_ALIGN;
   return status_from(launch_dispatch(cfg->dtype, x, cand_idx, cand_gate, slot, kept, cfg->T,
@@ -281,7 +291,8 @@ int moe_combine(const moe_config* cfg, const void* op, const float* row_gate,
   Derived d;
   int st = validate(cfg, &d);
   if (st != MOE_OK) return st;
-  if (!op || !row_gate || !tok_rows || !y) return MOE_ERR_NULL;
+  const int64_t T = cfg->T, R = d.rows_max;
+  if (!have(op, R) || !have(row_gate, R) || !have(tok_rows, T) || !have(y, T)) return MOE_ERR_NULL;
   if (!aligned16(op) || !aligned16(y) || (shared_out && !aligned16(shared_out)))
     return MOE_ERR_ALIGN;
   return status_from(launch_combine(cfg->dtype, op, row_gate, tok_rows, shared_out, y, cfg->T,
@@ -293,7 +304,7 @@ int moe_load_stats(const moe_config* cfg, const int32_t* demand, const int32_t* 
   Derived d;
   int st = validate(cfg, &d);
   if (st != MOE_OK) return st;
-  if (!demand || !kept || !scores || !stats || !ws) return MOE_ERR_NULL;
+  if (!demand || !kept || !have(scores, cfg->T) || !stats || !ws) return MOE_ERR_NULL;
   if (ws_bytes < stats_partial_doubles(cfg->T, cfg->N) * 8) return MOE_ERR_WORKSPACE;
   return status_from(launch_stats(demand, kept, scores, cfg->T, cfg->N, static_cast<double*>(ws),
                                   stats, as_stream(stream)));
@@ -309,8 +320,8 @@ int moe_layer_forward(const moe_config* cfg, const void* x, const void* W_router
   if (st != MOE_OK) return st;
   const moe_config& c = *cfg;
   const bool given = (c.flags & MOE_LOGITS_GIVEN) != 0;
-  if (!x || !W1 || !W3 || !W2 || !y || !ws) return MOE_ERR_NULL;
-  if (given ? !logits : !W_router) return MOE_ERR_NULL;
+  if (!have(x, c.T) || !W1 || !W3 || !W2 || !have(y, c.T) || !ws) return MOE_ERR_NULL;
+  if (given ? !have(logits, c.T) : !W_router) return MOE_ERR_NULL;
   if (c.f_shared > 0 && (!Ws1 || !Ws3 || !Ws2)) return MOE_ERR_NULL;
   if (!aligned16(x) || !aligned16(W1) || !aligned16(W3) || !aligned16(W2) || !aligned16(y) ||
       (reinterpret_cast<uintptr_t>(ws) & 255u) || (!given && !aligned16(W_router)))
