@@ -216,6 +216,37 @@ int moe_expert_ffn(const moe_config* cfg, const void* xp, const int32_t* offsets
                    void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * moe_expert_ffn for callers that cannot allocate device memory. The source
+ * pages have no counterpart: this is an integration convenience, not part of
+ * the method.
+ *
+ * Who needs it: a host framework that owns every device buffer and hands an
+ * operator only its inputs and outputs (no workspace), or a latency-critical
+ * loop where cudaMalloc, which may synchronise the device, is not allowed.
+ * Same computation and arguments as moe_expert_ffn minus the workspace: the
+ * SwiGLU hidden activations live in a library-owned static device array of
+ * MOE_NOALLOC_SCRATCH_BYTES bytes that every GPU loading this library holds
+ * until the process exits. The call allocates and frees nothing.
+ *
+ *   rows_max * f * sizeof(dtype) must not exceed MOE_NOALLOC_SCRATCH_BYTES - 256,
+ *            otherwise MOE_ERR_WORKSPACE is returned and nothing is enqueued
+ *            (e.g. bf16 with f = 14336 fits up to 2340 rows).
+ *   device_status [1] int32 nullable, device: cleared to 0 by the call, then
+ *            receives MOE_ERR_DEVICE_TIMEOUT if a bounded wait expires; NULL
+ *            uses a word inside the library's array.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture. Every call on a device shares the one array:
+ * calls whose work overlaps on the GPU (different streams, or host threads
+ * without ordering) race on it and must be serialised by the caller.
+ */
+#define MOE_NOALLOC_SCRATCH_BYTES (64u << 20)
+int moe_expert_ffn_noalloc(const moe_config* cfg, const void* xp, const int32_t* offsets,
+                           int32_t n_segments, int64_t rows_max, int32_t f, const void* W1,
+                           const void* W3, const void* W2, void* op, int32_t* device_status,
+                           void* stream);
+
+/*
  * One grouped GEMM, out[r] = A[r] B[s] for rows r of segment s, the second
  * half of the expert FFN on its own. A [rows_max, K], B [n_segments, K, n_out],
  * out [rows_max, n_out], all dtype; K and n_out multiples of 64 (bf16).

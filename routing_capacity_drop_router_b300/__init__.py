@@ -34,6 +34,7 @@ MOE_F32 = 0
 MOE_BF16 = 1
 MOE_LOGITS_GIVEN = 1
 MOE_STATS_LEN = 8
+MOE_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 MODES = {"token_choice": MOE_TOKEN_CHOICE, "expert_choice": MOE_EXPERT_CHOICE,
          "capacity_drop": MOE_CAPACITY_DROP}
@@ -80,6 +81,8 @@ SIGNATURES = {
     "moe_expert_ffn": (ctypes.c_int, [_CFG, _VP, _VP, ctypes.c_int32, ctypes.c_int64,
                                       ctypes.c_int32, _VP, _VP, _VP, _VP, _VP, ctypes.c_size_t,
                                       _VP]),
+    "moe_expert_ffn_noalloc": (ctypes.c_int, [_CFG, _VP, _VP, ctypes.c_int32, ctypes.c_int64,
+                                              ctypes.c_int32, _VP, _VP, _VP, _VP, _VP, _VP]),
     "moe_grouped_gemm": (ctypes.c_int, [ctypes.c_int32, _VP, _VP, ctypes.c_int32, ctypes.c_int64,
                                         ctypes.c_int32, ctypes.c_int32, _VP, _VP, _VP,
                                         ctypes.c_size_t, _VP]),
@@ -200,6 +203,18 @@ def moe_expert_ffn(cfg, xp, offsets, n_segments, rows_max, f, W1, W3, W2, op, ws
     _check(lib().moe_expert_ffn(ctypes.byref(cfg), _p(xp), _p(offsets), n_segments, rows_max, f,
                                 _p(W1), _p(W3), _p(W2), _p(op), _p(ws), ws.numel() * ws.element_size(),
                                 _stream(stream)), "moe_expert_ffn")
+
+
+def moe_expert_ffn_noalloc(cfg, xp, offsets, n_segments, rows_max, f, W1, W3, W2, op,
+                           device_status=None, stream=None) -> None:
+    """moe_expert_ffn without a workspace, for callers that cannot allocate
+    device memory (the library keeps the hidden activations in its own
+    MOE_NOALLOC_SCRATCH_BYTES device array; calls that overlap on the GPU
+    race on it)."""
+    _check(lib().moe_expert_ffn_noalloc(ctypes.byref(cfg), _p(xp), _p(offsets), n_segments,
+                                        rows_max, f, _p(W1), _p(W3), _p(W2), _p(op),
+                                        _p(device_status), _stream(stream)),
+           "moe_expert_ffn_noalloc")
 
 
 def moe_grouped_gemm(dtype, A, offsets, n_segments, rows_max, K, n_out, B, out, ws,
