@@ -235,11 +235,13 @@ def run_ours(args, rank, world, local_rank):
         clocks.mark_start()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
+    torch.cuda.nvtx.range_push("moe_timed_steps")
     for a, b in evs:
         flush.zero_()
         a.record(stream)
         step()
         b.record(stream)
+    torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     if clocks:
         clocks.mark_end()
@@ -293,9 +295,10 @@ def run_ours(args, rank, world, local_rank):
     tok_rows = M.view_tensor(v.tok_rows, (w.T, kc), torch.int32)
     logits = M.view_tensor(v.logits, (w.T, w.N), torch.float32)
     ec = w.mode == W.EXPERT_CHOICE
+    rws = torch.zeros(M.route_workspace_size(cfg), dtype=torch.uint8, device=dev)
     stages = {
         "route": lambda: M.moe_route(cfg, d["x"], d["W_r"], d["bias"], logits, scores,
-                                     None if ec else cand_idx, cand_gate, stream=stream),
+                                     None if ec else cand_idx, cand_gate, rws, stream=stream),
         "select": lambda: M.moe_capacity_drop(cfg, None if ec else cand_idx, cand_gate, slot, keep,
                                               demand, kept, stream=stream),
         "dispatch": lambda: M.moe_dispatch(cfg, d["x"], None if ec else cand_idx, cand_gate, slot,
@@ -400,6 +403,80 @@ def run_ours(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def run_stage(args):
+    """--kernel STAGE: loop one stage of the layer on the workload (T
+    overridable with --T) and print its device time and algorithmic GB/s.
+    Holds only the routing-side tensors on the device, so a single kernel can
+    be profiled with ncu on inputs larger than L2."""
+    import routing_capacity_drop_router_b300 as M
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    w = W.ALL[args.workload]
+    if args.T:
+        w = w.replace(T=args.T)
+    inp = W.make_inputs(w, with_experts=False)
+    d = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
+    cfg = M.config_from_workload(w)
+    sz = M.sizes(cfg)
+    R, kc = int(sz.rows_max), sz.kc
+    ec = w.mode == W.EXPERT_CHOICE
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    f32, i32 = torch.float32, torch.int32
+    logits = torch.empty((w.T, w.N), dtype=f32, device=dev)
+    scores = torch.empty((w.T, w.N), dtype=f32, device=dev)
+    cand_idx = torch.empty((w.T, kc), dtype=i32, device=dev)
+    cand_gate = torch.empty((w.T, kc), dtype=f32, device=dev)
+    slot = torch.empty((w.T, kc), dtype=i32, device=dev)
+    keep = torch.empty((w.T, kc), dtype=torch.uint8, device=dev)
+    demand = torch.empty((w.N,), dtype=i32, device=dev)
+    kept = torch.empty((w.N,), dtype=i32, device=dev)
+    offs = torch.empty((w.N + 1,), dtype=i32, device=dev)
+    row_token = torch.empty((R,), dtype=i32, device=dev)
+    row_gate = torch.empty((R,), dtype=f32, device=dev)
+    tok_rows = torch.empty((w.T, kc), dtype=i32, device=dev)
+    xp = torch.empty((R, w.d), dtype=dt, device=dev)
+    op = torch.zeros((R, w.d), dtype=dt, device=dev)
+    y = torch.empty((w.T, w.d), dtype=dt, device=dev)
+    rws = torch.zeros(M.route_workspace_size(cfg), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    ci = None if ec else cand_idx
+    fns = {
+        "route": lambda: M.moe_route(cfg, d["x"], d["W_r"], d["bias"], logits, scores, ci,
+                                     cand_gate, rws),
+        "select": lambda: M.moe_capacity_drop(cfg, ci, cand_gate, slot, keep, demand, kept),
+        "dispatch": lambda: M.moe_dispatch(cfg, d["x"], ci, cand_gate, slot, kept, offs,
+                                           row_token, row_gate, tok_rows, xp),
+        "combine": lambda: M.moe_combine(cfg, op, row_gate, tok_rows, None, y),
+    }
+    for name in ("route", "select", "dispatch"):
+        fns[name]()
+    torch.cuda.synchronize()
+    P = int(offs[-1].item())
+    fn = fns[args.kernel]
+    for _ in range(args.warmup):
+        flush.zero_()
+        fn()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    torch.cuda.nvtx.range_push("moe_stage")
+    for a, b in evs:
+        flush.zero_()
+        a.record()
+        fn()
+        b.record()
+    torch.cuda.nvtx.range_pop()
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    nbytes = stage_bytes(w, P).get(args.kernel)
+    peaks, src = load_peaks()
+    out = {"kernel": args.kernel, "workload": w.describe(), "kept_pairs": P, "ms": ms}
+    if nbytes:
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out.update({"bytes": nbytes, "GB/s": gbs, "frac_hbm": gbs / float(peaks["hbm_gbs"]),
+                    "peak_source": src})
+    print(json.dumps(out), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -411,7 +488,13 @@ def main():
     ap.add_argument("--cpu-sample-tokens", type=int, default=256)
     ap.add_argument("--distinct-batches", action="store_true",
                     help="each rank draws its own x (seed + rank)")
+    ap.add_argument("--kernel", choices=["route", "select", "dispatch", "combine"],
+                    help="time one stage alone instead of the layer")
+    ap.add_argument("--T", type=int, default=0, help="token count override for --kernel")
     args = ap.parse_args()
+    if args.kernel:
+        run_stage(args)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

@@ -118,6 +118,10 @@ int moe_sizes(const moe_config* cfg, moe_sizes_t* out);
 /* Bytes of workspace moe_layer_forward needs (0 if the config is invalid). */
 size_t moe_workspace_size(const moe_config* cfg);
 
+/* Bytes of workspace moe_route needs (its status word and, for the
+ * tensor-core router, the per-split partial logits). */
+size_t moe_route_workspace_size(const moe_config* cfg);
+
 /* Bytes of workspace moe_expert_ffn needs for `rows_max` rows of hidden width f. */
 size_t moe_ffn_workspace_size(int64_t rows_max, int32_t f, int32_t dtype);
 
@@ -143,10 +147,15 @@ size_t moe_ffn_workspace_size(int64_t rows_max, int32_t f, int32_t dtype);
  *            choice kc = N and cand_gate receives the scores p.
  *   home_group [T] int32 nullable: device group of each token for expanded
  *            drop; NULL = contiguous shards, group floor(t*G/T), G = N/group_size.
+ *   ws       >= moe_route_workspace_size(cfg) bytes, 256-byte aligned.
+ * bf16 layers with N a multiple of 8 compute the logits on the tcgen05 tensor
+ * cores, the d axis split over several CTAs per 128-token tile; the splits'
+ * fp32 partials are added in a fixed order, then the bias. Other shapes use
+ * fp32 FMA. Either way L is fp32-accumulated, not the exact dot product.
  */
 int moe_route(const moe_config* cfg, const void* x, const void* W_router, const float* bias,
               float* logits, float* scores, int32_t* cand_idx, float* cand_gate,
-              const int32_t* home_group, void* stream);
+              const int32_t* home_group, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * Per-expert selection over the candidates (one thread block per expert).

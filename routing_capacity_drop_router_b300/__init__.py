@@ -75,7 +75,9 @@ SIGNATURES = {
     "moe_sizes": (ctypes.c_int, [_CFG, ctypes.POINTER(moe_sizes_t)]),
     "moe_workspace_size": (ctypes.c_size_t, [_CFG]),
     "moe_ffn_workspace_size": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32]),
-    "moe_route": (ctypes.c_int, [_CFG, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "moe_route_workspace_size": (ctypes.c_size_t, [_CFG]),
+    "moe_route": (ctypes.c_int, [_CFG, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                 ctypes.c_size_t, _VP]),
     "moe_capacity_drop": (ctypes.c_int, [_CFG, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "moe_dispatch": (ctypes.c_int, [_CFG, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "moe_expert_ffn": (ctypes.c_int, [_CFG, _VP, _VP, ctypes.c_int32, ctypes.c_int64,
@@ -178,11 +180,15 @@ def ffn_workspace_size(rows_max: int, f: int, dtype) -> int:
     return int(lib().moe_ffn_workspace_size(rows_max, f, DTYPES.get(dtype, dtype)))
 
 
-def moe_route(cfg, x, W_router, bias, logits, scores, cand_idx, cand_gate, home_group=None,
+def route_workspace_size(cfg: moe_config) -> int:
+    return int(lib().moe_route_workspace_size(ctypes.byref(cfg)))
+
+
+def moe_route(cfg, x, W_router, bias, logits, scores, cand_idx, cand_gate, ws, home_group=None,
               stream=None) -> None:
     _check(lib().moe_route(ctypes.byref(cfg), _p(x), _p(W_router), _p(bias), _p(logits),
-                           _p(scores), _p(cand_idx), _p(cand_gate), _p(home_group),
-                           _stream(stream)), "moe_route")
+                           _p(scores), _p(cand_idx), _p(cand_gate), _p(home_group), _p(ws),
+                           ws.numel() * ws.element_size(), _stream(stream)), "moe_route")
 
 
 def moe_capacity_drop(cfg, cand_idx, cand_gate, slot, keep, demand, kept, stream=None) -> None:

@@ -33,13 +33,14 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "device_common.cuh"
 #include "internal.h"
+#include "tc_ptx.cuh"
 
 namespace moe {
 namespace {
+
+using namespace tc;
 
 constexpr int kBM = 128;
 constexpr int kBN = 256;  // accumulator columns per tile
@@ -69,124 +70,6 @@ struct __align__(8) Ctrl {
 };
 constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + static_cast<int>(sizeof(Ctrl));
 
-// ---- PTX wrappers ---------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ unsigned long long global_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0u;
-}
-// Bounded wait: false if the abort flag is raised or the limit expires
-// (which raises the flag).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          unsigned long long limit_ns) {
-  if (mbar_try(bar, parity)) return true;
-  const unsigned long long t0 = global_ns();
-  while (true) {
-    if (mbar_try(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (global_ns() - t0 > limit_ns) {
-      *abort_flag = 1;
-      return false;
-    }
-  }
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
-                                            int c2, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                       uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-               : "memory");
-}
-__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t* v) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
-        "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
-        "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
-        "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
-      : "r"(taddr));
-}
-__device__ __forceinline__ void tc_wait_ld() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format: start
-// address >> 4 in bits 0-13, leading byte offset >> 4 in 16-29, stride byte
-// offset >> 4 in 32-45, descriptor version 1 in 46-47, swizzle mode 2 =
-// 128-byte in 61-63).
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
-  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
-  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
-  d |= 1ull << 46;
-  d |= 2ull << 61;
-  return d;
-}
-// A tile: 128 rows x 64 k, K-major, each row one 128-byte swizzled line;
-// 8-row groups 1024 bytes apart. A k-step of 16 elements moves 32 bytes.
-__device__ __forceinline__ uint64_t a_desc(uint32_t a_base, int kk) {
-  return sw128_desc(a_base + kk * 32, 16, 1024);
-}
-// B tile: four 64-column boxes of 64 k-rows (8 KiB each), MN-major: 64
-// contiguous n per 128-byte line, lines for consecutive k; 8-line k-groups
-// 1024 bytes apart (stride offset), boxes 8 KiB apart (leading offset). A
-// k-step of 16 is two k-groups: 2048 bytes.
-__device__ __forceinline__ uint64_t b_desc(uint32_t b_base, int kk) {
-  return sw128_desc(b_base + kk * 2048, kBBoxBytes, 1024);
-}
 // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A bf16 (7-9 = 1),
 // B bf16 (10-12 = 1), A K-major (bit 15 = 0), B MN-major (bit 16 = 1),
 // N >> 3 in bits 17-22, M >> 4 in bits 24-28.
@@ -355,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
         const uint32_t sb = sa + kABytes;
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk)
-          tc_mma(d_tmem, a_desc(sa, kk), b_desc(sb, kk), kIdesc, (kb | kk) != 0 ? 1u : 0u);
+          tc_mma(d_tmem, kmajor_desc(sa, kk), mnmajor_desc(sb, kk, kBBoxBytes), kIdesc, (kb | kk) != 0 ? 1u : 0u);
         tc_commit(smem_u32(&ctrl->empty[stage]));
         if (++stage == kStages) {
           stage = 0;
@@ -444,52 +327,6 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
   }
 }
 
-// ---- host: tensor maps ----------------------------------------------------
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static std::once_flag once;
-  static EncodeTiledFn fn = nullptr;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  });
-  return fn;
-}
-
-// 2-D bf16 map [rows, cols] row-major, box 64 cols x box_rows rows, 128B swizzle.
-bool make_map_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * 2};
-  const cuuint32_t box[2] = {64, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// 3-D bf16 map [S, K, n] row-major, box 64 n x 64 k x 1.
-bool make_map_3d(CUtensorMap* m, const void* ptr, uint64_t S, uint64_t K, uint64_t n) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[3] = {n, K, S};
-  const cuuint64_t strides[2] = {n * 2, n * K * 2};
-  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kBK), 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 cudaError_t launch_grouped_gemm_tc_bf16(const void* A, const int32_t* offsets, int S,
@@ -499,11 +336,11 @@ cudaError_t launch_grouped_gemm_tc_bf16(const void* A, const int32_t* offsets, i
   if (S == 0 || rows_max == 0) return cudaSuccess;
   if (S > kMaxSegments) return cudaErrorInvalidValue;
   CUtensorMap mA, mB1, mB3;
-  if (!make_map_2d(&mA, A, static_cast<uint64_t>(rows_max), static_cast<uint64_t>(K), kBM))
+  if (!make_tmap_2d_bf16(&mA, A, static_cast<uint64_t>(rows_max), static_cast<uint64_t>(K), 64, kBM))
     return cudaErrorInvalidValue;
-  if (!make_map_3d(&mB1, B1, S, K, n_out)) return cudaErrorInvalidValue;
+  if (!make_tmap_3d_bf16(&mB1, B1, S, K, n_out, 64, kBK)) return cudaErrorInvalidValue;
   if (swiglu) {
-    if (!make_map_3d(&mB3, B3, S, K, n_out)) return cudaErrorInvalidValue;
+    if (!make_tmap_3d_bf16(&mB3, B3, S, K, n_out, 64, kBK)) return cudaErrorInvalidValue;
   } else {
     mB3 = mB1;
   }

@@ -2,6 +2,7 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace moe {
@@ -10,8 +11,23 @@ namespace moe {
 cudaError_t launch_router_logits(int dtype, const void* x, const void* W_r, const float* bias,
                                  float* L, int T, int d, int N, cudaStream_t s);
 
-// Per-token scores, candidates and gates from fp32 logits.
-cudaError_t launch_route_tokens(const float* L, float* scores, int32_t* cand_idx,
+// Router logits on tcgen05 (bf16, N % 8 == 0): split-K partials
+// partial[split][T][N] fp32, summed by launch_route_tokens.
+struct RouterSplit {
+  int splits = 1;
+  int kb_per_split = 1;
+};
+bool router_tc_supported(int dtype, int d, int N);
+RouterSplit router_split_plan(int T, int d, int N);
+cudaError_t launch_router_logits_tc(const void* x, const void* W_r, int T, int d, int N,
+                                    const RouterSplit& plan, float* partial, int32_t* status,
+                                    cudaStream_t s);
+
+// Per-token scores, candidates and gates. The logits of token t are
+// sum_{s < nsplit} partial[s][t][:] (+ bias), summed in ascending s; with
+// logits_out they are also stored there.
+cudaError_t launch_route_tokens(const float* partial, int nsplit, const float* bias,
+                                float* logits_out, float* scores, int32_t* cand_idx,
                                 float* cand_gate, const int32_t* home_group, int T, int N, int k,
                                 int m, int group_size, int renorm, int expert_choice,
                                 cudaStream_t s);
@@ -51,5 +67,12 @@ cudaError_t launch_stats(const int32_t* demand, const int32_t* kept, const float
                          int N, double* partial, double* stats, cudaStream_t s);
 
 int device_sm_count();
+
+// bf16 TMA maps with 128-byte swizzle. 2-D: [rows, cols] row-major, box
+// box_cols x box_rows. 3-D: [S, K, n] row-major, box box_n x box_k x 1.
+bool make_tmap_2d_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols,
+                       uint32_t box_cols, uint32_t box_rows);
+bool make_tmap_3d_bf16(CUtensorMap* m, const void* ptr, uint64_t S, uint64_t K, uint64_t n,
+                       uint32_t box_n, uint32_t box_k);
 
 }  // namespace moe

@@ -91,8 +91,49 @@ int validate(const moe_config* c, Derived* dv) {
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+int status_from(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH; }
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+// Scratch of the tensor-core router: one fp32 [T, N] partial per k-split.
+size_t router_partial_bytes(const moe_config& c) {
+  if ((c.flags & MOE_LOGITS_GIVEN) || !router_tc_supported(c.dtype, c.d, c.N) || c.T == 0) return 0;
+  const RouterSplit p = router_split_plan(c.T, c.d, c.N);
+  return static_cast<size_t>(p.splits) * c.T * c.N * 4;
+}
+
+// Logits (unless given) and per-token routing. logits: output buffer, or the
+// input when MOE_LOGITS_GIVEN. partial: router scratch (router_partial_bytes).
+int run_router(const moe_config& c, bool ec, const void* x, const void* W_r, const float* bias,
+               float* logits, float* scores, int32_t* cand_idx, float* cand_gate,
+               const int32_t* home_group, float* partial, int32_t* status, cudaStream_t s) {
+  if (c.T == 0) return MOE_OK;
+  const bool given = (c.flags & MOE_LOGITS_GIVEN) != 0;
+  const float* src = logits;
+  int nsplit = 1;
+  const float* add_bias = nullptr;
+  float* logits_out = nullptr;
+  if (!given) {
+    if (router_tc_supported(c.dtype, c.d, c.N)) {
+      const RouterSplit p = router_split_plan(c.T, c.d, c.N);
+      if (launch_router_logits_tc(x, W_r, c.T, c.d, c.N, p, partial, status, s) != cudaSuccess)
+        return MOE_ERR_LAUNCH;
+      src = partial;
+      nsplit = p.splits;
+      add_bias = bias;
+      logits_out = logits;
+    } else if (launch_router_logits(c.dtype, x, W_r, bias, logits, c.T, c.d, c.N, s) !=
+               cudaSuccess) {
+      return MOE_ERR_LAUNCH;
+    }
+  }
+  return status_from(launch_route_tokens(src, nsplit, add_bias, logits_out, scores, cand_idx,
+                                         cand_gate, home_group, c.T, c.N, c.k, c.m, c.group_size,
+                                         c.renorm, ec ? 1 : 0, s));
+}
+
 struct Layout {
-  size_t status, logits, scores, cand_idx, cand_gate, slot, keep, demand, kept, offsets,
+  size_t status, router_partial, logits, scores, cand_idx, cand_gate, slot, keep, demand, kept, offsets,
       shared_offsets, row_token, row_gate, tok_rows, xp, hp, op, shared_out, stats_partial, total;
 };
 
@@ -106,6 +147,7 @@ Layout layout(const moe_config& c, const Derived& d) {
   };
   const size_t T = c.T, N = c.N, kc = d.kc, R = d.rows_max, dd = c.d;
   L.status = take(256);
+  L.router_partial = take(router_partial_bytes(c));
   L.logits = take(T * N * 4);
   L.scores = take(T * N * 4);
   L.cand_idx = take(T * kc * 4);
@@ -134,9 +176,6 @@ P* at(void* ws, size_t off) {
   return reinterpret_cast<P*>(static_cast<unsigned char*>(ws) + off);
 }
 
-int status_from(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH; }
-
-cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
 // FFN over expert-contiguous rows; hp is scratch of rows_max * f elements.
 int run_ffn(int dtype, const void* xp, const int32_t* offsets, int S, int64_t rows_max, int d,
@@ -191,27 +230,29 @@ size_t moe_ffn_workspace_size(int64_t rows_max, int32_t f, int32_t dtype) {
   return 256 + align256(static_cast<size_t>(rows_max) * static_cast<size_t>(f) * sx);
 }
 
+size_t moe_route_workspace_size(const moe_config* cfg) {
+  Derived d;
+  if (validate(cfg, &d) != MOE_OK) return 0;
+  return 256 + align256(router_partial_bytes(*cfg));
+}
+
 int moe_route(const moe_config* cfg, const void* x, const void* W_router, const float* bias,
               float* logits, float* scores, int32_t* cand_idx, float* cand_gate,
-              const int32_t* home_group, void* stream) {
+              const int32_t* home_group, void* ws, size_t ws_bytes, void* stream) {
   Derived d;
   int st = validate(cfg, &d);
   if (st != MOE_OK) return st;
   const bool given = (cfg->flags & MOE_LOGITS_GIVEN) != 0;
   const int64_t T = cfg->T;
-  if (!have(logits, T) || !have(cand_gate, T) || (!d.ec && !have(cand_idx, T)))
+  if (!have(logits, T) || !have(cand_gate, T) || (!d.ec && !have(cand_idx, T)) || !ws)
     return MOE_ERR_NULL;
   if (!given && (!have(x, T) || !W_router)) return MOE_ERR_NULL;
   if (!given && (!aligned16(x) || !aligned16(W_router))) return MOE_ERR_ALIGN;
-  cudaStream_t s = as_stream(stream);
-  if (!given) {
-    if (launch_router_logits(cfg->dtype, x, W_router, bias, logits, cfg->T, cfg->d, cfg->N, s) !=
-        cudaSuccess)
-      return MOE_ERR_LAUNCH;
-  }
-  return status_from(launch_route_tokens(logits, scores, cand_idx, cand_gate, home_group, cfg->T,
-                                         cfg->N, cfg->k, cfg->m, cfg->group_size, cfg->renorm,
-                                         d.ec ? 1 : 0, s));
+  if (reinterpret_cast<uintptr_t>(ws) & 255u) return MOE_ERR_ALIGN;
+  if (ws_bytes < moe_route_workspace_size(cfg)) return MOE_ERR_WORKSPACE;
+  return run_router(*cfg, d.ec, x, W_router, bias, logits, scores, cand_idx, cand_gate,
+                    home_group, reinterpret_cast<float*>(static_cast<unsigned char*>(ws) + 256),
+                    static_cast<int32_t*>(ws), as_stream(stream));
 }
 
 int moe_capacity_drop(const moe_config* cfg, const int32_t* cand_idx, const float* cand_gate,
@@ -349,11 +390,9 @@ int moe_layer_forward(const moe_config* cfg, const void* x, const void* W_router
   void* op = at<void>(ws, L.op);
   void* ys = c.f_shared > 0 ? at<void>(ws, L.shared_out) : nullptr;
 
-  if (!given && launch_router_logits(c.dtype, x, W_router, bias, Lg, c.T, c.d, c.N, s) != cudaSuccess)
-    return MOE_ERR_LAUNCH;
-  if (launch_route_tokens(Lg, scores, cand_idx, cand_gate, home_group, c.T, c.N, c.k, c.m,
-                          c.group_size, c.renorm, d.ec ? 1 : 0, s) != cudaSuccess)
-    return MOE_ERR_LAUNCH;
+  st = run_router(c, d.ec, x, W_router, bias, Lg, scores, cand_idx, cand_gate, home_group,
+                  at<float>(ws, L.router_partial), status, s);
+  if (st != MOE_OK) return st;
   if (launch_select(cand_idx, cand_gate, c.T, d.kc, c.N, d.ec ? 1 : 0, d.cap, slot, keep, demand,
                     kept, s) != cudaSuccess)
     return MOE_ERR_LAUNCH;

@@ -129,16 +129,35 @@ cudaError_t logits_dispatch_ne(const E* x, const E* W_r, const float* bias, floa
 //   gates: p of the slot; with renorm divided by the slots' left-to-right sum.
 // ---------------------------------------------------------------------------
 template <int NMAX>
-__global__ void __launch_bounds__(128) route_tokens_kernel(
-    const float* __restrict__ L, float* __restrict__ scores, int32_t* __restrict__ cand_idx,
+__global__ void __launch_bounds__(64) route_tokens_kernel(
+    const float* __restrict__ partial, int nsplit, const float* __restrict__ bias,
+    float* __restrict__ logits_out, float* __restrict__ scores, int32_t* __restrict__ cand_idx,
     float* __restrict__ cand_gate, const int32_t* __restrict__ home_group, int T, int N, int k,
     int m, int group_size, int renorm, int expert_choice) {
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= T) return;
-  const float* row = L + static_cast<size_t>(t) * N;
   float l[NMAX];
+  {
+    const float* row = partial + static_cast<size_t>(t) * N;
 #pragma unroll
-  for (int e = 0; e < NMAX; ++e) l[e] = (e < N) ? row[e] : 0.f;
+    for (int e = 0; e < NMAX; ++e) l[e] = (e < N) ? row[e] : 0.f;
+    for (int sp = 1; sp < nsplit; ++sp) {  // splits added in ascending order
+      row += static_cast<size_t>(T) * N;
+#pragma unroll
+      for (int e = 0; e < NMAX; ++e)
+        if (e < N) l[e] += row[e];
+    }
+    if (bias) {
+#pragma unroll
+      for (int e = 0; e < NMAX; ++e)
+        if (e < N) l[e] += bias[e];
+    }
+    if (logits_out) {
+#pragma unroll
+      for (int e = 0; e < NMAX; ++e)
+        if (e < N) logits_out[static_cast<size_t>(t) * N + e] = l[e];
+    }
+  }
   float mx = l[0];
 #pragma unroll
   for (int e = 1; e < NMAX; ++e)
@@ -213,12 +232,14 @@ __global__ void __launch_bounds__(128) route_tokens_kernel(
 }
 
 template <int NMAX>
-cudaError_t route_tokens_launch(const float* L, float* scores, int32_t* cand_idx, float* cand_gate,
-                                const int32_t* home_group, int T, int N, int k, int m,
-                                int group_size, int renorm, int ec, cudaStream_t s) {
-  const int threads = 128;
+cudaError_t route_tokens_launch(const float* partial, int nsplit, const float* bias,
+                                float* logits_out, float* scores, int32_t* cand_idx,
+                                float* cand_gate, const int32_t* home_group, int T, int N, int k,
+                                int m, int group_size, int renorm, int ec, cudaStream_t s) {
+  const int threads = 64;
   route_tokens_kernel<NMAX><<<(T + threads - 1) / threads, threads, 0, s>>>(
-      L, scores, cand_idx, cand_gate, home_group, T, N, k, m, group_size, renorm, ec);
+      partial, nsplit, bias, logits_out, scores, cand_idx, cand_gate, home_group, T, N, k, m,
+      group_size, renorm, ec);
   return cudaGetLastError();
 }
 
@@ -234,14 +255,15 @@ cudaError_t launch_router_logits(int dtype, const void* x, const void* W_r, cons
                             T, d, N, s);
 }
 
-cudaError_t launch_route_tokens(const float* L, float* scores, int32_t* cand_idx,
+cudaError_t launch_route_tokens(const float* partial, int nsplit, const float* bias,
+                                float* logits_out, float* scores, int32_t* cand_idx,
                                 float* cand_gate, const int32_t* home_group, int T, int N, int k,
                                 int m, int group_size, int renorm, int ec, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
 #define MOE_ROUTE_CASE(NM)                                                                     \
   if (N <= NM)                                                                                 \
-    return route_tokens_launch<NM>(L, scores, cand_idx, cand_gate, home_group, T, N, k, m,     \
-                                   group_size, renorm, ec, s);
+    return route_tokens_launch<NM>(partial, nsplit, bias, logits_out, scores, cand_idx,       \
+                                   cand_gate, home_group, T, N, k, m, group_size, renorm, ec, s);
   MOE_ROUTE_CASE(8)
   MOE_ROUTE_CASE(16)
   MOE_ROUTE_CASE(32)

@@ -61,8 +61,9 @@ def gpu_routing(w: W.Workload, L: torch.Tensor, home_group: Optional[torch.Tenso
     scores = torch.empty((T, N), dtype=torch.float32, device=dev)
     cand_idx = torch.full((T, kc), -7, dtype=torch.int32, device=dev)
     cand_gate = torch.full((T, kc), -7.0, dtype=torch.float32, device=dev)
+    rws = torch.zeros(M.route_workspace_size(cfg), dtype=torch.uint8, device=dev)
     M.moe_route(cfg, None, None, None, Ld, scores, None if w.mode == W.EXPERT_CHOICE else cand_idx,
-                cand_gate, cuda(home_group))
+                cand_gate, rws, home_group=cuda(home_group))
     slot = torch.full((T, kc), -7, dtype=torch.int32, device=dev)
     keep = torch.full((T, kc), 7, dtype=torch.uint8, device=dev)
     demand = torch.full((N,), -7, dtype=torch.int32, device=dev)

@@ -91,7 +91,7 @@ def test_null_pointers_rejected_before_any_launch():
     lib = M.lib()
     cfg = _cfg()
     r = ctypes.byref(cfg)
-    assert lib.moe_route(r, None, None, None, None, None, None, None, None, None) == M.MOE_ERR_NULL
+    assert lib.moe_route(r, *([None] * 9), 0, None) == M.MOE_ERR_NULL
     assert lib.moe_capacity_drop(r, None, None, None, None, None, None, None) == M.MOE_ERR_NULL
     assert lib.moe_dispatch(r, *([None] * 10), None) == M.MOE_ERR_NULL
     assert lib.moe_combine(r, None, None, None, None, None, None) == M.MOE_ERR_NULL
@@ -100,7 +100,8 @@ def test_null_pointers_rejected_before_any_launch():
                               None) == M.MOE_ERR_NULL
     assert lib.moe_load_stats(r, None, None, None, None, None, 0, None) == M.MOE_ERR_NULL
     assert lib.moe_get_device_status(None, None, None) == M.MOE_ERR_NULL
-    assert lib.moe_route(None, *([None] * 9)) == M.MOE_ERR_NULL
+    assert lib.moe_route(None, *([None] * 9), 0, None) == M.MOE_ERR_NULL
+    assert lib.moe_route_workspace_size(None) == 0
 
 
 def test_misaligned_and_small_workspace_rejected_before_any_launch():

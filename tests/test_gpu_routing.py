@@ -93,8 +93,9 @@ def test_router_logits_within_fp32_bound(name):
     Lg = torch.empty((w.T, w.N), dtype=torch.float32, device=dev)
     idx = torch.empty((w.T, sz.kc), dtype=torch.int32, device=dev)
     gate = torch.empty((w.T, sz.kc), dtype=torch.float32, device=dev)
+    rws = torch.zeros(G.M.route_workspace_size(cfg), dtype=torch.uint8, device=dev)
     G.M.moe_route(cfg, G.cuda(inp["x"]), G.cuda(inp["W_r"]), G.cuda(inp["bias"]), Lg, None,
-                  None if w.mode == W.EXPERT_CHOICE else idx, gate)
+                  None if w.mode == W.EXPERT_CHOICE else idx, gate, rws)
     torch.cuda.synchronize()
     diff = np.abs(Lg.cpu().numpy().astype(np.float64) - L.astype(np.float64))
     bound = G.logit_bound(G.np32(inp["x"]), G.np32(inp["W_r"]), L)
