@@ -120,16 +120,6 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm), "window": window}
 
 
-def count_launches(w, with_stats=True) -> int:
-    """Kernels of this library one moe_layer_forward launches."""
-    n = 1 + 1 + 1 + 1 + 2 + 1          # logits, route, select, dispatch, 2 GEMMs, combine
-    if w.f_shared:
-        n += 1 + 2                      # shared offsets, 2 GEMMs
-    if with_stats:
-        n += 2 if w.T > 0 else 1
-    return n
-
-
 def ffn_flops(w, P: int) -> float:
     return 6.0 * w.d * w.f * P + (6.0 * w.d * w.f_shared * w.T if w.f_shared else 0.0)
 
@@ -144,23 +134,59 @@ def stage_bytes(w, P: int):
     }
 
 
-def cpu_oracle_sample(w, n_tokens: int):
-    """The oracle, as it stands, on a bounded sample: full-batch routing (the
-    capacity couples all tokens) plus the expert FFN of n_tokens tokens."""
-    import oracle as O
-    inp = W.make_inputs(w)
-    f = lambda t: None if t is None else t.float().numpy()  # noqa: E731
-    x, Wr, b = f(inp["x"]), f(inp["W_r"]), f(inp["bias"])
-    W1, W3, W2 = f(inp["W1"]), f(inp["W3"]), f(inp["W2"])
-    Ws = [f(inp.get(k)) for k in ("Ws1", "Ws3", "Ws2")]
-    rng = np.random.default_rng(0)
-    tokens = np.sort(rng.choice(w.T, size=min(n_tokens, w.T), replace=False))
-    t0 = time.perf_counter()
-    O.layer_forward(x, Wr, b, W1, W3, W2, mode=w.mode, k=w.k, gamma=w.gamma, m=w.m,
-                    group_size=w.group_size, renorm=w.renorm, dtype=w.dtype, Ws1=Ws[0],
-                    Ws3=Ws[1], Ws2=Ws[2], tokens=tokens)
-    dt = time.perf_counter() - t0
-    return len(tokens), dt
+def _blas_threads() -> int:
+    """Threads the oracle's fp64 BLAS calls actually run on."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+class OracleSampler:
+    """The oracle, as it stands, on bounded samples of one workload: the
+    routing of the whole batch (capacity and expert choice couple all tokens)
+    plus the expert FFN of a fixed random subset of tokens. The subset size is
+    calibrated once so that one sample takes about ``target_s`` seconds."""
+
+    def __init__(self, w):
+        import oracle as O
+        self.O = O
+        self.w = w
+        inp = W.make_inputs(w)
+        f = lambda t: None if t is None else t.float().numpy()  # noqa: E731
+        self.args = (f(inp["x"]), f(inp["W_r"]), f(inp["bias"]), f(inp["W1"]), f(inp["W3"]),
+                     f(inp["W2"]))
+        self.shared = [f(inp.get(k)) for k in ("Ws1", "Ws3", "Ws2")]
+        self.n_tokens = None
+
+    def run(self, n_tokens: int):
+        w = self.w
+        rng = np.random.default_rng(0)
+        tokens = np.sort(rng.choice(w.T, size=min(n_tokens, w.T), replace=False))
+        t0 = time.perf_counter()
+        self.O.layer_forward(*self.args, mode=w.mode, k=w.k, gamma=w.gamma, m=w.m,
+                             group_size=w.group_size, renorm=w.renorm, dtype=w.dtype,
+                             Ws1=self.shared[0], Ws3=self.shared[1], Ws2=self.shared[2],
+                             tokens=tokens)
+        return len(tokens), time.perf_counter() - t0
+
+    def calibrate(self, target_s: float) -> int:
+        """Pick the token count whose sample takes about target_s seconds."""
+        n0, t0 = self.run(min(64, self.w.T))
+        n1, t1 = self.run(min(256, self.w.T))
+        per_tok = max((t1 - t0) / max(n1 - n0, 1), 1e-6)
+        fixed = max(t0 - per_tok * n0, 0.0)  # full-batch routing
+        n = int((target_s - fixed) / per_tok)
+        self.n_tokens = max(1, min(self.w.T, n))
+        return self.n_tokens
+
+    def describe(self, n: int, dt: float) -> str:
+        return (f"full-batch routing of {self.w.T} tokens + expert FFN of {n} of them "
+                f"(one sample, {dt:.1f} s)")
 
 
 def run_reference(args, rank, world):
@@ -168,26 +194,49 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     w = W.ALL[args.workload]
-    n_tok = args.cpu_sample_tokens
+    smp = OracleSampler(w)
+    # whole run (warm-up + timed) bounded to about args.reference_budget_s
+    per_step = min(20.0, max(1.0, args.reference_budget_s / max(1, args.steps + args.warmup)))
+    n_tok = smp.calibrate(per_step)
     for _ in range(args.warmup):
-        cpu_oracle_sample(w, n_tok)
+        smp.run(n_tok)
     times = []
     for _ in range(args.steps):
-        n, dt = cpu_oracle_sample(w, n_tok)
+        n, dt = smp.run(n_tok)
         times.append(dt)
     tps = n / statistics.mean(times)
-    cores = os.cpu_count()  # OpenBLAS runs the fp64 matmuls on every core
     line = {
         "impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * statistics.mean(times), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.describe(), "sample_tokens": n},
-        "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": f"full-batch routing + expert FFN of {n} of {w.T} tokens"},
+        "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": _blas_threads(),
+                         "kind": "oracle",
+                         "sample": smp.describe(n, statistics.mean(times)) + " per step"},
         "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def gemm_traffic(w):
+    """DRAM bytes per launch of the grouped GEMM pair on this workload from
+    the committed ncu capture, or None when the kernel source differs from
+    the one captured (the counters no longer describe it)."""
+    import hashlib
+    src = os.path.join(ROOT, "routing_capacity_drop_router_b300", "csrc", "ffn_tcgen05.cu")
+    with open(src, "rb") as fh:
+        sha = hashlib.sha256(fh.read()).hexdigest()[:16]
+    rec = GEMM_TRAFFIC.get(w.name)
+    if rec is None or rec["kernel_sha"] != sha:
+        return None
+    return rec["bytes_per_launch_pair"]
+
+
+# dram__bytes_read.sum + dram__bytes_write.sum of expert_gemm1_swiglu +
+# expert_gemm2 from one ncu capture per workload (profiles/ has the summary),
+# keyed by the sha256 prefix of the kernel source it was taken on.
+GEMM_TRAFFIC = {}
 
 
 def run_ours(args, rank, world, local_rank):
@@ -207,8 +256,17 @@ def run_ours(args, rank, world, local_rank):
     dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     y = torch.empty((w.T, w.d), dtype=dt, device=dev)
     stats = torch.zeros(M.MOE_STATS_LEN, dtype=torch.float64, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
+    stages = M.moe_layer_stages(cfg, with_stats=True)
+    weight_bytes = sum(t.numel() * t.element_size() for k, t in d.items()
+                       if t is not None and k in ("W1", "W3", "W2", "Ws1", "Ws3", "Ws2"))
+    l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
+    # Between steps the L2 is not flushed: every step streams all expert
+    # weights it uses (far more than the L2) through it, so the next step's
+    # activations start cold. Smaller workloads flush explicitly.
+    flush = None
+    if weight_bytes < 4 * l2_bytes:
+        flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
 
     def step():
         M.moe_layer_forward(cfg, d["x"], d["W_r"], d["bias"], d["W1"], d["W3"], d["W2"],
@@ -216,7 +274,8 @@ def run_ours(args, rank, world, local_rank):
                             stream=stream)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        if flush is not None:
+            flush.zero_()
         step()
     torch.cuda.synchronize()
     if M.moe_get_device_status(ws) != M.MOE_OK:
@@ -224,7 +283,14 @@ def run_ours(args, rank, world, local_rank):
     st = stats.cpu().numpy()
     P = int(st[0])
 
-    # ---- timed region: K steps, L2 flushed between steps (outside the events) ----
+    # ---- timed region: K layer steps; the library records one event before
+    # its first launch and one after every kernel, on the launching stream ----
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)]
+           for _ in range(args.steps)]
+    for row in evs:  # give every event its CUDA handle before the timed region
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
     clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     if clocks:
         clocks.start()
@@ -233,93 +299,31 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     if clocks:
         clocks.mark_start()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
+    t_first, t_last = evs[0][0], evs[-1][-1]
     torch.cuda.nvtx.range_push("moe_timed_steps")
-    for a, b in evs:
-        flush.zero_()
-        a.record(stream)
+    for row in evs:
+        if flush is not None:
+            flush.zero_()
+        M.moe_set_trace_events(row)
         step()
-        b.record(stream)
+    M.moe_set_trace_events(None)
     torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     if clocks:
         clocks.mark_end()
     if dist:
         td.barrier()
-    ms = [a.elapsed_time(b) for a, b in evs]
     clk = clocks.stop() if clocks else None
-    total_ms = sum(ms)
+    step_ms = [row[0].elapsed_time(row[-1]) for row in evs]
+    stage_ms = {name: statistics.mean(row[i].elapsed_time(row[i + 1]) for row in evs)
+                for i, name in enumerate(stages)}
+    total_ms = sum(step_ms) if flush is not None else t_first.elapsed_time(t_last)
     if dist:
         t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
         td.all_reduce(t, op=td.ReduceOp.MAX)
         total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
     value = world * w.T * args.steps / (total_ms / 1e3)
-
-    # ---- the expert GEMMs on their own (the dominant kernel), same rows ----
-    v = M.moe_workspace_views(cfg, ws)
-    offs = M.view_tensor(v.expert_offsets, (w.N + 1,), torch.int32)
-    xp = M.view_tensor(v.xp, (int(sz.rows_max), w.d), dt)
-    op = M.view_tensor(v.op, (int(sz.rows_max), w.d), dt)
-    ffn_ws = torch.zeros(M.ffn_workspace_size(int(sz.rows_max), w.f, w.dtype), dtype=torch.uint8,
-                         device=dev)
-    kreps = max(3, args.steps)
-    for _ in range(2):
-        M.moe_expert_ffn(cfg, xp, offs, w.N, int(sz.rows_max), w.f, d["W1"], d["W3"], d["W2"], op,
-                         ffn_ws, stream=stream)
-    fev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(kreps)]
-    for a, b in fev:
-        flush.zero_()
-        a.record(stream)
-        M.moe_expert_ffn(cfg, xp, offs, w.N, int(sz.rows_max), w.f, d["W1"], d["W3"], d["W2"], op,
-                         ffn_ws, stream=stream)
-        b.record(stream)
-    torch.cuda.synchronize()
-    ffn_ms = statistics.mean(a.elapsed_time(b) for a, b in fev)
-    routed_flops = 6.0 * w.d * w.f * P
-    ffn_tflops = routed_flops / (ffn_ms * 1e-3) / 1e12
-
-    # ---- HBM-bound stages on their own (split entry points, same buffers) ----
-    kc = sz.kc
-    scores = M.view_tensor(v.scores, (w.T, w.N), torch.float32)
-    cand_idx = M.view_tensor(v.cand_idx, (w.T, kc), torch.int32)
-    cand_gate = M.view_tensor(v.cand_gate, (w.T, kc), torch.float32)
-    slot = M.view_tensor(v.slot, (w.T, kc), torch.int32)
-    keep = M.view_tensor(v.keep, (w.T, kc), torch.uint8)
-    demand = M.view_tensor(v.demand, (w.N,), torch.int32)
-    kept = M.view_tensor(v.kept, (w.N,), torch.int32)
-    row_token = M.view_tensor(v.row_token, (int(sz.rows_max),), torch.int32)
-    row_gate = M.view_tensor(v.row_gate, (int(sz.rows_max),), torch.float32)
-    tok_rows = M.view_tensor(v.tok_rows, (w.T, kc), torch.int32)
-    logits = M.view_tensor(v.logits, (w.T, w.N), torch.float32)
-    ec = w.mode == W.EXPERT_CHOICE
-    rws = torch.zeros(M.route_workspace_size(cfg), dtype=torch.uint8, device=dev)
-    stages = {
-        "route": lambda: M.moe_route(cfg, d["x"], d["W_r"], d["bias"], logits, scores,
-                                     None if ec else cand_idx, cand_gate, rws, stream=stream),
-        "select": lambda: M.moe_capacity_drop(cfg, None if ec else cand_idx, cand_gate, slot, keep,
-                                              demand, kept, stream=stream),
-        "dispatch": lambda: M.moe_dispatch(cfg, d["x"], None if ec else cand_idx, cand_gate, slot,
-                                           kept, offs, row_token, row_gate, tok_rows, xp,
-                                           stream=stream),
-        "combine": lambda: M.moe_combine(cfg, op, row_gate, tok_rows,
-                                         M.view_tensor(v.shared_out, (w.T, w.d), dt)
-                                         if w.f_shared else None, y, stream=stream),
-    }
-    stage_ms = {}
-    for name, fn in stages.items():
-        fn()
-        sev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(kreps)]
-        for a, b in sev:
-            flush.zero_()
-            a.record(stream)
-            fn()
-            b.record(stream)
-        torch.cuda.synchronize()
-        stage_ms[name] = statistics.mean(a.elapsed_time(b) for a, b in sev)
 
     # ---- end to end through host buffers: H2D x, layer, D2H y every step ----
     x_host = inp["x"].pin_memory()
@@ -359,23 +363,36 @@ def run_ours(args, rank, world, local_rank):
 
     peaks, peak_src = load_peaks()
     peak_tf = float(peaks["bf16_tflops"])
-    sbytes = stage_bytes(w, P)
     hbm = float(peaks["hbm_gbs"])
+    sbytes = stage_bytes(w, P)
     kernels = {}
-    for name in ("route", "dispatch", "combine"):
-        gbs = sbytes[name] / (stage_ms[name] * 1e-3) / 1e9
-        kernels[name] = {"ms": stage_ms[name], "bytes": sbytes[name], "GB/s": gbs,
-                         "frac_hbm": gbs / hbm}
+    route_ms = stage_ms.get("router_logits", 0.0) + stage_ms["route_tokens"]
+    for name, ms in (("route", route_ms), ("dispatch", stage_ms["dispatch"]),
+                     ("combine", stage_ms["combine"])):
+        gbs = sbytes[name] / (ms * 1e-3) / 1e9
+        kernels[name] = {"ms": ms, "bytes": sbytes[name], "GB/s": gbs, "frac_hbm": gbs / hbm}
     kernels["select"] = {"ms": stage_ms["select"]}
-    kernels["expert_ffn"] = {"ms": ffn_ms, "flops": routed_flops, "TFLOP/s": ffn_tflops,
-                             "frac_bf16": ffn_tflops / peak_tf}
+    g1, g2 = stage_ms["expert_gemm1_swiglu"], stage_ms["expert_gemm2"]
+    routed_flops = 6.0 * w.d * w.f * P
+    ffn_tflops = routed_flops / ((g1 + g2) * 1e-3) / 1e12
+    kernels["expert_gemm1_swiglu"] = {"ms": g1, "flops": 4.0 * w.d * w.f * P,
+                                      "TFLOP/s": 4.0 * w.d * w.f * P / (g1 * 1e-3) / 1e12}
+    kernels["expert_gemm2"] = {"ms": g2, "flops": 2.0 * w.d * w.f * P,
+                               "TFLOP/s": 2.0 * w.d * w.f * P / (g2 * 1e-3) / 1e12}
+    if w.f_shared:
+        sg = stage_ms["shared_gemm1_swiglu"] + stage_ms["shared_gemm2"]
+        kernels["shared_expert"] = {"ms": sg, "flops": 6.0 * w.d * w.f_shared * w.T,
+                                    "TFLOP/s": 6.0 * w.d * w.f_shared * w.T / (sg * 1e-3) / 1e12}
+    kernels["stats"] = {"ms": stage_ms["stats_partial"] + stage_ms["stats_final"]}
+    kernels["stage_ms"] = stage_ms
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        n, t_cpu = cpu_oracle_sample(w, args.cpu_sample_tokens)
-        cpu = {"value": n / t_cpu, "unit": "tokens/s", "cores": os.cpu_count(),
-               "kind": "oracle",
-               "sample": f"full-batch routing + expert FFN of {n} of {w.T} tokens ({t_cpu:.1f} s)"}
+        smp = OracleSampler(w)
+        n_tok = smp.calibrate(args.cpu_sample_s)
+        n, t_cpu = smp.run(n_tok)
+        cpu = {"value": n / t_cpu, "unit": "tokens/s", "cores": _blas_threads(),
+               "kind": "oracle", "sample": smp.describe(n, t_cpu)}
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -384,17 +401,23 @@ def run_ours(args, rank, world, local_rank):
         if w.dtype == "bf16" else "f32", "data": "synthetic",
         "config": {"workload": w.describe(), "T": w.T, "d": w.d, "N": w.N, "f": w.f, "k": w.k,
                    "mode": w.mode, "gamma": None if math.isinf(w.gamma) else w.gamma,
-                   "kept_pairs": P, "l2": "flushed (256 MiB write) before every timed step",
+                   "kept_pairs": P,
+                   "l2": ("flushed (256 MiB write) before every timed step" if flush is not None
+                          else f"not flushed: inputs larger than L2 ({weight_bytes / 1e9:.2f} GB "
+                               f"of expert weights stream through the {l2_bytes / 2**20:.0f} MiB "
+                               "L2 every step)"),
                    "parallelism": f"replicas x{world}"},
         "tflops": ffn_flops(w, P) * args.steps * world / (total_ms / 1e3) / 1e12,
-        "roofline": {"kernel": "grouped_gemm_tc (GEMM1+SwiGLU and GEMM2, one launch each)",
+        "roofline": {"kernel": "grouped_gemm_tc_kernel (expert GEMM1+SwiGLU and GEMM2, "
+                               "one launch each per step; times from the timed steps)",
                      "bound": "tensor", "achieved": ffn_tflops, "peak": peak_tf,
-                     "unit": "TFLOP/s", "frac": ffn_tflops / peak_tf, "traffic": None,
+                     "unit": "TFLOP/s", "frac": ffn_tflops / peak_tf,
+                     "traffic": gemm_traffic(w),
                      "peak_source": f"{peak_src} bf16 burst"},
         "kernels": kernels,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": w.T * w.d * sx,
                 "d2h_bytes_per_step": w.T * w.d * sx},
-        "gpu_launches": count_launches(w) * args.steps,
+        "gpu_launches": len(stages) * args.steps,
         "clocks": clk,
         "cpu_baseline": cpu,
         "stats": {"max_over_mean": float(st[4]), "drop_fraction": float(st[5]),
@@ -485,7 +508,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.ALL))
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-sample-tokens", type=int, default=256)
+    ap.add_argument("--cpu-sample-s", type=float, default=15.0,
+                    help="seconds of oracle work in the cpu_baseline sample")
+    ap.add_argument("--reference-budget-s", type=float, default=150.0,
+                    help="--impl reference: seconds for warm-up + timed samples together")
     ap.add_argument("--distinct-batches", action="store_true",
                     help="each rank draws its own x (seed + rank)")
     ap.add_argument("--kernel", choices=["route", "select", "dispatch", "combine"],

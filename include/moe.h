@@ -308,6 +308,28 @@ int moe_layer_forward(const moe_config* cfg, const void* x, const void* W_router
                       const int32_t* home_group, float* logits, void* y, double* stats,
                       void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * Stage tracing of moe_layer_forward (profiling aid; the pages have no
+ * counterpart). moe_layer_stages returns how many kernels moe_layer_forward
+ * launches for `cfg` (with_stats: a stats pointer will be passed) and, when
+ * `names` is non-NULL, stores up to max_names static stage names in launch
+ * order: router_logits (absent with MOE_LOGITS_GIVEN), route_tokens, select,
+ * dispatch, expert_gemm1_swiglu, expert_gemm2, [shared_offsets,
+ * shared_gemm1_swiglu, shared_gemm2 when f_shared > 0], combine,
+ * [stats_partial, stats_final]. Returns a negative MOE_ERR_* for an invalid
+ * config.
+ *
+ * moe_set_trace_events hands the library n_events cudaEvent_t handles
+ * (created by the caller, which keeps ownership; n_events <= 32, 0 turns
+ * tracing off). While set, every moe_layer_forward made from the SAME host
+ * thread records events[0] on its stream before the first launch and
+ * events[i + 1] right after stage i, for the events it has; the elapsed time
+ * between consecutive events is the device time of one stage, launch gap
+ * included. Events are re-recorded by every call.
+ */
+int moe_layer_stages(const moe_config* cfg, int with_stats, const char** names, int max_names);
+int moe_set_trace_events(void* const* events, int n_events);
+
 /* Device pointers to the intermediates moe_layer_forward leaves in ws. */
 typedef struct moe_views_t {
   int32_t* status;         /* [1] sticky device status */

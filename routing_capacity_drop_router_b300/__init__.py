@@ -93,6 +93,9 @@ SIGNATURES = {
     "moe_layer_forward": (ctypes.c_int, [_CFG, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                          _VP, _VP, _VP, _VP, ctypes.c_size_t, _VP]),
     "moe_workspace_views": (ctypes.c_int, [_CFG, _VP, ctypes.POINTER(moe_views_t)]),
+    "moe_layer_stages": (ctypes.c_int, [_CFG, ctypes.c_int, ctypes.POINTER(ctypes.c_char_p),
+                                        ctypes.c_int]),
+    "moe_set_trace_events": (ctypes.c_int, [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]),
     "moe_get_device_status": (ctypes.c_int, [_VP, _VP, ctypes.POINTER(ctypes.c_int32)]),
     "moe_clear_device_status": (ctypes.c_int, [_VP, _VP]),
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -256,6 +259,31 @@ def moe_workspace_views(cfg, ws) -> moe_views_t:
     _check(lib().moe_workspace_views(ctypes.byref(cfg), _p(ws), ctypes.byref(out)),
            "moe_workspace_views")
     return out
+
+
+def moe_layer_stages(cfg, with_stats: bool = True):
+    """Names of the kernels moe_layer_forward launches for cfg, in order."""
+    n = lib().moe_layer_stages(ctypes.byref(cfg), int(bool(with_stats)), None, 0)
+    if n < 0:
+        raise MoeError(n, "moe_layer_stages")
+    names = (ctypes.c_char_p * max(n, 1))()
+    lib().moe_layer_stages(ctypes.byref(cfg), int(bool(with_stats)), names, n)
+    return [names[i].decode() for i in range(n)]
+
+
+def moe_set_trace_events(events) -> None:
+    """Record ``events`` (torch.cuda.Event with enable_timing, one more than
+    the stages) inside every later moe_layer_forward of this host thread;
+    ``None`` or ``[]`` turns tracing off. Each event must have been created
+    (recorded once) so that it has a CUDA handle."""
+    events = list(events or [])
+    handles = (ctypes.c_void_p * max(len(events), 1))()
+    for i, ev in enumerate(events):
+        h = ev if isinstance(ev, int) else ev.cuda_event
+        if not h:
+            raise ValueError("event has no CUDA handle yet: record it once first")
+        handles[i] = h
+    _check(lib().moe_set_trace_events(handles, len(events)), "moe_set_trace_events")
 
 
 def moe_get_device_status(ws, stream=None) -> int:

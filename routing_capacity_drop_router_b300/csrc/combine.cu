@@ -3,7 +3,8 @@
 // MoE differs from the Transformer").
 //
 // One warp per token; the token's rows (ascending expert) and gates are staged
-// in shared memory, then each lane walks 16-byte column vectors: for every row
+// in shared memory, then each lane walks 16-byte column vectors (four per
+// pass, the loads of up to four rows issued before their FMAs): for every row
 // an FMA into fp32 accumulators in a fixed order (ascending expert, shared
 // expert last), one rounding to the output dtype at the end.
 #include <cuda_bf16.h>
@@ -18,6 +19,8 @@ namespace {
 constexpr int kCombThreads = 256;
 constexpr int kCombWarps = kCombThreads / 32;
 constexpr int kCombMaxRows = 256;
+constexpr int kU = 4;   // 16-byte column vectors per lane per pass
+constexpr int kRB = 4;  // rows loaded per batch
 
 template <typename E> struct Pack;  // 16 bytes of E <-> fp32
 template <> struct Pack<__nv_bfloat16> {
@@ -80,25 +83,55 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(
     const uint4* sh = shared_out ? reinterpret_cast<const uint4*>(shared_out + static_cast<size_t>(t) * d)
                                  : nullptr;
     uint4* dst = reinterpret_cast<uint4*>(y + static_cast<size_t>(t) * d);
-    for (int c = lane; c < nvec; c += 32) {
-      float acc[V];
+    // kU column vectors per lane and up to kRB rows loaded before their FMAs,
+    // so each lane keeps kU * kRB 16-byte loads in flight
+    for (int c0 = lane; c0 < nvec; c0 += 32 * kU) {
+      float acc[kU][V];
 #pragma unroll
-      for (int i = 0; i < V; ++i) acc[i] = 0.f;
-      for (int r = 0; r < nrows; ++r) {
-        const uint4 q = __ldg(reinterpret_cast<const uint4*>(op + static_cast<size_t>(s_row[wib][r]) * d) + c);
-        float v[V];
-        Pack<E>::unpack(q, v);
-        const float g = s_gate[wib][r];
+      for (int u = 0; u < kU; ++u)
 #pragma unroll
-        for (int i = 0; i < V; ++i) acc[i] = fmaf(g, v[i], acc[i]);
+        for (int i = 0; i < V; ++i) acc[u][i] = 0.f;
+      for (int r0 = 0; r0 < nrows; r0 += kRB) {
+        uint4 q[kRB][kU];
+#pragma unroll
+        for (int rr = 0; rr < kRB; ++rr) {
+          if (r0 + rr < nrows) {
+            const uint4* src =
+                reinterpret_cast<const uint4*>(op + static_cast<size_t>(s_row[wib][r0 + rr]) * d);
+#pragma unroll
+            for (int u = 0; u < kU; ++u)
+              if (c0 + 32 * u < nvec) q[rr][u] = __ldg(src + c0 + 32 * u);
+          }
+        }
+#pragma unroll
+        for (int rr = 0; rr < kRB; ++rr) {
+          if (r0 + rr < nrows) {
+            const float g = s_gate[wib][r0 + rr];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+              if (c0 + 32 * u < nvec) {
+                float v[V];
+                Pack<E>::unpack(q[rr][u], v);
+#pragma unroll
+                for (int i = 0; i < V; ++i) acc[u][i] = fmaf(g, v[i], acc[u][i]);
+              }
+            }
+          }
+        }
       }
-      if (sh) {
-        float v[V];
-        Pack<E>::unpack(__ldg(sh + c), v);
 #pragma unroll
-        for (int i = 0; i < V; ++i) acc[i] += v[i];
+      for (int u = 0; u < kU; ++u) {
+        const int c = c0 + 32 * u;
+        if (c < nvec) {
+          if (sh) {
+            float v[V];
+            Pack<E>::unpack(__ldg(sh + c), v);
+#pragma unroll
+            for (int i = 0; i < V; ++i) acc[u][i] += v[i];
+          }
+          dst[c] = Pack<E>::pack(acc[u]);
+        }
       }
-      dst[c] = Pack<E>::pack(acc);
     }
     __syncwarp();
   }

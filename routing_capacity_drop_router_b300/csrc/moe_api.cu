@@ -91,6 +91,50 @@ int validate(const moe_config* c, Derived* dv) {
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// Stage timing of moe_layer_forward (moe_set_trace_events): caller-owned
+// events, per host thread.
+constexpr int kMaxTraceEvents = 32;
+thread_local cudaEvent_t g_trace_events[kMaxTraceEvents];
+thread_local int g_trace_n = 0;
+
+// Records the trace events of one moe_layer_forward: event 0 before the first
+// launch, event i + 1 after stage i (no-op when no events are set).
+struct Tracer {
+  cudaStream_t s;
+  int next = 0;
+  bool mark(int stages = 1) {
+    for (int j = 0; j < stages; ++j, ++next)
+      if (next < g_trace_n && cudaEventRecord(g_trace_events[next], s) != cudaSuccess)
+        return false;
+    return true;
+  }
+};
+
+// The kernels moe_layer_forward launches for c, in launch order.
+int layer_stage_names(const moe_config& c, bool with_stats, const char** names, int max_names) {
+  const char* list[16];
+  int n = 0;
+  if (!(c.flags & MOE_LOGITS_GIVEN)) list[n++] = "router_logits";
+  list[n++] = "route_tokens";
+  list[n++] = "select";
+  list[n++] = "dispatch";
+  list[n++] = "expert_gemm1_swiglu";
+  list[n++] = "expert_gemm2";
+  if (c.f_shared > 0) {
+    list[n++] = "shared_offsets";
+    list[n++] = "shared_gemm1_swiglu";
+    list[n++] = "shared_gemm2";
+  }
+  list[n++] = "combine";
+  if (with_stats) {
+    list[n++] = "stats_partial";
+    list[n++] = "stats_final";
+  }
+  if (names)
+    for (int i = 0; i < n && i < max_names; ++i) names[i] = list[i];
+  return n;
+}
+
 int status_from(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH; }
 
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
@@ -106,9 +150,10 @@ size_t router_partial_bytes(const moe_config& c) {
 // input when MOE_LOGITS_GIVEN. partial: router scratch (router_partial_bytes).
 int run_router(const moe_config& c, bool ec, const void* x, const void* W_r, const float* bias,
                float* logits, float* scores, int32_t* cand_idx, float* cand_gate,
-               const int32_t* home_group, float* partial, int32_t* status, cudaStream_t s) {
-  if (c.T == 0) return MOE_OK;
+               const int32_t* home_group, float* partial, int32_t* status, cudaStream_t s,
+               Tracer* tr = nullptr) {
   const bool given = (c.flags & MOE_LOGITS_GIVEN) != 0;
+  if (c.T == 0) return (!tr || tr->mark(given ? 1 : 2)) ? MOE_OK : MOE_ERR_LAUNCH;
   const float* src = logits;
   int nsplit = 1;
   const float* add_bias = nullptr;
@@ -116,20 +161,25 @@ int run_router(const moe_config& c, bool ec, const void* x, const void* W_r, con
   if (!given) {
     if (router_tc_supported(c.dtype, c.d, c.N)) {
       const RouterSplit p = router_split_plan(c.T, c.d, c.N);
-      if (launch_router_logits_tc(x, W_r, c.T, c.d, c.N, p, partial, status, s) != cudaSuccess)
+      if (launch_router_logits_tc(x, W_r, c.T, c.d, c.N, p, partial, status, s) != cudaSuccess ||
+          (tr && !tr->mark()))
         return MOE_ERR_LAUNCH;
       src = partial;
       nsplit = p.splits;
       add_bias = bias;
       logits_out = logits;
     } else if (launch_router_logits(c.dtype, x, W_r, bias, logits, c.T, c.d, c.N, s) !=
-               cudaSuccess) {
+                   cudaSuccess ||
+               (tr && !tr->mark())) {
       return MOE_ERR_LAUNCH;
     }
   }
-  return status_from(launch_route_tokens(src, nsplit, add_bias, logits_out, scores, cand_idx,
-                                         cand_gate, home_group, c.T, c.N, c.k, c.m, c.group_size,
-                                         c.renorm, ec ? 1 : 0, s));
+  if (launch_route_tokens(src, nsplit, add_bias, logits_out, scores, cand_idx, cand_gate,
+                          home_group, c.T, c.N, c.k, c.m, c.group_size, c.renorm, ec ? 1 : 0,
+                          s) != cudaSuccess ||
+      (tr && !tr->mark()))
+    return MOE_ERR_LAUNCH;
+  return MOE_OK;
 }
 
 struct Layout {
@@ -180,22 +230,23 @@ P* at(void* ws, size_t off) {
 // FFN over expert-contiguous rows; hp is scratch of rows_max * f elements.
 int run_ffn(int dtype, const void* xp, const int32_t* offsets, int S, int64_t rows_max, int d,
             int f, const void* W1, const void* W3, const void* W2, void* hp, void* op,
-            int32_t* status, cudaStream_t s) {
+            int32_t* status, cudaStream_t s, Tracer* tr = nullptr) {
   cudaError_t e;
   if (dtype == MOE_BF16) {
     e = launch_grouped_gemm_tc_bf16(xp, offsets, S, rows_max, d, f, W1, W3, hp, true, status, s);
-    if (e != cudaSuccess) return MOE_ERR_LAUNCH;
+    if (e != cudaSuccess || (tr && !tr->mark())) return MOE_ERR_LAUNCH;
     e = launch_grouped_gemm_tc_bf16(hp, offsets, S, rows_max, f, d, W2, nullptr, op, false, status, s);
   } else {
     e = launch_grouped_gemm_simt_f32(static_cast<const float*>(xp), offsets, S, rows_max, d, f,
                                      static_cast<const float*>(W1), static_cast<const float*>(W3),
                                      static_cast<float*>(hp), true, s);
-    if (e != cudaSuccess) return MOE_ERR_LAUNCH;
+    if (e != cudaSuccess || (tr && !tr->mark())) return MOE_ERR_LAUNCH;
     e = launch_grouped_gemm_simt_f32(static_cast<const float*>(hp), offsets, S, rows_max, f, d,
                                      static_cast<const float*>(W2), nullptr,
                                      static_cast<float*>(op), false, s);
   }
-  return status_from(e);
+  if (e != cudaSuccess || (tr && !tr->mark())) return MOE_ERR_LAUNCH;
+  return MOE_OK;
 }
 
 }  // namespace
@@ -372,6 +423,8 @@ int moe_layer_forward(const moe_config* cfg, const void* x, const void* W_router
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
 
   cudaStream_t s = as_stream(stream);
+  Tracer tr{s};
+  if (!tr.mark()) return MOE_ERR_LAUNCH;
   int32_t* status = at<int32_t>(ws, L.status);
   float* Lg = given ? logits : (logits ? logits : at<float>(ws, L.logits));
   float* scores = at<float>(ws, L.scores);
@@ -391,31 +444,59 @@ int moe_layer_forward(const moe_config* cfg, const void* x, const void* W_router
   void* ys = c.f_shared > 0 ? at<void>(ws, L.shared_out) : nullptr;
 
   st = run_router(c, d.ec, x, W_router, bias, Lg, scores, cand_idx, cand_gate, home_group,
-                  at<float>(ws, L.router_partial), status, s);
+                  at<float>(ws, L.router_partial), status, s, &tr);
   if (st != MOE_OK) return st;
   if (launch_select(cand_idx, cand_gate, c.T, d.kc, c.N, d.ec ? 1 : 0, d.cap, slot, keep, demand,
-                    kept, s) != cudaSuccess)
+                    kept, s) != cudaSuccess || !tr.mark(1))
     return MOE_ERR_LAUNCH;
   if (launch_dispatch(c.dtype, x, cand_idx, cand_gate, slot, kept, c.T, c.d, c.N, d.kc,
                       d.ec ? 1 : 0, d.rows_max, offsets, row_token, row_gate, tok_rows, xp,
-                      s) != cudaSuccess)
+                      s) != cudaSuccess || !tr.mark(1))
     return MOE_ERR_LAUNCH;
-  st = run_ffn(c.dtype, xp, offsets, c.N, d.rows_max, c.d, c.f, W1, W3, W2, hp, op, status, s);
+  st = run_ffn(c.dtype, xp, offsets, c.N, d.rows_max, c.d, c.f, W1, W3, W2, hp, op, status, s,
+               &tr);
   if (st != MOE_OK) return st;
-  if (c.f_shared > 0 && c.T > 0) {
-    int32_t* soff = at<int32_t>(ws, L.shared_offsets);
-    write_pair_kernel<<<1, 1, 0, s>>>(soff, 0, c.T);
-    st = run_ffn(c.dtype, x, soff, 1, c.T, c.d, c.f_shared, Ws1, Ws3, Ws2, hp, ys, status, s);
-    if (st != MOE_OK) return st;
+  if (c.f_shared > 0) {
+    if (c.T > 0) {
+      int32_t* soff = at<int32_t>(ws, L.shared_offsets);
+      write_pair_kernel<<<1, 1, 0, s>>>(soff, 0, c.T);
+      if (cudaGetLastError() != cudaSuccess || !tr.mark(1)) return MOE_ERR_LAUNCH;
+      st = run_ffn(c.dtype, x, soff, 1, c.T, c.d, c.f_shared, Ws1, Ws3, Ws2, hp, ys, status, s,
+                   &tr);
+      if (st != MOE_OK) return st;
+    } else if (!tr.mark(3)) {
+      return MOE_ERR_LAUNCH;
+    }
   }
   if (launch_combine(c.dtype, op, row_gate, tok_rows, ys, y, c.T, c.d, d.kc, d.rows_max, s) !=
-      cudaSuccess)
+          cudaSuccess ||
+      !tr.mark(1))
     return MOE_ERR_LAUNCH;
   if (stats) {
     if (launch_stats(demand, kept, scores, c.T, c.N, at<double>(ws, L.stats_partial), stats, s) !=
-        cudaSuccess)
+            cudaSuccess ||
+        !tr.mark(2))
       return MOE_ERR_LAUNCH;
   }
+  return MOE_OK;
+}
+
+int moe_layer_stages(const moe_config* cfg, int with_stats, const char** names,
+                     int max_names) {
+  const int st = validate(cfg, nullptr);
+  if (st != MOE_OK) return st;
+  if (max_names < 0) return MOE_ERR_SHAPE;
+  return layer_stage_names(*cfg, with_stats != 0, names, max_names);
+}
+
+int moe_set_trace_events(void* const* events, int n_events) {
+  if (n_events < 0 || n_events > kMaxTraceEvents) return MOE_ERR_SHAPE;
+  if (n_events > 0 && !events) return MOE_ERR_NULL;
+  for (int i = 0; i < n_events; ++i) {
+    if (!events[i]) return MOE_ERR_NULL;
+  }
+  for (int i = 0; i < n_events; ++i) g_trace_events[i] = static_cast<cudaEvent_t>(events[i]);
+  g_trace_n = n_events;
   return MOE_OK;
 }
 

@@ -38,22 +38,38 @@ __global__ void __launch_bounds__(256) stats_final_kernel(const int32_t* __restr
                                                           int nblocks, int T, int N,
                                                           double* __restrict__ stats) {
   __shared__ double psum[256];
+  __shared__ double s_kept[256], s_dem[256];
   if (threadIdx.x < N) {
+    // partials in block order; four independent loads in flight
+    const int e = threadIdx.x;
     double acc = 0.0;
-    for (int b = 0; b < nblocks; ++b) acc += partial[static_cast<size_t>(b) * N + threadIdx.x];
-    psum[threadIdx.x] = acc;
+    int b = 0;
+    for (; b + 4 <= nblocks; b += 4) {
+      const double v0 = partial[static_cast<size_t>(b) * N + e];
+      const double v1 = partial[static_cast<size_t>(b + 1) * N + e];
+      const double v2 = partial[static_cast<size_t>(b + 2) * N + e];
+      const double v3 = partial[static_cast<size_t>(b + 3) * N + e];
+      acc += v0;
+      acc += v1;
+      acc += v2;
+      acc += v3;
+    }
+    for (; b < nblocks; ++b) acc += partial[static_cast<size_t>(b) * N + e];
+    psum[e] = acc;
+    s_kept[e] = static_cast<double>(kept[e]);
+    s_dem[e] = static_cast<double>(demand[e]);
   }
   __syncthreads();
   if (threadIdx.x == 0) {
     double P = 0, D = 0, mx = 0;
     for (int e = 0; e < N; ++e) {
-      P += kept[e];
-      D += demand[e];
-      mx = fmax(mx, static_cast<double>(kept[e]));
+      P += s_kept[e];
+      D += s_dem[e];
+      mx = fmax(mx, s_kept[e]);
     }
     double B = 0;
     if (D > 0 && T > 0)
-      for (int e = 0; e < N; ++e) B += (demand[e] / D) * (psum[e] / T);
+      for (int e = 0; e < N; ++e) B += (s_dem[e] / D) * (psum[e] / T);
     const double mean = P / N;
     stats[0] = P;
     stats[1] = D;

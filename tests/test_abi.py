@@ -131,3 +131,23 @@ def test_status_strings():
     for code in range(-8, 1):
         assert M.status_string(code) and M.status_string(code) != "unknown status"
     assert M.status_string(-99) == "unknown status"
+
+
+def test_layer_stage_list_follows_the_config():
+    names = M.moe_layer_stages(_cfg(), with_stats=True)
+    assert names == ["router_logits", "route_tokens", "select", "dispatch", "expert_gemm1_swiglu",
+                     "expert_gemm2", "combine", "stats_partial", "stats_final"]
+    names = M.moe_layer_stages(_cfg(f_shared=128, logits_given=True), with_stats=False)
+    assert names == ["route_tokens", "select", "dispatch", "expert_gemm1_swiglu", "expert_gemm2",
+                     "shared_offsets", "shared_gemm1_swiglu", "shared_gemm2", "combine"]
+    assert M.lib().moe_layer_stages(ctypes.byref(_cfg(N=0)), 1, None, 0) == M.MOE_ERR_SHAPE
+
+
+def test_trace_event_arguments_checked_on_the_host():
+    lib = M.lib()
+    assert lib.moe_set_trace_events(None, 0) == M.MOE_OK
+    assert lib.moe_set_trace_events(None, 3) == M.MOE_ERR_NULL
+    assert lib.moe_set_trace_events(None, -1) == M.MOE_ERR_SHAPE
+    handles = (ctypes.c_void_p * 40)()
+    assert lib.moe_set_trace_events(handles, 33) == M.MOE_ERR_SHAPE
+    assert lib.moe_set_trace_events(handles, 2) == M.MOE_ERR_NULL  # NULL handles

@@ -108,3 +108,31 @@ def test_benchmark_workloads_full_size(name, sample):
         tokens = np.sort(rng.choice(w.T, size=sample, replace=False))
     L, ref, _ = _check_layer(w, inp, tokens=tokens)
     _check_own_logits(w, inp, L, ref, tokens=tokens)
+
+
+def test_trace_events_time_every_stage():
+    """moe_set_trace_events: one event before the first kernel and one after
+    each stage, in launch order, on the call's stream."""
+    w = SMALL[3]  # expanded drop + shared expert: the longest stage list
+    inp = W.make_inputs(w)
+    cfg = G.M.config_from_workload(w)
+    names = G.M.moe_layer_stages(cfg, with_stats=True)
+    d = {k: G.cuda(v) for k, v in inp.items()}
+    ws = torch.zeros(G.M.workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    y = torch.empty((w.T, w.d), dtype=torch.bfloat16, device="cuda")
+    stats = torch.zeros(G.M.MOE_STATS_LEN, dtype=torch.float64, device="cuda")
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+    for e in evs:
+        e.record()
+    torch.cuda.synchronize()
+    G.M.moe_set_trace_events(evs)
+    try:
+        G.M.moe_layer_forward(cfg, d["x"], d["W_r"], d["bias"], d["W1"], d["W3"], d["W2"],
+                              d["Ws1"], d["Ws3"], d["Ws2"], y, ws, stats=stats)
+    finally:
+        G.M.moe_set_trace_events(None)
+    torch.cuda.synchronize()
+    ms = [evs[i].elapsed_time(evs[i + 1]) for i in range(len(names))]
+    assert all(m >= 0 for m in ms)
+    assert evs[0].elapsed_time(evs[-1]) > 0
+    assert G.M.moe_get_device_status(ws) == G.M.MOE_OK
