@@ -118,7 +118,16 @@ int moe_sizes(const moe_config* cfg, moe_sizes_t* out);
 /* Bytes of workspace moe_layer_forward needs (0 if the config is invalid). */
 size_t moe_workspace_size(const moe_config* cfg);
 
-/* Bytes of workspace moe_route needs (its status word and, for the
+/* Every workspace (moe_layer_forward, moe_route, moe_expert_ffn,
+ * moe_grouped_gemm) begins with a 1024-byte control block: the sticky status
+ * word and the arrival counters of kernels whose last block finishes the step
+ * (the tensor-core router's per-tile routing, the load statistics). The
+ * control block must be zero before the workspace's first use (allocate it
+ * zeroed, or call moe_clear_device_status); every call leaves the counters at
+ * zero again. Calls that share a workspace must not overlap on the GPU. */
+#define MOE_CTRL_BYTES 1024
+
+/* Bytes of workspace moe_route needs (the control block and, for the
  * tensor-core router, the per-split partial logits). */
 size_t moe_route_workspace_size(const moe_config* cfg);
 
@@ -149,9 +158,11 @@ size_t moe_ffn_workspace_size(int64_t rows_max, int32_t f, int32_t dtype);
  *            drop; NULL = contiguous shards, group floor(t*G/T), G = N/group_size.
  *   ws       >= moe_route_workspace_size(cfg) bytes, 256-byte aligned.
  * bf16 layers with N a multiple of 8 compute the logits on the tcgen05 tensor
- * cores, the d axis split over several CTAs per 128-token tile; the splits'
- * fp32 partials are added in a fixed order, then the bias. Other shapes use
- * fp32 FMA. Either way L is fp32-accumulated, not the exact dot product.
+ * cores, the d axis split over several CTAs per 128-token tile; the last CTA
+ * of each tile to finish adds the splits' fp32 partials in a fixed order, then
+ * the bias, and routes the tile's tokens in the same launch. Other shapes use
+ * fp32 FMA and a second kernel for the routing. Either way L is
+ * fp32-accumulated, not the exact dot product.
  */
 int moe_route(const moe_config* cfg, const void* x, const void* W_router, const float* bias,
               float* logits, float* scores, int32_t* cand_idx, float* cand_gate,
@@ -215,7 +226,8 @@ int moe_dispatch(const moe_config* cfg, const void* x, const int32_t* cand_idx,
  *   f            hidden width of these experts
  *   W1, W3       [n_segments, d, f] dtype;  W2 [n_segments, f, d] dtype
  *   op           [rows_max, d] dtype out (rows >= offsets[n_segments] untouched)
- *   ws           >= moe_ffn_workspace_size(rows_max, f, dtype) bytes
+ *   ws           >= moe_ffn_workspace_size(rows_max, f, dtype) bytes (control
+ *                block, then the hidden activations)
  * bf16 runs on the tcgen05 tensor cores (fp32 accumulate in tensor memory);
  * fp32 runs on the fp32 FMA pipes.
  */
@@ -280,7 +292,10 @@ int moe_combine(const moe_config* cfg, const void* op, const float* row_gate,
 
 /*
  * Load statistics of one routed batch into stats[MOE_STATS_LEN] (device
- * doubles; layout above). scores [T, N] are the router probabilities.
+ * doubles; layout above). scores [T, N] are the router probabilities; their
+ * column sums are taken in fixed point (units of 2^-40, exact u64 sums), so
+ * P_i does not depend on the order of the additions.
+ * ws >= 8 * N * ceil(T / 128) bytes, 16-byte aligned (scratch).
  */
 int moe_load_stats(const moe_config* cfg, const int32_t* demand, const int32_t* kept,
                    const float* scores, double* stats, void* ws, size_t ws_bytes, void* stream);
@@ -311,23 +326,27 @@ int moe_layer_forward(const moe_config* cfg, const void* x, const void* W_router
 /*
  * Stage tracing of moe_layer_forward (profiling aid; the pages have no
  * counterpart). moe_layer_stages returns how many kernels moe_layer_forward
- * launches for `cfg` (with_stats: a stats pointer will be passed) and, when
- * `names` is non-NULL, stores up to max_names static stage names in launch
- * order: router_logits (absent with MOE_LOGITS_GIVEN), route_tokens, select,
- * dispatch, expert_gemm1_swiglu, expert_gemm2, [shared_offsets,
- * shared_gemm1_swiglu, shared_gemm2 when f_shared > 0], combine,
- * [stats_partial, stats_final]. Returns a negative MOE_ERR_* for an invalid
- * config.
+ * launches for `cfg` and, when `names` is non-NULL, stores up to max_names
+ * static stage names in launch order: the routing ("router" for the fused
+ * tensor-core router, "router_logits" + "route_tokens" on the FMA path,
+ * "route_tokens" alone with MOE_LOGITS_GIVEN), select (which also finishes
+ * the load statistics when a stats pointer is passed), dispatch,
+ * expert_gemm1_swiglu, expert_gemm2, [shared_offsets, shared_gemm1_swiglu,
+ * shared_gemm2 when f_shared > 0], combine. Returns a negative MOE_ERR_* for
+ * an invalid config.
  *
  * moe_set_trace_events hands the library n_events cudaEvent_t handles
  * (created by the caller, which keeps ownership; n_events <= 32, 0 turns
- * tracing off). While set, every moe_layer_forward made from the SAME host
- * thread records events[0] on its stream before the first launch and
- * events[i + 1] right after stage i, for the events it has; the elapsed time
- * between consecutive events is the device time of one stage, launch gap
- * included. Events are re-recorded by every call.
+ * tracing off; a NULL entry records nothing at that point). While set, every
+ * moe_layer_forward made from the SAME host thread records events[0] on its
+ * stream before the first launch and events[i + 1] right after stage i, for
+ * the events it has; the elapsed time between consecutive events is the
+ * device time of one stage, launch gap included. Events are re-recorded by
+ * every call. The kernels are launched with programmatic dependent launch, so
+ * without events a kernel's launch and set-up overlap the previous kernel; an
+ * event between two stages serialises them.
  */
-int moe_layer_stages(const moe_config* cfg, int with_stats, const char** names, int max_names);
+int moe_layer_stages(const moe_config* cfg, const char** names, int max_names);
 int moe_set_trace_events(void* const* events, int n_events);
 
 /* Device pointers to the intermediates moe_layer_forward leaves in ws. */
@@ -355,12 +374,12 @@ int moe_workspace_views(const moe_config* cfg, void* ws, moe_views_t* out);
 
 /* Enqueue a read of the sticky device status word at ws and synchronise
  * `stream`; *out_host receives MOE_OK or the first MOE_ERR_DEVICE_* recorded.
- * `ws` is any workspace passed to the calls above. The status word is the
- * first 4 bytes of the workspace: zero the workspace, or call
- * moe_clear_device_status, before its first use. */
+ * `ws` is any workspace passed to the calls above; the status word is the
+ * first 4 bytes of its control block. */
 int moe_get_device_status(const void* ws, void* stream, int32_t* out_host);
 
-/* Enqueue a reset of the sticky device status word at ws to MOE_OK. */
+/* Enqueue a reset of ws's control block (MOE_CTRL_BYTES: status word and
+ * arrival counters) to zero. */
 int moe_clear_device_status(void* ws, void* stream);
 
 /* Static description of a status code. */

@@ -34,6 +34,7 @@ MOE_F32 = 0
 MOE_BF16 = 1
 MOE_LOGITS_GIVEN = 1
 MOE_STATS_LEN = 8
+MOE_CTRL_BYTES = 1024
 MOE_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 MODES = {"token_choice": MOE_TOKEN_CHOICE, "expert_choice": MOE_EXPERT_CHOICE,
@@ -93,8 +94,7 @@ SIGNATURES = {
     "moe_layer_forward": (ctypes.c_int, [_CFG, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                          _VP, _VP, _VP, _VP, ctypes.c_size_t, _VP]),
     "moe_workspace_views": (ctypes.c_int, [_CFG, _VP, ctypes.POINTER(moe_views_t)]),
-    "moe_layer_stages": (ctypes.c_int, [_CFG, ctypes.c_int, ctypes.POINTER(ctypes.c_char_p),
-                                        ctypes.c_int]),
+    "moe_layer_stages": (ctypes.c_int, [_CFG, ctypes.POINTER(ctypes.c_char_p), ctypes.c_int]),
     "moe_set_trace_events": (ctypes.c_int, [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]),
     "moe_get_device_status": (ctypes.c_int, [_VP, _VP, ctypes.POINTER(ctypes.c_int32)]),
     "moe_clear_device_status": (ctypes.c_int, [_VP, _VP]),
@@ -261,24 +261,27 @@ def moe_workspace_views(cfg, ws) -> moe_views_t:
     return out
 
 
-def moe_layer_stages(cfg, with_stats: bool = True):
+def moe_layer_stages(cfg):
     """Names of the kernels moe_layer_forward launches for cfg, in order."""
-    n = lib().moe_layer_stages(ctypes.byref(cfg), int(bool(with_stats)), None, 0)
+    n = lib().moe_layer_stages(ctypes.byref(cfg), None, 0)
     if n < 0:
         raise MoeError(n, "moe_layer_stages")
     names = (ctypes.c_char_p * max(n, 1))()
-    lib().moe_layer_stages(ctypes.byref(cfg), int(bool(with_stats)), names, n)
+    lib().moe_layer_stages(ctypes.byref(cfg), names, n)
     return [names[i].decode() for i in range(n)]
 
 
 def moe_set_trace_events(events) -> None:
     """Record ``events`` (torch.cuda.Event with enable_timing, one more than
-    the stages) inside every later moe_layer_forward of this host thread;
-    ``None`` or ``[]`` turns tracing off. Each event must have been created
-    (recorded once) so that it has a CUDA handle."""
+    the stages; ``None`` entries record nothing at that boundary) inside every
+    later moe_layer_forward of this host thread; ``None`` or ``[]`` turns
+    tracing off. Each event must have been created (recorded once) so that it
+    has a CUDA handle."""
     events = list(events or [])
     handles = (ctypes.c_void_p * max(len(events), 1))()
     for i, ev in enumerate(events):
+        if ev is None:
+            continue  # no event at this stage boundary
         h = ev if isinstance(ev, int) else ev.cuda_event
         if not h:
             raise ValueError("event has no CUDA handle yet: record it once first")

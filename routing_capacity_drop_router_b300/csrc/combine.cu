@@ -60,6 +60,8 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(
     const int32_t* __restrict__ tok_rows, const E* __restrict__ shared_out, E* __restrict__ y,
     int T, int d, int kc, int rows_max) {
   constexpr int V = Pack<E>::n;
+  pdl_launch_dependents();
+  pdl_wait();
   __shared__ int s_row[kCombWarps][kCombMaxRows];
   __shared__ float s_gate[kCombWarps][kCombMaxRows];
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
@@ -148,13 +150,15 @@ cudaError_t launch_combine(int dtype, const void* op, const float* row_gate,
   const int cap = device_sm_count() * 8;
   if (blocks > cap) blocks = cap;
   if (dtype == 1) {
-    combine_kernel<__nv_bfloat16><<<blocks, kCombThreads, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(op), row_gate, tok_rows,
-        static_cast<const __nv_bfloat16*>(shared_out), static_cast<__nv_bfloat16*>(y), T, d, kc, rmax);
+    return launch_pdl(combine_kernel<__nv_bfloat16>, blocks, kCombThreads, 0, s,
+                      static_cast<const __nv_bfloat16*>(op), row_gate, tok_rows,
+                      static_cast<const __nv_bfloat16*>(shared_out),
+                      static_cast<__nv_bfloat16*>(y), T, d, kc, rmax);
   } else {
-    combine_kernel<float><<<blocks, kCombThreads, 0, s>>>(
-        static_cast<const float*>(op), row_gate, tok_rows, static_cast<const float*>(shared_out),
-        static_cast<float*>(y), T, d, kc, rmax);
+    return launch_pdl(combine_kernel<float>, blocks, kCombThreads, 0, s,
+                      static_cast<const float*>(op), row_gate, tok_rows,
+                      static_cast<const float*>(shared_out), static_cast<float*>(y), T, d, kc,
+                      rmax);
   }
   return cudaGetLastError();
 }

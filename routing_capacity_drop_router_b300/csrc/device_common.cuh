@@ -64,6 +64,16 @@ __device__ __forceinline__ uint32_t order_key(float v) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// ---- programmatic dependent launch ----------------------------------------
+// pdl_wait: block until the previous kernel on the stream has completed and
+// its writes are visible (a no-op when the launch was not programmatic).
+// pdl_launch_dependents: allow the next kernel to be scheduled now; it still
+// waits in its own pdl_wait before reading anything this kernel writes.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- sticky status --------------------------------------------------------
 __device__ __forceinline__ void record_status(int32_t* status, int32_t code) {
   if (status) atomicCAS(status, 0, code);

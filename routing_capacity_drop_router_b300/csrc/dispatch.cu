@@ -61,6 +61,8 @@ __global__ void __launch_bounds__(kDispThreads) dispatch_kernel(
     float* __restrict__ row_gate, int32_t* __restrict__ tok_rows, E* __restrict__ xp) {
   __shared__ int s_off[257];
   __shared__ int s_rows[kDispWarps][kMaxRowsPerToken];
+  pdl_launch_dependents();
+  pdl_wait();
   scan_offsets(kept, N, s_off);
   if (blockIdx.x == 0)
     for (int e = threadIdx.x; e <= N; e += blockDim.x) expert_offsets[e] = s_off[e];
@@ -153,16 +155,15 @@ cudaError_t launch_dispatch(int dtype, const void* x, const int32_t* cand_idx,
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;  // still writes expert_offsets when T == 0
   if (dtype == 1) {
-    dispatch_kernel<__nv_bfloat16><<<blocks, kDispThreads, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(x), cand_idx, cand_gate, slot, kept, T, d, N, kc,
-        expert_choice, rmax, expert_offsets, row_token, row_gate, tok_rows,
-        static_cast<__nv_bfloat16*>(xp));
-  } else {
-    dispatch_kernel<float><<<blocks, kDispThreads, 0, s>>>(
-        static_cast<const float*>(x), cand_idx, cand_gate, slot, kept, T, d, N, kc,
-        expert_choice, rmax, expert_offsets, row_token, row_gate, tok_rows, static_cast<float*>(xp));
+    return launch_pdl(dispatch_kernel<__nv_bfloat16>, blocks, kDispThreads, 0, s,
+                      static_cast<const __nv_bfloat16*>(x), cand_idx, cand_gate, slot, kept, T, d,
+                      N, kc, expert_choice, rmax, expert_offsets, row_token, row_gate, tok_rows,
+                      static_cast<__nv_bfloat16*>(xp));
   }
-  return cudaGetLastError();
+  return launch_pdl(dispatch_kernel<float>, blocks, kDispThreads, 0, s,
+                    static_cast<const float*>(x), cand_idx, cand_gate, slot, kept, T, d, N, kc,
+                    expert_choice, rmax, expert_offsets, row_token, row_gate, tok_rows,
+                    static_cast<float*>(xp));
 }
 
 }  // namespace moe

@@ -26,6 +26,8 @@ __global__ void __launch_bounds__(256) grouped_gemm_f32_kernel(
   __shared__ float As[kTK][kTM + 4];
   __shared__ float B1s[kTK][kTN];
   __shared__ float B3s[SWIGLU ? kTK : 1][SWIGLU ? kTN : 1];
+  pdl_launch_dependents();
+  pdl_wait();
   if (threadIdx.x == 0) {
     int tile = blockIdx.x, acc = 0;
     s_seg = -1;
@@ -117,11 +119,10 @@ cudaError_t launch_grouped_gemm_simt_f32(const float* A, const int32_t* offsets,
   const int rmax = rows_max > 0x7fffffff ? 0x7fffffff : static_cast<int>(rows_max);
   const dim3 grid(static_cast<unsigned>(mt), (n_out + kTN - 1) / kTN);
   if (swiglu)
-    grouped_gemm_f32_kernel<true><<<grid, 256, 0, s>>>(A, offsets, S, K, n_out, rmax, B1, B3, out);
-  else
-    grouped_gemm_f32_kernel<false><<<grid, 256, 0, s>>>(A, offsets, S, K, n_out, rmax, B1, nullptr,
-                                                        out);
-  return cudaGetLastError();
+    return launch_pdl(grouped_gemm_f32_kernel<true>, grid, 256, 0, s, A, offsets, S, K, n_out,
+                      rmax, B1, B3, out);
+  return launch_pdl(grouped_gemm_f32_kernel<false>, grid, 256, 0, s, A, offsets, S, K, n_out,
+                    rmax, B1, static_cast<const float*>(nullptr), out);
 }
 
 }  // namespace moe

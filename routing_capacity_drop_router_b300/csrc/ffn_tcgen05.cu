@@ -114,6 +114,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
+  // barrier set-up overlaps the previous kernel; the offsets come from it
+  pdl_launch_dependents();
+  pdl_wait();
   if (warp == 0) {  // tile table: running count of m-tiles x n-tiles per segment
     int run = 0;
     for (int s0 = 0; s0 < S; s0 += 32) {
@@ -367,12 +370,10 @@ cudaError_t launch_grouped_gemm_tc_bf16(const void* A, const int32_t* offsets, i
   __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
   const int rmax = rows_max > 0x7fffffff ? 0x7fffffff : static_cast<int>(rows_max);
   if (swiglu)
-    grouped_gemm_tc_kernel<true><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, s>>>(
-        mA, mB1, mB3, offsets, S, K, n_out, rmax, o, status);
-  else
-    grouped_gemm_tc_kernel<false><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, s>>>(
-        mA, mB1, mB3, offsets, S, K, n_out, rmax, o, status);
-  return cudaGetLastError();
+    return launch_pdl(grouped_gemm_tc_kernel<true>, static_cast<unsigned>(grid), kThreads,
+                      kSmemBytes, s, mA, mB1, mB3, offsets, S, K, n_out, rmax, o, status);
+  return launch_pdl(grouped_gemm_tc_kernel<false>, static_cast<unsigned>(grid), kThreads,
+                    kSmemBytes, s, mA, mB1, mB3, offsets, S, K, n_out, rmax, o, status);
 }
 
 }  // namespace moe

@@ -7,36 +7,112 @@
 
 namespace moe {
 
+// Launches kernel<<<grid, block, smem, s>>>(args...) with programmatic
+// dependent launch allowed: the kernel may be scheduled while the previous
+// kernel on the stream finishes, and every kernel of this library waits
+// (griddepcontrol.wait, pdl_wait) before it touches global memory, so the
+// overlap covers only launch latency and set-up.
+template <typename... P, typename... A>
+cudaError_t launch_pdl(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       A&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<A&&>(args)...);
+}
+
 // Router logits L = x W_r + b (fp32 out).
 cudaError_t launch_router_logits(int dtype, const void* x, const void* W_r, const float* bias,
                                  float* L, int T, int d, int N, cudaStream_t s);
 
-// Router logits on tcgen05 (bf16, N % 8 == 0): split-K partials
-// partial[split][T][N] fp32, summed by launch_route_tokens.
+// The first kCtrlBytes of every workspace: the sticky status word, then
+// arrival counters of the kernels that finish with a last-block step (they
+// count modulo their number of blocks, so they must start at zero: the
+// workspace is zeroed, or moe_clear_device_status is called, before first use).
+constexpr size_t kCtrlBytes = 1024;
+constexpr int kCtrlSelectCounter = 1;    // int32 index in the control block
+constexpr int kCtrlRouterCounters = 16;  // int32 index of the router's per-tile counters
+constexpr int kRouteTile = 128;          // tokens per routing block / router tile
+constexpr int kMaxRouterTiles = (static_cast<int>(kCtrlBytes) / 4) - kCtrlRouterCounters;
+
+// Per-token routing (route_token.cuh) inputs and outputs. The logits of
+// 128-token tile m are the sum, in slot order, of nslots(m) fp32 slices
+// partial[(m * max_slots + s) * 128 * N ...] of [128, N] each (plus bias):
+// one slice holding the logits themselves, or the k-segments of the
+// tensor-core router (see router_segments below).
+struct RouteArgs {
+  const float* partial = nullptr;
+  int max_slots = 1;
+  int seg_ctas = 0, seg_total = 0, seg_kb = 0;  // router partition; seg_ctas == 0: one slot
+  const float* bias = nullptr;     // [N], added after the slices
+  float* logits_out = nullptr;     // [T, N] nullable
+  float* scores = nullptr;         // [T, N] nullable
+  int32_t* cand_idx = nullptr;     // [T, kc] (unused under expert choice)
+  float* cand_gate = nullptr;      // [T, kc]
+  const int32_t* home_group = nullptr;
+  unsigned long long* colsum = nullptr;  // [ceil(T/128), N] fixed-point column sums of p, nullable
+  int T = 0, N = 0, k = 0, m = 0, group_size = 1, renorm = 0, ec = 0;
+};
+
+// Partition of the tensor-core router's work: the m_tiles * num_kb k-blocks,
+// tile-major, split into `ctas` contiguous ranges of near-equal length; CTA i
+// takes [floor(i*W/G), floor((i+1)*W/G)). A range may cross one tile
+// boundary, so a tile's logits are the sum of the segments of consecutive
+// CTAs; the CTA holding k-block q is ceil((q+1)*G/W) - 1.
+__host__ __device__ inline int router_cta_of(long long q, int G, long long W) {
+  return static_cast<int>(((q + 1) * G + W - 1) / W) - 1;
+}
+__host__ __device__ inline int router_tile_segments(int m, int num_kb, int G, long long W) {
+  const long long q0 = static_cast<long long>(m) * num_kb;
+  return router_cta_of(q0 + num_kb - 1, G, W) - router_cta_of(q0, G, W) + 1;
+}
+
+// Router logits on tcgen05 (bf16, N % 8 == 0): per-segment partials in
+// ra.partial ([m_tiles][max_slots][128][N] fp32), and in the same launch the
+// last CTA to finish a tile routes its tokens.
 struct RouterSplit {
-  int splits = 1;
-  int kb_per_split = 1;
+  int ctas = 1;       // G
+  int num_kb = 1;     // k-blocks of 64 per tile
+  long long total = 1;  // W = m_tiles * num_kb
+  int max_slots = 1;  // most segments any tile has
 };
 bool router_tc_supported(int dtype, int d, int N);
 RouterSplit router_split_plan(int T, int d, int N);
-cudaError_t launch_router_logits_tc(const void* x, const void* W_r, int T, int d, int N,
-                                    const RouterSplit& plan, float* partial, int32_t* status,
-                                    cudaStream_t s);
+cudaError_t launch_router_tc(const void* x, const void* W_r, int d, const RouterSplit& plan,
+                             const RouteArgs& ra, uint32_t* tile_counters, int32_t* status,
+                             cudaStream_t s);
 
-// Per-token scores, candidates and gates. The logits of token t are
-// sum_{s < nsplit} partial[s][t][:] (+ bias), summed in ascending s; with
-// logits_out they are also stored there.
-cudaError_t launch_route_tokens(const float* partial, int nsplit, const float* bias,
-                                float* logits_out, float* scores, int32_t* cand_idx,
-                                float* cand_gate, const int32_t* home_group, int T, int N, int k,
-                                int m, int group_size, int renorm, int expert_choice,
-                                cudaStream_t s);
+// Per-token scores, candidates and gates from fp32 logits (ra.partial).
+cudaError_t launch_route_tokens(const RouteArgs& ra, cudaStream_t s);
+
+// Load statistics. colsum: [ceil(T/128), N] fixed-point column sums of the
+// scores (route_tokens / router_tc with ra.colsum, or launch_colsum).
+struct StatsArgs {
+  const unsigned long long* colsum = nullptr;
+  double* stats = nullptr;  // [MOE_STATS_LEN]
+};
+size_t colsum_bytes(int T, int N);
+cudaError_t launch_colsum(const float* scores, int T, int N, unsigned long long* colsum,
+                          cudaStream_t s);
+cudaError_t launch_stats_final(const int32_t* demand, const int32_t* kept,
+                               const unsigned long long* colsum, int T, int N, double* stats,
+                               cudaStream_t s);
 
 // Per-expert selection (token choice: rank only; capacity drop: top-cap by
-// gate; expert choice: top-cap tokens by score).
+// gate; expert choice: top-cap tokens by score). With st.stats set, the last
+// block to finish also writes the load statistics (counter: the control
+// block's select counter).
 cudaError_t launch_select(const int32_t* cand_idx, const float* cand_gate, int T, int kc, int N,
                           int expert_choice, int cap, int32_t* slot, uint8_t* keep,
-                          int32_t* demand, int32_t* kept, cudaStream_t s);
+                          int32_t* demand, int32_t* kept, const StatsArgs& st,
+                          uint32_t* counter, cudaStream_t s);
 int select_max_tokens();
 
 // Offsets, row maps, token rows and the gather of x into xp.
@@ -60,11 +136,6 @@ cudaError_t launch_grouped_gemm_tc_bf16(const void* A, const int32_t* offsets, i
 cudaError_t launch_combine(int dtype, const void* op, const float* row_gate,
                            const int32_t* tok_rows, const void* shared_out, void* y, int T,
                            int d, int kc, int64_t rows_max, cudaStream_t s);
-
-// Load statistics. partial: >= stats_partial_doubles(T, N) doubles of scratch.
-size_t stats_partial_doubles(int T, int N);
-cudaError_t launch_stats(const int32_t* demand, const int32_t* kept, const float* scores, int T,
-                         int N, double* partial, double* stats, cudaStream_t s);
 
 int device_sm_count();
 

@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/moe.h"
+#include "device_common.cuh"
 #include "internal.h"
 
 namespace moe {
@@ -27,10 +28,16 @@ int device_sm_count() {
 namespace {
 
 __global__ void write_pair_kernel(int32_t* p, int32_t a, int32_t b) {
+  pdl_launch_dependents();
+  pdl_wait();
   p[0] = a;
   p[1] = b;
 }
-__global__ void clear_status_kernel(int32_t* status) { *status = 0; }
+// Zeroes a workspace's control block (status word and arrival counters).
+__global__ void clear_ctrl_kernel(int32_t* ctrl) {
+  pdl_wait();
+  for (int i = threadIdx.x; i < static_cast<int>(kCtrlBytes / 4); i += blockDim.x) ctrl[i] = 0;
+}
 
 struct Derived {
   int kc = 0;
@@ -104,18 +111,25 @@ struct Tracer {
   int next = 0;
   bool mark(int stages = 1) {
     for (int j = 0; j < stages; ++j, ++next)
-      if (next < g_trace_n && cudaEventRecord(g_trace_events[next], s) != cudaSuccess)
+      if (next < g_trace_n && g_trace_events[next] &&
+          cudaEventRecord(g_trace_events[next], s) != cudaSuccess)
         return false;
     return true;
   }
 };
 
 // The kernels moe_layer_forward launches for c, in launch order.
-int layer_stage_names(const moe_config& c, bool with_stats, const char** names, int max_names) {
+int layer_stage_names(const moe_config& c, const char** names, int max_names) {
   const char* list[16];
   int n = 0;
-  if (!(c.flags & MOE_LOGITS_GIVEN)) list[n++] = "router_logits";
-  list[n++] = "route_tokens";
+  if (c.flags & MOE_LOGITS_GIVEN) {
+    list[n++] = "route_tokens";
+  } else if (router_tc_supported(c.dtype, c.d, c.N)) {
+    list[n++] = "router";
+  } else {
+    list[n++] = "router_logits";
+    list[n++] = "route_tokens";
+  }
   list[n++] = "select";
   list[n++] = "dispatch";
   list[n++] = "expert_gemm1_swiglu";
@@ -126,10 +140,6 @@ int layer_stage_names(const moe_config& c, bool with_stats, const char** names, 
     list[n++] = "shared_gemm2";
   }
   list[n++] = "combine";
-  if (with_stats) {
-    list[n++] = "stats_partial";
-    list[n++] = "stats_final";
-  }
   if (names)
     for (int i = 0; i < n && i < max_names; ++i) names[i] = list[i];
   return n;
@@ -139,52 +149,69 @@ int status_from(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_LAUN
 
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
-// Scratch of the tensor-core router: one fp32 [T, N] partial per k-split.
+// Scratch of the tensor-core router: per tile, one fp32 [128, N] partial per
+// k-segment.
 size_t router_partial_bytes(const moe_config& c) {
   if ((c.flags & MOE_LOGITS_GIVEN) || !router_tc_supported(c.dtype, c.d, c.N) || c.T == 0) return 0;
   const RouterSplit p = router_split_plan(c.T, c.d, c.N);
-  return static_cast<size_t>(p.splits) * c.T * c.N * 4;
+  const size_t m_tiles = (static_cast<size_t>(c.T) + kRouteTile - 1) / kRouteTile;
+  return m_tiles * p.max_slots * kRouteTile * c.N * sizeof(float);
 }
 
 // Logits (unless given) and per-token routing. logits: output buffer, or the
-// input when MOE_LOGITS_GIVEN. partial: router scratch (router_partial_bytes).
+// input when MOE_LOGITS_GIVEN. partial: router scratch (router_partial_bytes);
+// ctrl: the workspace's control block; colsum: column sums of the scores for
+// the load statistics (nullable).
 int run_router(const moe_config& c, bool ec, const void* x, const void* W_r, const float* bias,
                float* logits, float* scores, int32_t* cand_idx, float* cand_gate,
-               const int32_t* home_group, float* partial, int32_t* status, cudaStream_t s,
-               Tracer* tr = nullptr) {
+               const int32_t* home_group, float* partial, int32_t* ctrl,
+               unsigned long long* colsum, cudaStream_t s, Tracer* tr = nullptr) {
   const bool given = (c.flags & MOE_LOGITS_GIVEN) != 0;
-  if (c.T == 0) return (!tr || tr->mark(given ? 1 : 2)) ? MOE_OK : MOE_ERR_LAUNCH;
-  const float* src = logits;
-  int nsplit = 1;
-  const float* add_bias = nullptr;
-  float* logits_out = nullptr;
-  if (!given) {
-    if (router_tc_supported(c.dtype, c.d, c.N)) {
-      const RouterSplit p = router_split_plan(c.T, c.d, c.N);
-      if (launch_router_logits_tc(x, W_r, c.T, c.d, c.N, p, partial, status, s) != cudaSuccess ||
-          (tr && !tr->mark()))
-        return MOE_ERR_LAUNCH;
-      src = partial;
-      nsplit = p.splits;
-      add_bias = bias;
-      logits_out = logits;
-    } else if (launch_router_logits(c.dtype, x, W_r, bias, logits, c.T, c.d, c.N, s) !=
-                   cudaSuccess ||
-               (tr && !tr->mark())) {
+  const bool tc = !given && router_tc_supported(c.dtype, c.d, c.N);
+  const int stages = (given || tc) ? 1 : 2;
+  if (c.T == 0) return (!tr || tr->mark(stages)) ? MOE_OK : MOE_ERR_LAUNCH;
+  RouteArgs ra;
+  ra.partial = logits;
+  ra.scores = scores;
+  ra.cand_idx = cand_idx;
+  ra.cand_gate = cand_gate;
+  ra.home_group = home_group;
+  ra.colsum = colsum;
+  ra.T = c.T;
+  ra.N = c.N;
+  ra.k = c.k;
+  ra.m = c.m;
+  ra.group_size = c.group_size > 0 ? c.group_size : 1;
+  ra.renorm = c.renorm;
+  ra.ec = ec ? 1 : 0;
+  if (tc) {
+    const RouterSplit p = router_split_plan(c.T, c.d, c.N);
+    ra.partial = partial;
+    ra.max_slots = p.max_slots;
+    ra.seg_ctas = p.ctas;
+    ra.seg_kb = p.num_kb;
+    ra.seg_total = p.total;
+    ra.bias = bias;
+    ra.logits_out = logits;
+    if (launch_router_tc(x, W_r, c.d, p, ra,
+                         reinterpret_cast<uint32_t*>(ctrl + kCtrlRouterCounters), ctrl,
+                         s) != cudaSuccess ||
+        (tr && !tr->mark()))
       return MOE_ERR_LAUNCH;
-    }
+    return MOE_OK;
   }
-  if (launch_route_tokens(src, nsplit, add_bias, logits_out, scores, cand_idx, cand_gate,
-                          home_group, c.T, c.N, c.k, c.m, c.group_size, c.renorm, ec ? 1 : 0,
-                          s) != cudaSuccess ||
-      (tr && !tr->mark()))
-    return MOE_ERR_LAUNCH;
+  if (!given) {
+    if (launch_router_logits(c.dtype, x, W_r, bias, logits, c.T, c.d, c.N, s) != cudaSuccess ||
+        (tr && !tr->mark()))
+      return MOE_ERR_LAUNCH;
+  }
+  if (launch_route_tokens(ra, s) != cudaSuccess || (tr && !tr->mark())) return MOE_ERR_LAUNCH;
   return MOE_OK;
 }
 
 struct Layout {
-  size_t status, router_partial, logits, scores, cand_idx, cand_gate, slot, keep, demand, kept, offsets,
-      shared_offsets, row_token, row_gate, tok_rows, xp, hp, op, shared_out, stats_partial, total;
+  size_t ctrl, router_partial, logits, scores, cand_idx, cand_gate, slot, keep, demand, kept, offsets,
+      shared_offsets, row_token, row_gate, tok_rows, xp, hp, op, shared_out, colsum, total;
 };
 
 Layout layout(const moe_config& c, const Derived& d) {
@@ -196,7 +223,7 @@ Layout layout(const moe_config& c, const Derived& d) {
     return o;
   };
   const size_t T = c.T, N = c.N, kc = d.kc, R = d.rows_max, dd = c.d;
-  L.status = take(256);
+  L.ctrl = take(kCtrlBytes);
   L.router_partial = take(router_partial_bytes(c));
   L.logits = take(T * N * 4);
   L.scores = take(T * N * 4);
@@ -216,7 +243,7 @@ Layout layout(const moe_config& c, const Derived& d) {
   L.hp = take(hp_rows * d.sx);
   L.op = take(R * dd * d.sx);
   L.shared_out = take(c.f_shared > 0 ? T * dd * d.sx : 0);
-  L.stats_partial = take(stats_partial_doubles(c.T, c.N) * 8);
+  L.colsum = take(colsum_bytes(c.T, c.N));
   L.total = off;
   return L;
 }
@@ -278,13 +305,13 @@ size_t moe_workspace_size(const moe_config* cfg) {
 size_t moe_ffn_workspace_size(int64_t rows_max, int32_t f, int32_t dtype) {
   if (rows_max < 0 || f < 0) return 0;
   const size_t sx = dtype == MOE_BF16 ? 2 : 4;
-  return 256 + align256(static_cast<size_t>(rows_max) * static_cast<size_t>(f) * sx);
+  return kCtrlBytes + align256(static_cast<size_t>(rows_max) * static_cast<size_t>(f) * sx);
 }
 
 size_t moe_route_workspace_size(const moe_config* cfg) {
   Derived d;
   if (validate(cfg, &d) != MOE_OK) return 0;
-  return 256 + align256(router_partial_bytes(*cfg));
+  return kCtrlBytes + align256(router_partial_bytes(*cfg));
 }
 
 int moe_route(const moe_config* cfg, const void* x, const void* W_router, const float* bias,
@@ -302,8 +329,9 @@ int moe_route(const moe_config* cfg, const void* x, const void* W_router, const 
   if (reinterpret_cast<uintptr_t>(ws) & 255u) return MOE_ERR_ALIGN;
   if (ws_bytes < moe_route_workspace_size(cfg)) return MOE_ERR_WORKSPACE;
   return run_router(*cfg, d.ec, x, W_router, bias, logits, scores, cand_idx, cand_gate,
-                    home_group, reinterpret_cast<float*>(static_cast<unsigned char*>(ws) + 256),
-                    static_cast<int32_t*>(ws), as_stream(stream));
+                    home_group,
+                    reinterpret_cast<float*>(static_cast<unsigned char*>(ws) + kCtrlBytes),
+                    static_cast<int32_t*>(ws), nullptr, as_stream(stream));
 }
 
 int moe_capacity_drop(const moe_config* cfg, const int32_t* cand_idx, const float* cand_gate,
@@ -315,7 +343,8 @@ int moe_capacity_drop(const moe_config* cfg, const int32_t* cand_idx, const floa
   if (!have(cand_gate, T) || !have(slot, T) || !demand || !kept || (!d.ec && !have(cand_idx, T)))
     return MOE_ERR_NULL;
   return status_from(launch_select(cand_idx, cand_gate, cfg->T, d.kc, cfg->N, d.ec ? 1 : 0, d.cap,
-                                   slot, keep, demand, kept, as_stream(stream)));
+                                   slot, keep, demand, kept, StatsArgs{}, nullptr,
+                                   as_stream(stream)));
 }
 
 int moe_dispatch(const moe_config* cfg, const void* x, const int32_t* cand_idx,
@@ -351,7 +380,7 @@ int moe_expert_ffn(const moe_config* cfg, const void* xp, const int32_t* offsets
     return MOE_ERR_ALIGN;
   if (ws_bytes < moe_ffn_workspace_size(rows_max, f, cfg->dtype)) return MOE_ERR_WORKSPACE;
   int32_t* status = static_cast<int32_t*>(ws);
-  void* hp = static_cast<unsigned char*>(ws) + 256;
+  void* hp = static_cast<unsigned char*>(ws) + kCtrlBytes;
   return run_ffn(cfg->dtype, xp, offsets, n_segments, rows_max, cfg->d, f, W1, W3, W2, hp, op,
                  status, as_stream(stream));
 }
@@ -397,9 +426,12 @@ int moe_load_stats(const moe_config* cfg, const int32_t* demand, const int32_t* 
   int st = validate(cfg, &d);
   if (st != MOE_OK) return st;
   if (!demand || !kept || !have(scores, cfg->T) || !stats || !ws) return MOE_ERR_NULL;
-  if (ws_bytes < stats_partial_doubles(cfg->T, cfg->N) * 8) return MOE_ERR_WORKSPACE;
-  return status_from(launch_stats(demand, kept, scores, cfg->T, cfg->N, static_cast<double*>(ws),
-                                  stats, as_stream(stream)));
+  if (ws_bytes < colsum_bytes(cfg->T, cfg->N)) return MOE_ERR_WORKSPACE;
+  if (!aligned16(ws)) return MOE_ERR_ALIGN;
+  cudaStream_t s = as_stream(stream);
+  auto* colsum = static_cast<unsigned long long*>(ws);
+  if (launch_colsum(scores, cfg->T, cfg->N, colsum, s) != cudaSuccess) return MOE_ERR_LAUNCH;
+  return status_from(launch_stats_final(demand, kept, colsum, cfg->T, cfg->N, stats, s));
 }
 
 int moe_layer_forward(const moe_config* cfg, const void* x, const void* W_router,
@@ -425,7 +457,8 @@ int moe_layer_forward(const moe_config* cfg, const void* x, const void* W_router
   cudaStream_t s = as_stream(stream);
   Tracer tr{s};
   if (!tr.mark()) return MOE_ERR_LAUNCH;
-  int32_t* status = at<int32_t>(ws, L.status);
+  int32_t* ctrl = at<int32_t>(ws, L.ctrl);
+  int32_t* status = ctrl;
   float* Lg = given ? logits : (logits ? logits : at<float>(ws, L.logits));
   float* scores = at<float>(ws, L.scores);
   int32_t* cand_idx = at<int32_t>(ws, L.cand_idx);
@@ -443,11 +476,17 @@ int moe_layer_forward(const moe_config* cfg, const void* x, const void* W_router
   void* op = at<void>(ws, L.op);
   void* ys = c.f_shared > 0 ? at<void>(ws, L.shared_out) : nullptr;
 
+  unsigned long long* colsum = stats ? at<unsigned long long>(ws, L.colsum) : nullptr;
   st = run_router(c, d.ec, x, W_router, bias, Lg, scores, cand_idx, cand_gate, home_group,
-                  at<float>(ws, L.router_partial), status, s, &tr);
+                  at<float>(ws, L.router_partial), ctrl, colsum, s, &tr);
   if (st != MOE_OK) return st;
+  StatsArgs sa;
+  sa.colsum = colsum;
+  sa.stats = stats;
   if (launch_select(cand_idx, cand_gate, c.T, d.kc, c.N, d.ec ? 1 : 0, d.cap, slot, keep, demand,
-                    kept, s) != cudaSuccess || !tr.mark(1))
+                    kept, sa, reinterpret_cast<uint32_t*>(ctrl + kCtrlSelectCounter),
+                    s) != cudaSuccess ||
+      !tr.mark(1))
     return MOE_ERR_LAUNCH;
   if (launch_dispatch(c.dtype, x, cand_idx, cand_gate, slot, kept, c.T, c.d, c.N, d.kc,
                       d.ec ? 1 : 0, d.rows_max, offsets, row_token, row_gate, tok_rows, xp,
@@ -459,8 +498,8 @@ int moe_layer_forward(const moe_config* cfg, const void* x, const void* W_router
   if (c.f_shared > 0) {
     if (c.T > 0) {
       int32_t* soff = at<int32_t>(ws, L.shared_offsets);
-      write_pair_kernel<<<1, 1, 0, s>>>(soff, 0, c.T);
-      if (cudaGetLastError() != cudaSuccess || !tr.mark(1)) return MOE_ERR_LAUNCH;
+      if (launch_pdl(write_pair_kernel, 1, 1, 0, s, soff, 0, c.T) != cudaSuccess || !tr.mark(1))
+        return MOE_ERR_LAUNCH;
       st = run_ffn(c.dtype, x, soff, 1, c.T, c.d, c.f_shared, Ws1, Ws3, Ws2, hp, ys, status, s,
                    &tr);
       if (st != MOE_OK) return st;
@@ -472,29 +511,19 @@ int moe_layer_forward(const moe_config* cfg, const void* x, const void* W_router
           cudaSuccess ||
       !tr.mark(1))
     return MOE_ERR_LAUNCH;
-  if (stats) {
-    if (launch_stats(demand, kept, scores, c.T, c.N, at<double>(ws, L.stats_partial), stats, s) !=
-            cudaSuccess ||
-        !tr.mark(2))
-      return MOE_ERR_LAUNCH;
-  }
   return MOE_OK;
 }
 
-int moe_layer_stages(const moe_config* cfg, int with_stats, const char** names,
-                     int max_names) {
+int moe_layer_stages(const moe_config* cfg, const char** names, int max_names) {
   const int st = validate(cfg, nullptr);
   if (st != MOE_OK) return st;
   if (max_names < 0) return MOE_ERR_SHAPE;
-  return layer_stage_names(*cfg, with_stats != 0, names, max_names);
+  return layer_stage_names(*cfg, names, max_names);
 }
 
 int moe_set_trace_events(void* const* events, int n_events) {
   if (n_events < 0 || n_events > kMaxTraceEvents) return MOE_ERR_SHAPE;
   if (n_events > 0 && !events) return MOE_ERR_NULL;
-  for (int i = 0; i < n_events; ++i) {
-    if (!events[i]) return MOE_ERR_NULL;
-  }
   for (int i = 0; i < n_events; ++i) g_trace_events[i] = static_cast<cudaEvent_t>(events[i]);
   g_trace_n = n_events;
   return MOE_OK;
@@ -506,7 +535,7 @@ int moe_workspace_views(const moe_config* cfg, void* ws, moe_views_t* out) {
   if (st != MOE_OK) return st;
   if (!ws || !out) return MOE_ERR_NULL;
   const Layout L = layout(*cfg, d);
-  out->status = at<int32_t>(ws, L.status);
+  out->status = at<int32_t>(ws, L.ctrl);
   out->logits = at<float>(ws, L.logits);
   out->scores = at<float>(ws, L.scores);
   out->cand_idx = at<int32_t>(ws, L.cand_idx);
@@ -537,7 +566,7 @@ int moe_get_device_status(const void* ws, void* stream, int32_t* out_host) {
 
 int moe_clear_device_status(void* ws, void* stream) {
   if (!ws) return MOE_ERR_NULL;
-  clear_status_kernel<<<1, 1, 0, as_stream(stream)>>>(static_cast<int32_t*>(ws));
+  clear_ctrl_kernel<<<1, 256, 0, as_stream(stream)>>>(static_cast<int32_t*>(ws));
   return status_from(cudaGetLastError());
 }
 

@@ -1,4 +1,6 @@
-// Router: logits, softmax scores, top-k / expanded candidates and gates.
+// Router on the fp32 FMA pipes (fp32 layers, or bf16 shapes the tensor-core
+// router does not take): logits, then softmax scores, top-k / expanded
+// candidates and gates.
 //
 // "Understanding Mixture of Experts", section "Expert and Router": the router
 // scores each token against every expert and activates TopK(G(x), k).
@@ -10,6 +12,7 @@
 
 #include "device_common.cuh"
 #include "internal.h"
+#include "route_token.cuh"
 
 namespace moe {
 namespace {
@@ -53,6 +56,8 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const E* __restrict_
   constexpr int PER = NE / 4;
   __shared__ float xs[kLogitKC][kLogitTM + 1];
   __shared__ float ws[kLogitKC][NE];
+  pdl_launch_dependents();
+  pdl_wait();
   const int tid = threadIdx.x;
   const int t0 = blockIdx.x * kLogitTM;
   const int e0 = blockIdx.y * NE;
@@ -105,142 +110,22 @@ cudaError_t logits_dispatch_ne(const E* x, const E* W_r, const float* bias, floa
                                int N, cudaStream_t s) {
   const dim3 block(256);
   const int gx = (T + kLogitTM - 1) / kLogitTM;
-  if (N <= 8) {
-    router_logits_kernel<E, 8><<<dim3(gx, 1), block, 0, s>>>(x, W_r, bias, L, T, d, N);
-  } else if (N <= 16) {
-    router_logits_kernel<E, 16><<<dim3(gx, 1), block, 0, s>>>(x, W_r, bias, L, T, d, N);
-  } else if (N <= 32) {
-    router_logits_kernel<E, 32><<<dim3(gx, 1), block, 0, s>>>(x, W_r, bias, L, T, d, N);
-  } else {
-    router_logits_kernel<E, 64><<<dim3(gx, (N + 63) / 64), block, 0, s>>>(x, W_r, bias, L, T, d, N);
-  }
-  return cudaGetLastError();
+  if (N <= 8) return launch_pdl(router_logits_kernel<E, 8>, dim3(gx, 1), block, 0, s, x, W_r, bias, L, T, d, N);
+  if (N <= 16) return launch_pdl(router_logits_kernel<E, 16>, dim3(gx, 1), block, 0, s, x, W_r, bias, L, T, d, N);
+  if (N <= 32) return launch_pdl(router_logits_kernel<E, 32>, dim3(gx, 1), block, 0, s, x, W_r, bias, L, T, d, N);
+  return launch_pdl(router_logits_kernel<E, 64>, dim3(gx, (N + 63) / 64), block, 0, s, x, W_r, bias,
+                    L, T, d, N);
 }
 
 // ---------------------------------------------------------------------------
-// Per-token routing from fp32 logits, one thread per token, all N logits of
-// the token in registers (NMAX >= N).
-//   scores: m = max L; u_e = score_exp(L_e - m); Z = u_0 + u_1 + ... (in
-//   order); p_e = u_e / Z (correctly rounded).
-//   top-k: k passes of an argmax over order keys, strict '>' in ascending e,
-//   so ties go to the lower expert; a chosen expert's key is cleared to 0
-//   (every finite value has a key >= 0x00800000).
-//   expanded: m more passes restricted to the home group's experts.
-//   gates: p of the slot; with renorm divided by the slots' left-to-right sum.
+// Per-token routing from fp32 logits (route_token.cuh), 128 tokens per block,
+// one thread per token; the block also writes its tile's column sums of p.
 // ---------------------------------------------------------------------------
-template <int NMAX>
-__global__ void __launch_bounds__(64) route_tokens_kernel(
-    const float* __restrict__ partial, int nsplit, const float* __restrict__ bias,
-    float* __restrict__ logits_out, float* __restrict__ scores, int32_t* __restrict__ cand_idx,
-    float* __restrict__ cand_gate, const int32_t* __restrict__ home_group, int T, int N, int k,
-    int m, int group_size, int renorm, int expert_choice) {
-  const int t = blockIdx.x * blockDim.x + threadIdx.x;
-  if (t >= T) return;
-  float l[NMAX];
-  {
-    const float* row = partial + static_cast<size_t>(t) * N;
-#pragma unroll
-    for (int e = 0; e < NMAX; ++e) l[e] = (e < N) ? row[e] : 0.f;
-    for (int sp = 1; sp < nsplit; ++sp) {  // splits added in ascending order
-      row += static_cast<size_t>(T) * N;
-#pragma unroll
-      for (int e = 0; e < NMAX; ++e)
-        if (e < N) l[e] += row[e];
-    }
-    if (bias) {
-#pragma unroll
-      for (int e = 0; e < NMAX; ++e)
-        if (e < N) l[e] += bias[e];
-    }
-    if (logits_out) {
-#pragma unroll
-      for (int e = 0; e < NMAX; ++e)
-        if (e < N) logits_out[static_cast<size_t>(t) * N + e] = l[e];
-    }
-  }
-  float mx = l[0];
-#pragma unroll
-  for (int e = 1; e < NMAX; ++e)
-    if (e < N) mx = fmaxf(mx, l[e]);
-  float p[NMAX];
-  float Z = 0.f;
-#pragma unroll
-  for (int e = 0; e < NMAX; ++e) {
-    p[e] = (e < N) ? score_exp(__fsub_rn(l[e], mx)) : 0.f;
-    if (e == 0) Z = p[0];
-    else if (e < N) Z = __fadd_rn(Z, p[e]);
-  }
-#pragma unroll
-  for (int e = 0; e < NMAX; ++e) p[e] = __fdiv_rn(p[e], Z);
-
-  if (expert_choice) {
-    float* out = cand_gate + static_cast<size_t>(t) * N;
-#pragma unroll
-    for (int e = 0; e < NMAX; ++e)
-      if (e < N) {
-        out[e] = p[e];
-        if (scores) scores[static_cast<size_t>(t) * N + e] = p[e];
-      }
-    return;
-  }
-  if (scores) {
-#pragma unroll
-    for (int e = 0; e < NMAX; ++e)
-      if (e < N) scores[static_cast<size_t>(t) * N + e] = p[e];
-  }
-
-  uint32_t key[NMAX];
-#pragma unroll
-  for (int e = 0; e < NMAX; ++e) key[e] = (e < N) ? order_key(l[e]) : 0u;
-
-  const int kc = k + m;
-  int32_t* idx_out = cand_idx + static_cast<size_t>(t) * kc;
-  float* gate_out = cand_gate + static_cast<size_t>(t) * kc;
-  float g[32];
-  for (int j = 0; j < kc; ++j) {
-    int lo = 0, hi = N;  // pass range: all experts for top-k, the home group after
-    if (j >= k) {
-      const int G = N / group_size;
-      const int hg = home_group ? home_group[t]
-                                : static_cast<int>((static_cast<long long>(t) * G) / T);
-      lo = hg * group_size;
-      hi = lo + group_size;
-    }
-    int best = -1;
-    uint32_t bk = 0u;
-    float bp = 0.f;
-#pragma unroll
-    for (int e = 0; e < NMAX; ++e) {
-      if (e >= lo && e < hi && key[e] > bk) {
-        bk = key[e];
-        best = e;
-        bp = p[e];
-      }
-    }
-#pragma unroll
-    for (int e = 0; e < NMAX; ++e)
-      if (e == best) key[e] = 0u;
-    idx_out[j] = best;
-    g[j] = (best >= 0) ? bp : 0.f;
-  }
-  if (renorm) {
-    float S = g[0];
-    for (int j = 1; j < kc; ++j) S = __fadd_rn(S, g[j]);
-    for (int j = 0; j < kc; ++j) g[j] = __fdiv_rn(g[j], S);
-  }
-  for (int j = 0; j < kc; ++j) gate_out[j] = g[j];
-}
-
-template <int NMAX>
-cudaError_t route_tokens_launch(const float* partial, int nsplit, const float* bias,
-                                float* logits_out, float* scores, int32_t* cand_idx,
-                                float* cand_gate, const int32_t* home_group, int T, int N, int k,
-                                int m, int group_size, int renorm, int ec, cudaStream_t s) {
-  const int threads = 64;
-  route_tokens_kernel<NMAX><<<(T + threads - 1) / threads, threads, 0, s>>>(
-      partial, nsplit, bias, logits_out, scores, cand_idx, cand_gate, home_group, T, N, k, m,
-      group_size, renorm, ec);
-  return cudaGetLastError();
+__global__ void __launch_bounds__(kRouteTile) route_tokens_kernel(const RouteArgs a) {
+  extern __shared__ float s_p[];
+  pdl_launch_dependents();
+  pdl_wait();
+  route_tile(a, blockIdx.x, s_p);
 }
 
 }  // namespace
@@ -255,23 +140,22 @@ cudaError_t launch_router_logits(int dtype, const void* x, const void* W_r, cons
                             T, d, N, s);
 }
 
-cudaError_t launch_route_tokens(const float* partial, int nsplit, const float* bias,
-                                float* logits_out, float* scores, int32_t* cand_idx,
-                                float* cand_gate, const int32_t* home_group, int T, int N, int k,
-                                int m, int group_size, int renorm, int ec, cudaStream_t s) {
-  if (T == 0) return cudaSuccess;
-#define MOE_ROUTE_CASE(NM)                                                                     \
-  if (N <= NM)                                                                                 \
-    return route_tokens_launch<NM>(partial, nsplit, bias, logits_out, scores, cand_idx,       \
-                                   cand_gate, home_group, T, N, k, m, group_size, renorm, ec, s);
-  MOE_ROUTE_CASE(8)
-  MOE_ROUTE_CASE(16)
-  MOE_ROUTE_CASE(32)
-  MOE_ROUTE_CASE(64)
-  MOE_ROUTE_CASE(128)
-  MOE_ROUTE_CASE(256)
-#undef MOE_ROUTE_CASE
-  return cudaErrorInvalidValue;
+cudaError_t launch_route_tokens(const RouteArgs& a, cudaStream_t s) {
+  if (a.T == 0) return cudaSuccess;
+  if (a.N > 256) return cudaErrorInvalidValue;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    err = cudaFuncSetAttribute(route_tokens_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(route_tile_smem(256)));
+    if (err != cudaSuccess) return err;
+    attr_set[dev] = true;
+  }
+  return launch_pdl(route_tokens_kernel, (a.T + kRouteTile - 1) / kRouteTile, kRouteTile,
+                    route_tile_smem(a.N), s, a);
 }
 
 }  // namespace moe

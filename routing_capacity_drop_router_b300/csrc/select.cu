@@ -13,39 +13,42 @@
 //     over the 32-bit gate keys finds the capacity-th largest key K* and how
 //     many candidates equal to K* survive (the first ones in token order);
 //  3. an ordered pass writes each candidate's rank among the kept (ascending
-//     token) or -1.
+//     token) or -1;
+//  4. optionally, the last CTA to finish writes the layer's load statistics.
 // Keys are distinct up to ties of equal gates, and ties are settled by list
 // (token) order, so the kept set is unique and independent of thread timing.
 #include <cuda_runtime.h>
 
 #include "device_common.cuh"
 #include "internal.h"
+#include "stats_final.cuh"
 
 namespace moe {
 namespace {
 
 constexpr int kSelThreads = 1024;
-constexpr int kSelMaxTokens = 24576;  // 8 bytes of shared memory per list entry
+constexpr int kSelRounds = 8;             // 32-entry rounds per warp per pass
+constexpr int kSelPass = kSelThreads * kSelRounds;  // list entries per block pass
+constexpr int kSelMaxTokens = 24576;      // 8 bytes of shared memory per list entry
 
-// Exclusive prefix count of `pred` over the CTA in thread order; `total`
-// receives the CTA-wide count. Contains __syncthreads: call uniformly.
-__device__ __forceinline__ int cta_exclusive_count(bool pred, int* warp_sums, int& total) {
+// Exclusive prefix over warps of each warp's total (lane-uniform input);
+// `total` receives the block's sum. Contains __syncthreads: call uniformly.
+__device__ __forceinline__ int warp_exclusive_offset(int warp_total, int* warp_sums, int& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nwarps = blockDim.x >> 5;
-  const unsigned b = __ballot_sync(0xffffffffu, pred);
-  if (lane == 0) warp_sums[warp] = __popc(b);
+  if (lane == 0) warp_sums[warp] = warp_total;
   __syncthreads();
   if (warp == 0) {
-    int v = (lane < nwarps) ? warp_sums[lane] : 0;
+    int w = (lane < nwarps) ? warp_sums[lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(0xffffffffu, v, o);
-      if (lane >= o) v += n;
+      const int n = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += n;
     }
-    warp_sums[lane] = v;  // inclusive
+    warp_sums[lane] = w;  // inclusive over warps
   }
   __syncthreads();
-  const int excl = (warp ? warp_sums[warp - 1] : 0) + __popc(b & ((1u << lane) - 1u));
+  const int excl = warp ? warp_sums[warp - 1] : 0;
   total = warp_sums[nwarps - 1];
   __syncthreads();
   return excl;
@@ -54,53 +57,69 @@ __device__ __forceinline__ int cta_exclusive_count(bool pred, int* warp_sums, in
 __global__ void __launch_bounds__(kSelThreads) select_kernel(
     const int32_t* __restrict__ cand_idx, const float* __restrict__ cand_gate, int T, int kc,
     int N, int expert_choice, int cap, int32_t* __restrict__ slot, uint8_t* __restrict__ keep,
-    int32_t* __restrict__ demand, int32_t* __restrict__ kept) {
+    int32_t* __restrict__ demand, int32_t* __restrict__ kept, const StatsArgs st,
+    uint32_t* __restrict__ counter) {
   extern __shared__ __align__(16) unsigned char sel_smem[];
   int32_t* lflat = reinterpret_cast<int32_t*>(sel_smem);
   uint32_t* lkey = reinterpret_cast<uint32_t*>(lflat + T);
   __shared__ int warp_sums[32];
   __shared__ unsigned hist[256];
-  __shared__ int s_bin, s_need;
+  __shared__ int s_bin, s_need, s_last;
 
   const int e = blockIdx.x;
-  const int total = expert_choice ? T : T * kc;
+  const int lane = threadIdx.x & 31;
+  pdl_launch_dependents();
+  pdl_wait();
 
-  // 1. ordered compaction of expert e's candidates
+  // 1. ordered compaction of expert e's candidates into the shared list
   int n = 0;
-  for (int start = 0; start < total; start += blockDim.x) {
-    const int i = start + threadIdx.x;
-    bool pred = false;
-    int flat = 0;
-    float g = 0.f;
-    if (i < total) {
-      if (expert_choice) {
-        flat = i * N + e;
-        pred = true;
-        g = cand_gate[flat];
-      } else {
-        const int ce = cand_idx[i];
-        flat = i;
-        pred = (ce == e);
-        if (pred) {
-          g = cand_gate[i];
-        } else if (e == 0 && (ce < 0 || ce >= N)) {  // empty slot: claimed by CTA 0
+  if (expert_choice) {
+    n = T;
+    for (int i = threadIdx.x; i < T; i += blockDim.x) {
+      const int flat = i * N + e;
+      lflat[i] = flat;
+      lkey[i] = order_key(cand_gate[flat]);
+    }
+  } else {
+    // pass: warp w takes entries [base + 256 w, base + 256 w + 256) in 32-entry
+    // rounds (coalesced loads, conflict-free shared stores); ballots order the
+    // matches inside a round, one block scan orders the warps
+    const int total = T * kc;
+    const unsigned lt = (1u << lane) - 1u;
+    for (int base = 0; base < total; base += kSelPass) {
+      const int w0 = base + (static_cast<int>(threadIdx.x) >> 5) * (32 * kSelRounds) + lane;
+      int ce[kSelRounds];
+      int cnt = 0;
+#pragma unroll
+      for (int j = 0; j < kSelRounds; ++j) {
+        const int i = w0 + 32 * j;
+        ce[j] = (i < total) ? cand_idx[i] : N;  // N: no expert, and not an empty slot
+        cnt += __popc(__ballot_sync(0xffffffffu, ce[j] == e));
+        if (e == 0 && i < total && (ce[j] < 0 || ce[j] >= N)) {  // empty slots: block 0
           slot[i] = -1;
           if (keep) keep[i] = 0;
         }
       }
-    }
-    int tot;
-    const int pos = n + cta_exclusive_count(pred, warp_sums, tot);
-    if (pred) {
-      if (pos < T) {
-        lflat[pos] = flat;
-        lkey[pos] = order_key(g);
-      } else {  // only if a token lists the same expert twice: not selectable
-        slot[flat] = -1;
-        if (keep) keep[flat] = 0;
+      int tot;
+      int pos = n + warp_exclusive_offset(cnt, warp_sums, tot);
+#pragma unroll
+      for (int j = 0; j < kSelRounds; ++j) {
+        const int i = w0 + 32 * j;
+        const unsigned b = __ballot_sync(0xffffffffu, ce[j] == e);
+        if (ce[j] == e) {
+          const int p = pos + __popc(b & lt);
+          if (p < T) {
+            lflat[p] = i;
+            lkey[p] = order_key(cand_gate[i]);
+          } else {  // only if a token lists the same expert twice: not selectable
+            slot[i] = -1;
+            if (keep) keep[i] = 0;
+          }
+        }
+        pos += __popc(b);
       }
+      n += tot;
     }
-    n += tot;
   }
   __syncthreads();
   const int n_all = n;  // candidates counted, reported as demand
@@ -112,21 +131,28 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
       if (keep) keep[lflat[i]] = 1;
     }
   } else {
-    // 2. radix select of the cap-th largest key (cap >= 1 here; cap <= 0 keeps none)
+    // 2. radix select of the cap-th largest key (cap >= 1 here; cap <= 0 keeps
+    //    none); histogram counts are aggregated per warp over equal bins, since
+    //    gates of one expert share their high bits
     uint32_t prefix = 0u, pmask = 0u;
     int need = cap;
     if (cap > 0) {
       for (int shift = 24; shift >= 0; shift -= 8) {
         for (int b = threadIdx.x; b < 256; b += blockDim.x) hist[b] = 0u;
         __syncthreads();
-        for (int i = threadIdx.x; i < n; i += blockDim.x) {
-          const uint32_t kk = lkey[i];
-          if ((kk & pmask) == prefix) atomicAdd(&hist[(kk >> shift) & 255u], 1u);
+        for (int i0 = 0; i0 < n; i0 += blockDim.x) {  // uniform trip count per warp
+          const int i = i0 + static_cast<int>(threadIdx.x);
+          int bin = -1;
+          if (i < n) {
+            const uint32_t kk = lkey[i];
+            if ((kk & pmask) == prefix) bin = static_cast<int>((kk >> shift) & 255u);
+          }
+          const unsigned peers = __match_any_sync(0xffffffffu, bin);
+          if (bin >= 0 && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
         }
         __syncthreads();
         if (threadIdx.x < 32) {
           // lane owns bins [8*lane, 8*lane + 8); walk down from bin 255
-          const int lane = threadIdx.x;
           unsigned c[8], sum = 0u;
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
@@ -166,23 +192,50 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
     const uint32_t thr = prefix;
     const int need_eq = (cap > 0) ? need : 0;  // candidates equal to thr that stay
 
-    // 3. ordered keep pass: rank among kept, ascending token
-    int eq_base = 0, k_base = 0;
-    for (int start = 0; start < n; start += blockDim.x) {
-      const int i = start + threadIdx.x;
-      const uint32_t kk = (i < n) ? lkey[i] : 0u;
-      const bool is_eq = (i < n) && cap > 0 && kk == thr;
-      int eq_tot;
-      const int eq_rank = eq_base + cta_exclusive_count(is_eq, warp_sums, eq_tot);
-      const bool kp = (i < n) && cap > 0 && (kk > thr || (is_eq && eq_rank < need_eq));
-      int k_tot;
-      const int r = k_base + cta_exclusive_count(kp, warp_sums, k_tot);
-      if (i < n) {
-        slot[lflat[i]] = kp ? r : -1;
-        if (keep) keep[lflat[i]] = kp ? 1 : 0;
+    // 3. ordered keep pass: a candidate is kept if its key is above thr, or
+    //    equal to it and among the first need_eq such in token order; its slot
+    //    is the number of kept candidates before it. One scan carries both
+    //    counts (above in the high half, equal in the low half; each < 2^16).
+    const unsigned lt = (1u << lane) - 1u;
+    int k_base = 0, eq_base = 0;  // kept and equal-to-thr entries before this pass
+    for (int base = 0; base < n; base += kSelPass) {
+      const int w0 = base + (static_cast<int>(threadIdx.x) >> 5) * (32 * kSelRounds) + lane;
+      uint32_t kk[kSelRounds];
+      int gt_w = 0, eq_w = 0;
+#pragma unroll
+      for (int j = 0; j < kSelRounds; ++j) {
+        const int i = w0 + 32 * j;
+        kk[j] = (i < n) ? lkey[i] : 0u;
+        const bool valid = i < n && cap > 0;
+        gt_w += __popc(__ballot_sync(0xffffffffu, valid && kk[j] > thr));
+        eq_w += __popc(__ballot_sync(0xffffffffu, valid && kk[j] == thr));
       }
-      eq_base += eq_tot;
-      k_base += k_tot;
+      // one scan carries both warp counts (above in the high half, equal in
+      // the low half; each < 2^16)
+      int tot;
+      const int ex = warp_exclusive_offset((gt_w << 16) | eq_w, warp_sums, tot);
+      int gt_before = (ex >> 16), eq_before = eq_base + (ex & 0xffff);
+      // kept before an entry = above-thr before it + min(equal before it, need_eq)
+#pragma unroll
+      for (int j = 0; j < kSelRounds; ++j) {
+        const int i = w0 + 32 * j;
+        const bool valid = i < n && cap > 0;
+        const bool is_gt = valid && kk[j] > thr;
+        const bool is_eq = valid && kk[j] == thr;
+        const unsigned bg = __ballot_sync(0xffffffffu, is_gt);
+        const unsigned be = __ballot_sync(0xffffffffu, is_eq);
+        const int g_i = gt_before + __popc(bg & lt);
+        const int q_i = eq_before + __popc(be & lt);
+        if (i < n) {
+          const bool kp = is_gt || (is_eq && q_i < need_eq);
+          slot[lflat[i]] = kp ? k_base + g_i + min(q_i, need_eq) - min(eq_base, need_eq) : -1;
+          if (keep) keep[lflat[i]] = kp ? 1 : 0;
+        }
+        gt_before += __popc(bg);
+        eq_before += __popc(be);
+      }
+      k_base += (tot >> 16) + min(eq_base + (tot & 0xffff), need_eq) - min(eq_base, need_eq);
+      eq_base += tot & 0xffff;
     }
   }
   if (threadIdx.x == 0) {
@@ -190,6 +243,22 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
     // expert choice drops nothing: an expert's demand is the c tokens it takes
     demand[e] = expert_choice ? k_e : n_all;
     kept[e] = k_e;
+  }
+
+  // 4. load statistics: the last block to finish reads every expert's counts
+  if (st.stats) {
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const uint32_t old = atomicAdd(counter, 1u);
+      s_last = old == gridDim.x - 1;
+      if (s_last) *counter = 0u;
+    }
+    __syncthreads();
+    if (s_last) {
+      __threadfence();
+      stats_final_block(demand, kept, st.colsum, T, N, st.stats);
+    }
   }
 }
 
@@ -199,7 +268,9 @@ int select_max_tokens() { return kSelMaxTokens; }
 
 cudaError_t launch_select(const int32_t* cand_idx, const float* cand_gate, int T, int kc, int N,
                           int expert_choice, int cap, int32_t* slot, uint8_t* keep,
-                          int32_t* demand, int32_t* kept, cudaStream_t s) {
+                          int32_t* demand, int32_t* kept, const StatsArgs& st, uint32_t* counter,
+                          cudaStream_t s) {
+  if (st.stats && !counter) return cudaErrorInvalidValue;
   const size_t smem = static_cast<size_t>(T) * 8;
   static bool attr_set[64] = {};  // per device; setting it twice is harmless
   int dev = 0;
@@ -212,9 +283,8 @@ cudaError_t launch_select(const int32_t* cand_idx, const float* cand_gate, int T
     if (err != cudaSuccess) return err;
     attr_set[dev] = true;
   }
-  select_kernel<<<N, kSelThreads, smem, s>>>(cand_idx, cand_gate, T, kc, N, expert_choice, cap,
-                                             slot, keep, demand, kept);
-  return cudaGetLastError();
+  return launch_pdl(select_kernel, N, kSelThreads, smem, s, cand_idx, cand_gate, T, kc, N,
+                    expert_choice, cap, slot, keep, demand, kept, st, counter);
 }
 
 }  // namespace moe

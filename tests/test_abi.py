@@ -134,13 +134,15 @@ def test_status_strings():
 
 
 def test_layer_stage_list_follows_the_config():
-    names = M.moe_layer_stages(_cfg(), with_stats=True)
-    assert names == ["router_logits", "route_tokens", "select", "dispatch", "expert_gemm1_swiglu",
-                     "expert_gemm2", "combine", "stats_partial", "stats_final"]
-    names = M.moe_layer_stages(_cfg(f_shared=128, logits_given=True), with_stats=False)
+    names = M.moe_layer_stages(_cfg())
+    assert names == ["router", "select", "dispatch", "expert_gemm1_swiglu", "expert_gemm2",
+                     "combine"]
+    names = M.moe_layer_stages(_cfg(f_shared=128, logits_given=True))
     assert names == ["route_tokens", "select", "dispatch", "expert_gemm1_swiglu", "expert_gemm2",
                      "shared_offsets", "shared_gemm1_swiglu", "shared_gemm2", "combine"]
-    assert M.lib().moe_layer_stages(ctypes.byref(_cfg(N=0)), 1, None, 0) == M.MOE_ERR_SHAPE
+    names = M.moe_layer_stages(_cfg(dtype="f32"))
+    assert names[:2] == ["router_logits", "route_tokens"]
+    assert M.lib().moe_layer_stages(ctypes.byref(_cfg(N=0)), None, 0) == M.MOE_ERR_SHAPE
 
 
 def test_trace_event_arguments_checked_on_the_host():
@@ -150,4 +152,5 @@ def test_trace_event_arguments_checked_on_the_host():
     assert lib.moe_set_trace_events(None, -1) == M.MOE_ERR_SHAPE
     handles = (ctypes.c_void_p * 40)()
     assert lib.moe_set_trace_events(handles, 33) == M.MOE_ERR_SHAPE
-    assert lib.moe_set_trace_events(handles, 2) == M.MOE_ERR_NULL  # NULL handles
+    assert lib.moe_set_trace_events(handles, 2) == M.MOE_OK  # NULL entries: no event there
+    assert lib.moe_set_trace_events(None, 0) == M.MOE_OK

@@ -116,7 +116,7 @@ def test_trace_events_time_every_stage():
     w = SMALL[3]  # expanded drop + shared expert: the longest stage list
     inp = W.make_inputs(w)
     cfg = G.M.config_from_workload(w)
-    names = G.M.moe_layer_stages(cfg, with_stats=True)
+    names = G.M.moe_layer_stages(cfg)
     d = {k: G.cuda(v) for k, v in inp.items()}
     ws = torch.zeros(G.M.workspace_size(cfg), dtype=torch.uint8, device="cuda")
     y = torch.empty((w.T, w.d), dtype=torch.bfloat16, device="cuda")

@@ -100,3 +100,54 @@ def test_router_logits_within_fp32_bound(name):
     diff = np.abs(Lg.cpu().numpy().astype(np.float64) - L.astype(np.float64))
     bound = G.logit_bound(G.np32(inp["x"]), G.np32(inp["W_r"]), L)
     assert np.all(diff <= bound), float((diff / bound).max())
+
+
+def _route_own_logits(w, inp, rws=None):
+    """moe_route with the router computing its own logits (on bf16 layers the
+    tensor-core router, which routes each tile in its last CTA)."""
+    cfg = G.M.config_from_workload(w)
+    sz = G.M.sizes(cfg)
+    dev = torch.device("cuda")
+    Lg = torch.empty((w.T, w.N), dtype=torch.float32, device=dev)
+    scores = torch.empty((w.T, w.N), dtype=torch.float32, device=dev)
+    idx = torch.full((w.T, sz.kc), -7, dtype=torch.int32, device=dev)
+    gate = torch.full((w.T, sz.kc), -7.0, dtype=torch.float32, device=dev)
+    if rws is None:
+        rws = torch.zeros(G.M.route_workspace_size(cfg), dtype=torch.uint8, device=dev)
+    G.M.moe_route(cfg, G.cuda(inp["x"]), G.cuda(inp["W_r"]), G.cuda(inp["bias"]), Lg, scores,
+                  None if w.mode == W.EXPERT_CHOICE else idx, gate, rws)
+    torch.cuda.synchronize()
+    return Lg.cpu().numpy(), scores.cpu().numpy(), idx.cpu().numpy(), gate.cpu().numpy()
+
+
+def _assert_routing_of(w, L, scores, idx, gate):
+    rt = G.oracle_route(w, L)
+    assert np.array_equal(scores.view(np.uint32), rt["p"].view(np.uint32)), "scores differ"
+    if w.mode != W.EXPERT_CHOICE:
+        assert np.array_equal(idx, rt["idx"]), "candidate experts differ"
+    assert np.array_equal(gate.view(np.uint32), rt["gate"].view(np.uint32)), "gates differ"
+
+
+@pytest.mark.parametrize("name", ["expert_choice_bf16", "mixtral_bf16_gamma1", "finegrained_bf16",
+                                  "finegrained_bf16_expanded", "decode_bf16"])
+def test_fused_router_routes_its_own_logits_bit_exactly(name):
+    """The tensor-core router's in-kernel routing equals the oracle's routing
+    of the logits that router produced."""
+    w = W.ALL[name]
+    inp = W.make_inputs(w, with_experts=False)
+    _assert_routing_of(w, *_route_own_logits(w, inp))
+
+
+def test_router_workspace_reused_across_shapes():
+    """The router's per-tile arrival counters return to zero after every
+    launch, so one workspace serves configs with different split counts."""
+    big = W.Workload("reuse_big", T=1000, d=1024, N=16, f=64, k=2, zipf_s=1.0)
+    small = W.Workload("reuse_small", T=300, d=256, N=8, f=64, k=2, mode=W.CAPACITY_DROP,
+                       gamma=1.0)
+    n = max(G.M.route_workspace_size(G.M.config_from_workload(v)) for v in (big, small))
+    rws = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    for w in (big, small, big, small):
+        inp = W.make_inputs(w, with_experts=False)
+        _assert_routing_of(w, *_route_own_logits(w, inp, rws))
+    ctrl = rws[:G.M.MOE_CTRL_BYTES].view(torch.int32).cpu().numpy()
+    assert (ctrl == 0).all(), "control block not back at zero"
