@@ -120,15 +120,14 @@ size_t moe_workspace_size(const moe_config* cfg);
 
 /* Every workspace (moe_layer_forward, moe_route, moe_expert_ffn,
  * moe_grouped_gemm) begins with a 1024-byte control block: the sticky status
- * word and the arrival counters of kernels whose last block finishes the step
- * (the tensor-core router's per-tile routing, the load statistics). The
- * control block must be zero before the workspace's first use (allocate it
- * zeroed, or call moe_clear_device_status); every call leaves the counters at
- * zero again. Calls that share a workspace must not overlap on the GPU. */
+ * word and the arrival counter of the selection kernel, whose last block
+ * finishes the load statistics. The control block must be zero before the
+ * workspace's first use (allocate it zeroed, or call
+ * moe_clear_device_status); every call leaves the counter at zero again.
+ * Calls that share a workspace must not overlap on the GPU. */
 #define MOE_CTRL_BYTES 1024
 
-/* Bytes of workspace moe_route needs (the control block and, for the
- * tensor-core router, the per-split partial logits). */
+/* Bytes of workspace moe_route needs (the control block). */
 size_t moe_route_workspace_size(const moe_config* cfg);
 
 /* Bytes of workspace moe_expert_ffn needs for `rows_max` rows of hidden width f. */
@@ -158,11 +157,11 @@ size_t moe_ffn_workspace_size(int64_t rows_max, int32_t f, int32_t dtype);
  *            drop; NULL = contiguous shards, group floor(t*G/T), G = N/group_size.
  *   ws       >= moe_route_workspace_size(cfg) bytes, 256-byte aligned.
  * bf16 layers with N a multiple of 8 compute the logits on the tcgen05 tensor
- * cores, the d axis split over several CTAs per 128-token tile; the last CTA
- * of each tile to finish adds the splits' fp32 partials in a fixed order, then
- * the bias, and routes the tile's tokens in the same launch. Other shapes use
- * fp32 FMA and a second kernel for the routing. Either way L is
- * fp32-accumulated, not the exact dot product.
+ * cores, one thread-block cluster per 128-token tile splitting d; the
+ * cluster's fp32 partials are added in k order, then the bias, and the tokens
+ * are routed in the same launch. Other shapes use fp32 FMA and a second
+ * kernel for the routing. Either way L is fp32-accumulated, not the exact dot
+ * product.
  */
 int moe_route(const moe_config* cfg, const void* x, const void* W_router, const float* bias,
               float* logits, float* scores, int32_t* cand_idx, float* cand_gate,
@@ -295,7 +294,7 @@ int moe_combine(const moe_config* cfg, const void* op, const float* row_gate,
  * doubles; layout above). scores [T, N] are the router probabilities; their
  * column sums are taken in fixed point (units of 2^-40, exact u64 sums), so
  * P_i does not depend on the order of the additions.
- * ws >= 8 * N * ceil(T / 128) bytes, 16-byte aligned (scratch).
+ * ws >= 8 * N * ceil(T / 8) bytes, 16-byte aligned (scratch).
  */
 int moe_load_stats(const moe_config* cfg, const int32_t* demand, const int32_t* kept,
                    const float* scores, double* stats, void* ws, size_t ws_bytes, void* stream);
@@ -327,9 +326,10 @@ int moe_layer_forward(const moe_config* cfg, const void* x, const void* W_router
  * Stage tracing of moe_layer_forward (profiling aid; the pages have no
  * counterpart). moe_layer_stages returns how many kernels moe_layer_forward
  * launches for `cfg` and, when `names` is non-NULL, stores up to max_names
- * static stage names in launch order: the routing ("router" for the fused
- * tensor-core router, "router_logits" + "route_tokens" on the FMA path,
- * "route_tokens" alone with MOE_LOGITS_GIVEN), select (which also finishes
+ * static stage names in launch order: the routing ("router" for the
+ * tensor-core router, which routes in the same launch; "router_logits" +
+ * "route_tokens" on the FMA path; "route_tokens" alone with
+ * MOE_LOGITS_GIVEN), select (which also finishes
  * the load statistics when a stats pointer is passed), dispatch,
  * expert_gemm1_swiglu, expert_gemm2, [shared_offsets, shared_gemm1_swiglu,
  * shared_gemm2 when f_shared > 0], combine. Returns a negative MOE_ERR_* for

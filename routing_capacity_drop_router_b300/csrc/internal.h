@@ -32,78 +32,62 @@ cudaError_t launch_pdl(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem,
 cudaError_t launch_router_logits(int dtype, const void* x, const void* W_r, const float* bias,
                                  float* L, int T, int d, int N, cudaStream_t s);
 
-// The first kCtrlBytes of every workspace: the sticky status word, then
-// arrival counters of the kernels that finish with a last-block step (they
-// count modulo their number of blocks, so they must start at zero: the
-// workspace is zeroed, or moe_clear_device_status is called, before first use).
+// The first kCtrlBytes of every workspace: the sticky status word, then the
+// arrival counter of the selection kernel's last-block statistics step (it
+// must start at zero: the workspace is zeroed, or moe_clear_device_status is
+// called, before first use; the last block resets it).
 constexpr size_t kCtrlBytes = 1024;
 constexpr int kCtrlSelectCounter = 1;    // int32 index in the control block
-constexpr int kCtrlRouterCounters = 16;  // int32 index of the router's per-tile counters
-constexpr int kRouteTile = 128;          // tokens per routing block / router tile
-constexpr int kMaxRouterTiles = (static_cast<int>(kCtrlBytes) / 4) - kCtrlRouterCounters;
+constexpr int kRouteTile = 128;          // tokens per router tile (tensor-core M)
 
-// Per-token routing (route_token.cuh) inputs and outputs. The logits of
-// 128-token tile m are the sum, in slot order, of nslots(m) fp32 slices
-// partial[(m * max_slots + s) * 128 * N ...] of [128, N] each (plus bias):
-// one slice holding the logits themselves, or the k-segments of the
-// tensor-core router (see router_segments below).
+// Per-token routing (route_token.cuh) inputs and outputs.
 struct RouteArgs {
-  const float* partial = nullptr;
-  int max_slots = 1;
-  int seg_ctas = 0, seg_total = 0, seg_kb = 0;  // router partition; seg_ctas == 0: one slot
-  const float* bias = nullptr;     // [N], added after the slices
-  float* logits_out = nullptr;     // [T, N] nullable
+  const float* logits = nullptr;   // [T, N] input of the routing kernel (route.cu)
+  const float* bias = nullptr;     // [N], added to the logits by the tensor-core router
+  float* logits_out = nullptr;     // [T, N] nullable (tensor-core router)
   float* scores = nullptr;         // [T, N] nullable
   int32_t* cand_idx = nullptr;     // [T, kc] (unused under expert choice)
   float* cand_gate = nullptr;      // [T, kc]
   const int32_t* home_group = nullptr;
-  unsigned long long* colsum = nullptr;  // [ceil(T/128), N] fixed-point column sums of p, nullable
+  unsigned long long* colsum = nullptr;  // [rows, N] fixed-point column sums of p, nullable
   int T = 0, N = 0, k = 0, m = 0, group_size = 1, renorm = 0, ec = 0;
 };
 
-// Partition of the tensor-core router's work: the m_tiles * num_kb k-blocks,
-// tile-major, split into `ctas` contiguous ranges of near-equal length; CTA i
-// takes [floor(i*W/G), floor((i+1)*W/G)). A range may cross one tile
-// boundary, so a tile's logits are the sum of the segments of consecutive
-// CTAs; the CTA holding k-block q is ceil((q+1)*G/W) - 1.
-__host__ __device__ inline int router_cta_of(long long q, int G, long long W) {
-  return static_cast<int>(((q + 1) * G + W - 1) / W) - 1;
-}
-__host__ __device__ inline int router_tile_segments(int m, int num_kb, int G, long long W) {
-  const long long q0 = static_cast<long long>(m) * num_kb;
-  return router_cta_of(q0 + num_kb - 1, G, W) - router_cta_of(q0, G, W) + 1;
-}
-
-// Router logits on tcgen05 (bf16, N % 8 == 0): per-segment partials in
-// ra.partial ([m_tiles][max_slots][128][N] fp32), and in the same launch the
-// last CTA to finish a tile routes its tokens.
-struct RouterSplit {
-  int ctas = 1;       // G
-  int num_kb = 1;     // k-blocks of 64 per tile
-  long long total = 1;  // W = m_tiles * num_kb
-  int max_slots = 1;  // most segments any tile has
+// Router logits on tcgen05 (bf16, d % 64 == 0, N % 8 == 0, N <= 256): one
+// thread-block cluster of `cluster` CTAs per 128-token tile splits d; the
+// partial logits meet in distributed shared memory and each CTA routes
+// 128 / cluster of the tile's tokens. Column sums: one row per CTA.
+struct RouterPlan {
+  int cluster = 1;  // CTAs per tile (a power of two dividing d / 64, <= 8)
+  int m_tiles = 0;
+  int colsum_rows = 0;
 };
 bool router_tc_supported(int dtype, int d, int N);
-RouterSplit router_split_plan(int T, int d, int N);
-cudaError_t launch_router_tc(const void* x, const void* W_r, int d, const RouterSplit& plan,
-                             const RouteArgs& ra, uint32_t* tile_counters, int32_t* status,
-                             cudaStream_t s);
+RouterPlan router_plan(int T, int d, int N);
+cudaError_t launch_router_tc(const void* x, const void* W_r, int d, const RouterPlan& plan,
+                             const RouteArgs& ra, int32_t* status, cudaStream_t s);
 
-// Per-token scores, candidates and gates from fp32 logits (ra.partial).
+// Per-token scores, candidates and gates from fp32 logits [T, N] (ra.logits),
+// one warp segment per token; colsum rows: route_tokens_colsum_rows(T, N).
+int route_tokens_colsum_rows(int T, int N);
 cudaError_t launch_route_tokens(const RouteArgs& ra, cudaStream_t s);
 
-// Load statistics. colsum: [ceil(T/128), N] fixed-point column sums of the
-// scores (route_tokens / router_tc with ra.colsum, or launch_colsum).
+
+// Load statistics. colsum: [rows, N] fixed-point column sums of the scores
+// (the routing kernels with ra.colsum, or launch_colsum with
+// colsum_kernel_rows(T) rows).
 struct StatsArgs {
   const unsigned long long* colsum = nullptr;
+  int rows = 0;             // rows of colsum
   double* stats = nullptr;  // [MOE_STATS_LEN]
 };
-size_t colsum_bytes(int T, int N);
+size_t colsum_bytes(int T, int N);  // enough rows for either router
+int colsum_kernel_rows(int T);
 cudaError_t launch_colsum(const float* scores, int T, int N, unsigned long long* colsum,
                           cudaStream_t s);
 cudaError_t launch_stats_final(const int32_t* demand, const int32_t* kept,
-                               const unsigned long long* colsum, int T, int N, double* stats,
-                               cudaStream_t s);
+                               const unsigned long long* colsum, int rows, int T, int N,
+                               double* stats, cudaStream_t s);
 
 // Per-expert selection (token choice: rank only; capacity drop: top-cap by
 // gate; expert choice: top-cap tokens by score). With st.stats set, the last

@@ -125,7 +125,7 @@ int layer_stage_names(const moe_config& c, const char** names, int max_names) {
   if (c.flags & MOE_LOGITS_GIVEN) {
     list[n++] = "route_tokens";
   } else if (router_tc_supported(c.dtype, c.d, c.N)) {
-    list[n++] = "router";
+    list[n++] = "router";  // tensor-core logits and routing in one launch
   } else {
     list[n++] = "router_logits";
     list[n++] = "route_tokens";
@@ -149,29 +149,17 @@ int status_from(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_LAUN
 
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
-// Scratch of the tensor-core router: per tile, one fp32 [128, N] partial per
-// k-segment.
-size_t router_partial_bytes(const moe_config& c) {
-  if ((c.flags & MOE_LOGITS_GIVEN) || !router_tc_supported(c.dtype, c.d, c.N) || c.T == 0) return 0;
-  const RouterSplit p = router_split_plan(c.T, c.d, c.N);
-  const size_t m_tiles = (static_cast<size_t>(c.T) + kRouteTile - 1) / kRouteTile;
-  return m_tiles * p.max_slots * kRouteTile * c.N * sizeof(float);
-}
-
 // Logits (unless given) and per-token routing. logits: output buffer, or the
-// input when MOE_LOGITS_GIVEN. partial: router scratch (router_partial_bytes);
-// ctrl: the workspace's control block; colsum: column sums of the scores for
-// the load statistics (nullable).
+// input when MOE_LOGITS_GIVEN; colsum: column sums of the scores for the
+// load statistics (nullable), whose row count is stored in *colsum_rows.
 int run_router(const moe_config& c, bool ec, const void* x, const void* W_r, const float* bias,
                float* logits, float* scores, int32_t* cand_idx, float* cand_gate,
-               const int32_t* home_group, float* partial, int32_t* ctrl,
-               unsigned long long* colsum, cudaStream_t s, Tracer* tr = nullptr) {
+               const int32_t* home_group, int32_t* status, unsigned long long* colsum,
+               int* colsum_rows, cudaStream_t s, Tracer* tr = nullptr) {
   const bool given = (c.flags & MOE_LOGITS_GIVEN) != 0;
   const bool tc = !given && router_tc_supported(c.dtype, c.d, c.N);
-  const int stages = (given || tc) ? 1 : 2;
-  if (c.T == 0) return (!tr || tr->mark(stages)) ? MOE_OK : MOE_ERR_LAUNCH;
   RouteArgs ra;
-  ra.partial = logits;
+  ra.logits = logits;
   ra.scores = scores;
   ra.cand_idx = cand_idx;
   ra.cand_gate = cand_gate;
@@ -185,32 +173,28 @@ int run_router(const moe_config& c, bool ec, const void* x, const void* W_r, con
   ra.renorm = c.renorm;
   ra.ec = ec ? 1 : 0;
   if (tc) {
-    const RouterSplit p = router_split_plan(c.T, c.d, c.N);
-    ra.partial = partial;
-    ra.max_slots = p.max_slots;
-    ra.seg_ctas = p.ctas;
-    ra.seg_kb = p.num_kb;
-    ra.seg_total = p.total;
+    const RouterPlan p = router_plan(c.T, c.d, c.N);
+    if (colsum_rows) *colsum_rows = p.colsum_rows;
     ra.bias = bias;
     ra.logits_out = logits;
-    if (launch_router_tc(x, W_r, c.d, p, ra,
-                         reinterpret_cast<uint32_t*>(ctrl + kCtrlRouterCounters), ctrl,
-                         s) != cudaSuccess ||
-        (tr && !tr->mark()))
+    if (c.T > 0 && launch_router_tc(x, W_r, c.d, p, ra, status, s) != cudaSuccess)
       return MOE_ERR_LAUNCH;
-    return MOE_OK;
+    return (!tr || tr->mark()) ? MOE_OK : MOE_ERR_LAUNCH;
   }
+  if (colsum_rows) *colsum_rows = route_tokens_colsum_rows(c.T, c.N);
   if (!given) {
-    if (launch_router_logits(c.dtype, x, W_r, bias, logits, c.T, c.d, c.N, s) != cudaSuccess ||
+    if ((c.T > 0 &&
+         launch_router_logits(c.dtype, x, W_r, bias, logits, c.T, c.d, c.N, s) != cudaSuccess) ||
         (tr && !tr->mark()))
       return MOE_ERR_LAUNCH;
   }
-  if (launch_route_tokens(ra, s) != cudaSuccess || (tr && !tr->mark())) return MOE_ERR_LAUNCH;
+  if ((c.T > 0 && launch_route_tokens(ra, s) != cudaSuccess) || (tr && !tr->mark()))
+    return MOE_ERR_LAUNCH;
   return MOE_OK;
 }
 
 struct Layout {
-  size_t ctrl, router_partial, logits, scores, cand_idx, cand_gate, slot, keep, demand, kept, offsets,
+  size_t ctrl, logits, scores, cand_idx, cand_gate, slot, keep, demand, kept, offsets,
       shared_offsets, row_token, row_gate, tok_rows, xp, hp, op, shared_out, colsum, total;
 };
 
@@ -224,7 +208,6 @@ Layout layout(const moe_config& c, const Derived& d) {
   };
   const size_t T = c.T, N = c.N, kc = d.kc, R = d.rows_max, dd = c.d;
   L.ctrl = take(kCtrlBytes);
-  L.router_partial = take(router_partial_bytes(c));
   L.logits = take(T * N * 4);
   L.scores = take(T * N * 4);
   L.cand_idx = take(T * kc * 4);
@@ -311,7 +294,7 @@ size_t moe_ffn_workspace_size(int64_t rows_max, int32_t f, int32_t dtype) {
 size_t moe_route_workspace_size(const moe_config* cfg) {
   Derived d;
   if (validate(cfg, &d) != MOE_OK) return 0;
-  return kCtrlBytes + align256(router_partial_bytes(*cfg));
+  return kCtrlBytes;
 }
 
 int moe_route(const moe_config* cfg, const void* x, const void* W_router, const float* bias,
@@ -329,9 +312,7 @@ int moe_route(const moe_config* cfg, const void* x, const void* W_router, const 
   if (reinterpret_cast<uintptr_t>(ws) & 255u) return MOE_ERR_ALIGN;
   if (ws_bytes < moe_route_workspace_size(cfg)) return MOE_ERR_WORKSPACE;
   return run_router(*cfg, d.ec, x, W_router, bias, logits, scores, cand_idx, cand_gate,
-                    home_group,
-                    reinterpret_cast<float*>(static_cast<unsigned char*>(ws) + kCtrlBytes),
-                    static_cast<int32_t*>(ws), nullptr, as_stream(stream));
+                    home_group, static_cast<int32_t*>(ws), nullptr, nullptr, as_stream(stream));
 }
 
 int moe_capacity_drop(const moe_config* cfg, const int32_t* cand_idx, const float* cand_gate,
@@ -431,7 +412,8 @@ int moe_load_stats(const moe_config* cfg, const int32_t* demand, const int32_t* 
   cudaStream_t s = as_stream(stream);
   auto* colsum = static_cast<unsigned long long*>(ws);
   if (launch_colsum(scores, cfg->T, cfg->N, colsum, s) != cudaSuccess) return MOE_ERR_LAUNCH;
-  return status_from(launch_stats_final(demand, kept, colsum, cfg->T, cfg->N, stats, s));
+  return status_from(launch_stats_final(demand, kept, colsum, colsum_kernel_rows(cfg->T), cfg->T,
+                                        cfg->N, stats, s));
 }
 
 int moe_layer_forward(const moe_config* cfg, const void* x, const void* W_router,
@@ -477,11 +459,13 @@ int moe_layer_forward(const moe_config* cfg, const void* x, const void* W_router
   void* ys = c.f_shared > 0 ? at<void>(ws, L.shared_out) : nullptr;
 
   unsigned long long* colsum = stats ? at<unsigned long long>(ws, L.colsum) : nullptr;
-  st = run_router(c, d.ec, x, W_router, bias, Lg, scores, cand_idx, cand_gate, home_group,
-                  at<float>(ws, L.router_partial), ctrl, colsum, s, &tr);
+  int colsum_rows = 0;
+  st = run_router(c, d.ec, x, W_router, bias, Lg, scores, cand_idx, cand_gate, home_group, status,
+                  colsum, &colsum_rows, s, &tr);
   if (st != MOE_OK) return st;
   StatsArgs sa;
   sa.colsum = colsum;
+  sa.rows = colsum_rows;
   sa.stats = stats;
   if (launch_select(cand_idx, cand_gate, c.T, d.kc, c.N, d.ec ? 1 : 0, d.cap, slot, keep, demand,
                     kept, sa, reinterpret_cast<uint32_t*>(ctrl + kCtrlSelectCounter),

@@ -118,14 +118,47 @@ cudaError_t logits_dispatch_ne(const E* x, const E* W_r, const float* bias, floa
 }
 
 // ---------------------------------------------------------------------------
-// Per-token routing from fp32 logits (route_token.cuh), 128 tokens per block,
-// one thread per token; the block also writes its tile's column sums of p.
+// Per-token routing from fp32 logits [T, N] (route_token.cuh): 8 warps per
+// block, each warp routing 32 / W tokens at once (one W-lane segment each);
+// the block writes one row of column sums of p.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kRouteTile) route_tokens_kernel(const RouteArgs a) {
-  extern __shared__ float s_p[];
+constexpr int kRouteWarpsPerBlock = 8;
+
+template <int W, int PER>
+__global__ void __launch_bounds__(kRouteWarpsPerBlock * 32) route_tokens_kernel(const RouteArgs a) {
+  __shared__ unsigned long long s_cs[256];
   pdl_launch_dependents();
   pdl_wait();
-  route_tile(a, blockIdx.x, s_p);
+  constexpr int kTokensPerBlock = kRouteWarpsPerBlock * (32 / W);
+  const int N = a.N;
+  unsigned long long* cs = a.colsum ? s_cs : nullptr;
+  if (cs) {
+    for (int e = threadIdx.x; e < N; e += blockDim.x) cs[e] = 0ull;
+    __syncthreads();
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int ls = lane % W;
+  const int t = blockIdx.x * kTokensPerBlock + warp * (32 / W) + lane / W;
+  const bool valid = t < a.T;
+  float l[PER];
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int e = ls + W * j;
+    l[j] = (valid && e < N) ? a.logits[static_cast<size_t>(t) * N + e] : 0.f;
+  }
+  route_token_seg<W, PER>(a, t, valid, l, cs);
+  if (cs) {
+    __syncthreads();
+    for (int e = threadIdx.x; e < N; e += blockDim.x)
+      a.colsum[static_cast<size_t>(blockIdx.x) * N + e] = cs[e];
+  }
+}
+
+template <int W, int PER>
+cudaError_t route_launch(const RouteArgs& a, cudaStream_t s) {
+  constexpr int kTokensPerBlock = kRouteWarpsPerBlock * (32 / W);
+  return launch_pdl(route_tokens_kernel<W, PER>, (a.T + kTokensPerBlock - 1) / kTokensPerBlock,
+                    kRouteWarpsPerBlock * 32, 0, s, a);
 }
 
 }  // namespace
@@ -140,22 +173,20 @@ cudaError_t launch_router_logits(int dtype, const void* x, const void* W_r, cons
                             T, d, N, s);
 }
 
+int route_tokens_colsum_rows(int T, int N) {
+  const int per_block = kRouteWarpsPerBlock * (32 / route_seg_width(N));
+  return (T + per_block - 1) / per_block;
+}
+
 cudaError_t launch_route_tokens(const RouteArgs& a, cudaStream_t s) {
   if (a.T == 0) return cudaSuccess;
-  if (a.N > 256) return cudaErrorInvalidValue;
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
-  if (err != cudaSuccess) return err;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_set[dev]) {
-    err = cudaFuncSetAttribute(route_tokens_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(route_tile_smem(256)));
-    if (err != cudaSuccess) return err;
-    attr_set[dev] = true;
-  }
-  return launch_pdl(route_tokens_kernel, (a.T + kRouteTile - 1) / kRouteTile, kRouteTile,
-                    route_tile_smem(a.N), s, a);
+  if (a.N <= 8) return route_launch<8, 1>(a, s);
+  if (a.N <= 16) return route_launch<16, 1>(a, s);
+  if (a.N <= 32) return route_launch<32, 1>(a, s);
+  if (a.N <= 64) return route_launch<32, 2>(a, s);
+  if (a.N <= 128) return route_launch<32, 4>(a, s);
+  if (a.N <= 256) return route_launch<32, 8>(a, s);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace moe

@@ -1,22 +1,24 @@
-// Router logits on the tcgen05 tensor cores (bf16 in, fp32 accumulate), with
+// Router logits on the tcgen05 tensor cores (bf16 in, fp32 accumulate), and
 // the per-token routing in the same launch.
 //
 // "Understanding Mixture of Experts", section "Expert and Router": the router
 // scores every token against every expert, L = x W_r (+ b). The read of x
-// bounds this step, so the design goal is an even spread of that read: the
-// m_tiles * (d / 64) k-blocks (128 tokens x 64 of d each), tile-major, are cut
-// into one contiguous range per CTA (2 CTAs per SM for N <= 64), so every CTA
-// streams the same number of k-blocks through its 4-stage TMA ring whatever
-// T and d are. A range covers at most two tiles; for each tile one thread
-// issues 128 x (64*NB) x 16 MMAs into its own TMEM accumulator, and the
-// accumulator is written as one fp32 segment partial[tile][slot] (slot = the
-// CTA's rank among the tile's CTAs, i.e. k order). Each CTA then counts
-// itself in the tile's arrival counter; the last to arrive adds the tile's
-// segments in slot order plus the bias and routes its 128 tokens
-// (route_token.cuh), so the logits and every decision are deterministic and
-// the routing needs no second launch. W_r [d, N] is read as stored
-// (MN-major, N contiguous) in 64-expert TMA boxes; experts past N load as
-// zeros.
+// bounds this step, so the design goal is an even spread of that read over
+// the SMs. Each 128-token tile is one thread-block cluster of C CTAs (C a
+// power of two <= 8 chosen so that all clusters are resident at once): CTA r
+// of the cluster streams k-blocks [r*d/(64C), (r+1)*d/(64C)) of the tile's x
+// rows and of W_r through a 4-stage TMA ring, and one thread issues
+// 128 x (64*NB) x 16 MMAs into TMEM. W_r [d, N] is read as stored (MN-major,
+// N contiguous) in 64-expert TMA boxes; experts past N load as zeros.
+//
+// Tail, through distributed shared memory: after a cluster barrier (every
+// CTA's MMAs are done, so its stage buffers are free) each CTA writes TMEM
+// row i of its partial logits into the stage buffer of the CTA that routes
+// token i (CTA i / (128/C)), at the slot of its own rank; after a second
+// cluster barrier each CTA adds, for its 128/C tokens, the C partials in rank
+// order (= k order) and the bias, and routes them (route_token.cuh). So the
+// logits and every decision are deterministic, and no partial goes through
+// global memory.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -35,16 +37,17 @@ constexpr int kRM = 128;        // tokens per tile (MMA M)
 constexpr int kRK = 64;         // k per stage
 constexpr int kRStages = 4;
 constexpr int kRThreads = 128;  // 4 warps: producer, MMA, then all four drain TMEM
-static_assert(kRM == kRouteTile && kRThreads == kRouteTile, "one routing thread per tile row");
+static_assert(kRM == kRouteTile && kRThreads == kRouteTile, "one drain thread per tile row");
 constexpr int kRABytes = kRM * kRK * 2;
 constexpr int kRBoxBytes = 64 * kRK * 2;
 constexpr unsigned long long kRWaitNs = 1000000000ull;
 constexpr int kErrDeviceTimeout = -7;  // MOE_ERR_DEVICE_TIMEOUT
+constexpr int kMaxCluster = 8;
 
 struct __align__(8) RouterCtrl {
   unsigned long long full[kRStages];
   unsigned long long empty[kRStages];
-  unsigned long long acc_full[2];
+  unsigned long long acc_full;
   unsigned long long drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -54,23 +57,44 @@ template <int NB>
 constexpr int router_smem_bytes() {
   return 1024 + kRStages * (kRABytes + NB * kRBoxBytes) + static_cast<int>(sizeof(RouterCtrl));
 }
-// the routing tail reuses the stage buffers for its [128, N + 1] staging array
-static_assert(route_tile_smem(64) <= kRStages * (kRABytes + 1 * kRBoxBytes), "stage reuse");
-static_assert(route_tile_smem(128) <= kRStages * (kRABytes + 2 * kRBoxBytes), "stage reuse");
-static_assert(route_tile_smem(256) <= kRStages * (kRABytes + 4 * kRBoxBytes), "stage reuse");
+// the tail receives 128 rows x N fp32 partials into the stage buffers
+static_assert(128 * 64 * 4 <= kRStages * (kRABytes + 1 * kRBoxBytes), "receive buffer");
+static_assert(128 * 128 * 4 <= kRStages * (kRABytes + 2 * kRBoxBytes), "receive buffer");
+static_assert(128 * 256 * 4 <= kRStages * (kRABytes + 4 * kRBoxBytes), "receive buffer");
 
-template <int NB>
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+// Address of the same shared-memory location in cluster CTA `rank`.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
+}
+
+template <int NB, int W, int PER>
 __global__ void __launch_bounds__(kRThreads) router_tc_kernel(
     const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-    const RouteArgs ra, uint32_t* __restrict__ tile_counters, int32_t* __restrict__ status) {
+    const RouteArgs ra, int num_kb, int32_t* __restrict__ status) {
   constexpr int kStageBytes = kRABytes + NB * kRBoxBytes;
-  constexpr uint32_t kCols = 64u * NB;  // accumulator columns of one segment
-  constexpr uint32_t kAlloc = 2u * kCols;
+  constexpr uint32_t kCols = 64u * NB;  // accumulator columns (>= 64: a valid allocation)
   // kind::f16 instruction descriptor: D fp32, A/B bf16, A K-major, B MN-major,
   // N = 64*NB, M = 128.
   constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
                               ((kCols >> 3) << 17) | (static_cast<uint32_t>(kRM >> 4) << 24);
   extern __shared__ unsigned char smem_raw[];
+  __shared__ unsigned long long s_cs[256];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   unsigned char* smem = smem_raw + (base - raw);
@@ -78,42 +102,31 @@ __global__ void __launch_bounds__(kRThreads) router_tc_kernel(
   volatile int* abort_flag = &ctrl->abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = ra.T, N = ra.N;
-  const int G = static_cast<int>(gridDim.x), num_kb = ra.seg_kb;
-  const long long W = ra.seg_total;
-
-  // ---- this CTA's k-blocks, cut at the tile boundary into <= 2 segments ----
-  const long long q0 = static_cast<long long>(blockIdx.x) * W / G;
-  const long long q1 = static_cast<long long>(blockIdx.x + 1) * W / G;
-  int nseg = 0, seg_tile[2] = {0, 0}, seg_kb0[2] = {0, 0}, seg_kb1[2] = {0, 0}, seg_slot[2] = {0, 0};
-  for (long long q = q0; q < q1 && nseg < 2;) {
-    const int m = static_cast<int>(q / num_kb);
-    const long long tile_end = static_cast<long long>(m + 1) * num_kb;
-    const long long e = q1 < tile_end ? q1 : tile_end;
-    seg_tile[nseg] = m;
-    seg_kb0[nseg] = static_cast<int>(q - static_cast<long long>(m) * num_kb);
-    seg_kb1[nseg] = static_cast<int>(e - static_cast<long long>(m) * num_kb);
-    seg_slot[nseg] = static_cast<int>(blockIdx.x) -
-                     router_cta_of(static_cast<long long>(m) * num_kb, G, W);
-    ++nseg;
-    q = e;
-  }
+  uint32_t nrank;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(nrank));
+  const int cl = static_cast<int>(nrank);
+  const uint32_t rank = cluster_rank();
+  const int tile = static_cast<int>(blockIdx.x) / cl;
+  const int kb_per = num_kb / cl;
+  const int kb0 = static_cast<int>(rank) * kb_per, kb1 = kb0 + kb_per;
+  const int tpc = kRM / cl;  // tokens routed by each CTA of the cluster
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kRStages; ++s) {
       mbar_init(smem_u32(&ctrl->full[s]), 1);
       mbar_init(smem_u32(&ctrl->empty[s]), 1);
     }
-    mbar_init(smem_u32(&ctrl->acc_full[0]), 1);
-    mbar_init(smem_u32(&ctrl->acc_full[1]), 1);
+    mbar_init(smem_u32(&ctrl->acc_full), 1);
     mbar_init(smem_u32(&ctrl->drain), 1);
     ctrl->abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
+  for (int e = threadIdx.x; e < 256; e += blockDim.x) s_cs[e] = 0ull;
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(&ctrl->tmem_base)),
-                 "r"(kAlloc)
+                 "r"(kCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -132,25 +145,23 @@ __global__ void __launch_bounds__(kRThreads) router_tc_kernel(
     bool issued[kRStages] = {};
     uint32_t issued_phase[kRStages] = {};
     bool ok = true;
-    for (int sg = 0; ok && sg < nseg; ++sg) {
-      for (int kb = seg_kb0[sg]; kb < seg_kb1[sg]; ++kb) {
-        if (!mbar_wait(smem_u32(&ctrl->empty[stage]), phase ^ 1u, abort_flag, kRWaitNs)) {
-          ok = false;
-          break;
-        }
-        const uint32_t fb = smem_u32(&ctrl->full[stage]);
-        mbar_expect_tx(fb, kStageBytes);
-        const uint32_t sa = base + stage * kStageBytes;
-        tma_load_2d(sa, &tmX, kb * kRK, seg_tile[sg] * kRM, fb);
+    for (int kb = kb0; kb < kb1; ++kb) {
+      if (!mbar_wait(smem_u32(&ctrl->empty[stage]), phase ^ 1u, abort_flag, kRWaitNs)) {
+        ok = false;
+        break;
+      }
+      const uint32_t fb = smem_u32(&ctrl->full[stage]);
+      mbar_expect_tx(fb, kStageBytes);
+      const uint32_t sa = base + stage * kStageBytes;
+      tma_load_2d(sa, &tmX, kb * kRK, tile * kRM, fb);
 #pragma unroll
-        for (int j = 0; j < NB; ++j)
-          tma_load_2d(sa + kRABytes + j * kRBoxBytes, &tmW, 64 * j, kb * kRK, fb);
-        issued[stage] = true;
-        issued_phase[stage] = phase;
-        if (++stage == kRStages) {
-          stage = 0;
-          phase ^= 1u;
-        }
+      for (int j = 0; j < NB; ++j)
+        tma_load_2d(sa + kRABytes + j * kRBoxBytes, &tmW, 64 * j, kb * kRK, fb);
+      issued[stage] = true;
+      issued_phase[stage] = phase;
+      if (++stage == kRStages) {
+        stage = 0;
+        phase ^= 1u;
       }
     }
     if (!ok) {  // drain copies in flight before the CTA can exit (bounded)
@@ -162,31 +173,28 @@ __global__ void __launch_bounds__(kRThreads) router_tc_kernel(
       }
     }
   } else if (warp == 1 && lane == 0) {
-    // ---- MMA issuer: segment sg accumulates in TMEM columns [sg*kCols, ...) ----
+    // ---- MMA issuer ----
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int sg = 0; ok && sg < nseg; ++sg) {
-      const uint32_t d_tmem = tmem + static_cast<uint32_t>(sg) * kCols;
-      for (int kb = seg_kb0[sg]; kb < seg_kb1[sg]; ++kb) {
-        if (!mbar_wait(smem_u32(&ctrl->full[stage]), phase, abort_flag, kRWaitNs)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t sa = base + stage * kStageBytes;
-#pragma unroll
-        for (int kk = 0; kk < kRK / 16; ++kk)
-          tc_mma(d_tmem, kmajor_desc(sa, kk), mnmajor_desc(sa + kRABytes, kk, kRBoxBytes), kIdesc,
-                 (kb > seg_kb0[sg] || kk > 0) ? 1u : 0u);
-        tc_commit(smem_u32(&ctrl->empty[stage]));
-        if (++stage == kRStages) {
-          stage = 0;
-          phase ^= 1u;
-        }
+    for (int kb = kb0; kb < kb1; ++kb) {
+      if (!mbar_wait(smem_u32(&ctrl->full[stage]), phase, abort_flag, kRWaitNs)) {
+        ok = false;
+        break;
       }
-      if (ok) tc_commit(smem_u32(&ctrl->acc_full[sg]));
+      tc_fence_after();
+      const uint32_t sa = base + stage * kStageBytes;
+#pragma unroll
+      for (int kk = 0; kk < kRK / 16; ++kk)
+        tc_mma(tmem, kmajor_desc(sa, kk), mnmajor_desc(sa + kRABytes, kk, kRBoxBytes), kIdesc,
+               (kb > kb0 || kk > 0) ? 1u : 0u);
+      tc_commit(smem_u32(&ctrl->empty[stage]));
+      if (++stage == kRStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
     }
+    if (ok) tc_commit(smem_u32(&ctrl->acc_full));
     // every MMA issued so far completes before this arrives
     tc_commit(smem_u32(&ctrl->drain));
     const unsigned long long t0 = global_ns();
@@ -197,80 +205,81 @@ __global__ void __launch_bounds__(kRThreads) router_tc_kernel(
       }
   }
   __syncwarp();
+  int acc_ok = 1;
+  if (lane == 0) acc_ok = mbar_wait(smem_u32(&ctrl->acc_full), 0u, abort_flag, kRWaitNs);
+  acc_ok = __shfl_sync(0xffffffffu, acc_ok, 0);
+  // the stage buffers (written by TMA, read by the tensor cores) are about to
+  // receive generic stores from the cluster
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 
-  // ---- drain: TMEM lane = token row of the tile; row r -> partial row r ----
-  for (int sg = 0; sg < nseg; ++sg) {
-    int ok = 1;
-    if (lane == 0) ok = mbar_wait(smem_u32(&ctrl->acc_full[sg]), 0u, abort_flag, kRWaitNs);
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (!ok) break;
-    tc_fence_after();
+  // ---- cluster barrier 1: every CTA's MMAs are done, its stage buffers free ----
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+
+  // ---- drain: TMEM row r of this CTA's partial -> receive buffer of CTA
+  //      r / tpc, slot [rank][r % tpc][0..N) ----
+  if (acc_ok) {
     const int r = warp * 32 + lane;
-    float* dst = const_cast<float*>(ra.partial) +
-                 ((static_cast<size_t>(seg_tile[sg]) * ra.max_slots + seg_slot[sg]) * kRM + r) * N;
-    const uint32_t taddr =
-        tmem + (static_cast<uint32_t>(warp * 32) << 16) + static_cast<uint32_t>(sg) * kCols;
+    const uint32_t owner = static_cast<uint32_t>(r / tpc);
+    const uint32_t dst_local = base + static_cast<uint32_t>(((rank * tpc) + (r % tpc)) * N * 4);
+    const uint32_t dst = map_to_rank(dst_local, owner);
+    const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     for (int c = 0; c < N; c += 16) {
       uint32_t v[16];
       tc_ld16(taddr + c, v);
       tc_wait_ld();
-      if (c + 16 <= N) {  // N % 8 == 0, so dst + c is 16-byte aligned
-#pragma unroll
-        for (int i = 0; i < 16; i += 4)
-          *reinterpret_cast<float4*>(dst + c + i) =
-              make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
-                          __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
-      } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          if (c + i < N) dst[c + i] = __uint_as_float(v[i]);
-      }
+      const int nv = (N - c) >= 16 ? 4 : (N - c) / 4;  // N % 8 == 0
+      for (int i = 0; i < nv; ++i)
+        st_cluster_v4(dst + (c + 4 * i) * 4, __uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                      __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
     }
   }
-
   tc_fence_before();
-  __syncthreads();
+  // ---- cluster barrier 2: every partial has arrived ----
+  cluster_sync();
   tc_fence_after();
   if (threadIdx.x == 0 && *abort_flag) record_status(status, kErrDeviceTimeout);
   if (warp == 1) {
     __syncwarp();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kAlloc)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols)
                  : "memory");
   }
 
-  // ---- arrival: the last CTA of each tile routes its tokens ----
-  // Every CTA arrives (even after an expired wait), so each counter is back at
-  // zero at the end of every launch.
-  __shared__ int s_last[2];
-  __threadfence();  // this CTA's segments are visible before it arrives
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    for (int sg = 0; sg < nseg; ++sg) {
-      const int m = seg_tile[sg];
-      const uint32_t need = static_cast<uint32_t>(router_tile_segments(m, num_kb, G, W));
-      const uint32_t old = atomicAdd(&tile_counters[m], 1u);
-      s_last[sg] = old == need - 1;
-      if (s_last[sg]) tile_counters[m] = 0u;
+  // ---- routing of this CTA's tokens: rank*tpc + i, i < tpc, one W-lane
+  //      segment per token ----
+  const float* recv = reinterpret_cast<const float*>(smem);
+  const int ls = lane % W;
+  constexpr int kSegs = kRThreads / W;  // tokens per pass
+  for (int i0 = 0; i0 < tpc; i0 += kSegs) {
+    const int i = i0 + (static_cast<int>(threadIdx.x) / W);
+    const int t = tile * kRM + static_cast<int>(rank) * tpc + i;
+    const bool valid = i < tpc && t < T;
+    float l[PER];
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int e = ls + W * j;
+      float v = 0.f;
+      if (valid && e < N) {
+        v = recv[(0 * tpc + i) * N + e];
+        for (int src = 1; src < cl; ++src) v = __fadd_rn(v, recv[(src * tpc + i) * N + e]);
+        if (ra.bias) v = __fadd_rn(v, ra.bias[e]);
+        if (ra.logits_out) ra.logits_out[static_cast<size_t>(t) * N + e] = v;
+      }
+      l[j] = v;
     }
+    route_token_seg<W, PER>(ra, t, valid, l, ra.colsum ? s_cs : nullptr);
   }
-  __syncthreads();
-  for (int sg = 0; sg < nseg; ++sg) {
-    if (s_last[sg]) {
-      __threadfence();
-      // the stage buffers (last written by TMA, read by the tensor cores) are
-      // reused as generic shared memory
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      route_tile(ra, seg_tile[sg], reinterpret_cast<float*>(smem));
-      __syncthreads();
-    }
+  if (ra.colsum) {
+    __syncthreads();
+    for (int e = threadIdx.x; e < N; e += blockDim.x)
+      ra.colsum[static_cast<size_t>(blockIdx.x) * N + e] = s_cs[e];
   }
-  (void)T;
 }
 
-template <int NB>
-cudaError_t launch_nb(const CUtensorMap& mX, const CUtensorMap& mW, int ctas,
-                      const RouteArgs& ra, uint32_t* tile_counters, int32_t* status,
-                      cudaStream_t s) {
+template <int NB, int W, int PER>
+cudaError_t launch_router(const CUtensorMap& mX, const CUtensorMap& mW, const RouterPlan& plan,
+                          int num_kb, const RouteArgs& ra, int32_t* status, cudaStream_t s) {
   constexpr int smem = router_smem_bytes<NB>();
   static bool attr_set[64] = {};  // per device; setting it twice is harmless
   int dev = 0;
@@ -278,13 +287,26 @@ cudaError_t launch_nb(const CUtensorMap& mX, const CUtensorMap& mW, int ctas,
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    err = cudaFuncSetAttribute(router_tc_kernel<NB>,
+    err = cudaFuncSetAttribute(router_tc_kernel<NB, W, PER>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
     attr_set[dev] = true;
   }
-  return launch_pdl(router_tc_kernel<NB>, ctas, kRThreads, smem, s, mX, mW, ra, tile_counters,
-                    status);
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = static_cast<unsigned>(plan.cluster);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(plan.m_tiles * plan.cluster));
+  cfg.blockDim = dim3(kRThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, router_tc_kernel<NB, W, PER>, mX, mW, ra, num_kb, status);
 }
 
 }  // namespace
@@ -293,44 +315,37 @@ bool router_tc_supported(int dtype, int d, int N) {
   return dtype == 1 && d % 64 == 0 && N % 8 == 0 && N <= 256;
 }
 
-RouterSplit router_split_plan(int T, int d, int N) {
-  RouterSplit p;
-  const int m_tiles = (T + kRM - 1) / kRM;
-  p.num_kb = d / kRK;
-  p.total = static_cast<long long>(m_tiles) * p.num_kb;
-  const int nb = (N + 63) / 64;
-  const int per_sm = nb == 1 ? 2 : 1;  // CTAs whose shared memory fits on one SM
-  long long g = static_cast<long long>(device_sm_count()) * per_sm;
-  if (g < m_tiles) g = m_tiles;  // keeps every range within num_kb k-blocks (<= 2 tiles)
-  if (g > p.total) g = p.total;
-  if (g < 1) g = 1;
-  p.ctas = static_cast<int>(g);
-  p.max_slots = 1;
-  for (int m = 0; m < m_tiles; ++m) {
-    const int n = router_tile_segments(m, p.num_kb, p.ctas, p.total);
-    if (n > p.max_slots) p.max_slots = n;
-  }
+RouterPlan router_plan(int T, int d, int N) {
+  RouterPlan p;
+  p.m_tiles = (T + kRM - 1) / kRM;
+  const int num_kb = d / kRK;
+  const int per_sm = N <= 64 ? 2 : 1;  // CTAs whose shared memory fits on one SM
+  const int slots = device_sm_count() * per_sm;
+  int c = kMaxCluster;
+  while (c > 1 && (num_kb % c != 0 || p.m_tiles * c > slots)) c >>= 1;
+  p.cluster = c;
+  p.colsum_rows = p.m_tiles * c;
   return p;
 }
 
-cudaError_t launch_router_tc(const void* x, const void* W_r, int d, const RouterSplit& plan,
-                             const RouteArgs& ra, uint32_t* tile_counters, int32_t* status,
-                             cudaStream_t s) {
+cudaError_t launch_router_tc(const void* x, const void* W_r, int d, const RouterPlan& plan,
+                             const RouteArgs& ra, int32_t* status, cudaStream_t s) {
   const int T = ra.T, N = ra.N;
   if (T == 0) return cudaSuccess;
-  if ((T + kRM - 1) / kRM > kMaxRouterTiles) return cudaErrorInvalidValue;
-  if (ra.seg_ctas != plan.ctas || ra.seg_kb != plan.num_kb || ra.seg_total != plan.total ||
-      ra.max_slots != plan.max_slots)
+  if (plan.cluster < 1 || plan.cluster > kMaxCluster || (d / kRK) % plan.cluster != 0)
     return cudaErrorInvalidValue;
   CUtensorMap mX, mW;
   if (!make_tmap_2d_bf16(&mX, x, static_cast<uint64_t>(T), static_cast<uint64_t>(d), 64, kRM))
     return cudaErrorInvalidValue;
   if (!make_tmap_2d_bf16(&mW, W_r, static_cast<uint64_t>(d), static_cast<uint64_t>(N), 64, kRK))
     return cudaErrorInvalidValue;
-  const int g = plan.ctas;
-  if (N <= 64) return launch_nb<1>(mX, mW, g, ra, tile_counters, status, s);
-  if (N <= 128) return launch_nb<2>(mX, mW, g, ra, tile_counters, status, s);
-  if (N <= 256) return launch_nb<4>(mX, mW, g, ra, tile_counters, status, s);
+  const int nkb = d / kRK;
+  if (N <= 8) return launch_router<1, 8, 1>(mX, mW, plan, nkb, ra, status, s);
+  if (N <= 16) return launch_router<1, 16, 1>(mX, mW, plan, nkb, ra, status, s);
+  if (N <= 32) return launch_router<1, 32, 1>(mX, mW, plan, nkb, ra, status, s);
+  if (N <= 64) return launch_router<1, 32, 2>(mX, mW, plan, nkb, ra, status, s);
+  if (N <= 128) return launch_router<2, 32, 4>(mX, mW, plan, nkb, ra, status, s);
+  if (N <= 256) return launch_router<4, 32, 8>(mX, mW, plan, nkb, ra, status, s);
   return cudaErrorInvalidValue;
 }
 

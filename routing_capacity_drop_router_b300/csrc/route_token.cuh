@@ -1,24 +1,27 @@
-// Per-token routing from fp32 logits for one 128-token tile: used by the
-// stand-alone routing kernel and by the tail of the tensor-core router.
+// Per-token routing from fp32 logits by a segment of W lanes of a warp
+// (W = 8, 16 or 32: the smallest that holds N experts, or 32 with several
+// experts per lane); used by the routing kernel (route.cu) and by the
+// tensor-core router's cluster tail (route_tc.cu).
 //
 // "Understanding Mixture of Experts", section "Expert and Router": the router
 // activates the TopK(G(x), k) experts of each token with G(x) = softmax of the
 // logits. "Capacity-Aware Inference: Mitigating the Straggler Effect in MoE",
 // section 2 (2) Expanded Drop: m extra candidates from the token's own device.
 //
-//   logits: L = the tile's slices added in slot order (+ bias), staged in
-//           shared memory with coalesced loads;
+// Lane l of the segment holds experts e = l, l + W, ... (PER of them).
 //   scores: m = max L; u_e = score_exp(L_e - m); Z = u_0 + u_1 + ... (in
-//           order); p_e = u_e / Z (correctly rounded); one thread per token;
-//   top-k:  k passes, each taking the largest (key, -e) pair below the
-//           previous pass's pair in the order key descending, expert
+//           ascending e: a chain of adds through the lanes); p_e = u_e / Z
+//           (correctly rounded);
+//   top-k:  k passes, each a segment-wide maximum of (key, -e) over the pairs
+//           below the previous pass's pair in the order key descending, expert
 //           ascending (ties to the lower expert);
-//   expanded: m more passes restricted to the home group's experts;
+//   expanded: m more passes over the home group's experts, below the k-th
+//           top-k pair (so the top-k experts are excluded);
 //   gates:  p of the slot; with renorm divided by the slots' left-to-right sum.
 //   column sums (load statistics): p_e in fixed point (units of 2^-40,
-//           rounded half up, by integer operations on the fp32 bits) summed
-//           per tile in u64, so the sum is exact and independent of the order
-//           of the additions.
+//           rounded half up, by integer operations on the fp32 bits) added in
+//           u64, so the sum is exact and independent of the order of the
+//           additions.
 #pragma once
 #include <cstdint>
 
@@ -40,215 +43,144 @@ __device__ __forceinline__ unsigned long long fixed40(float p) {
   return (m + (1ull << (-sh - 1))) >> (-sh);
 }
 
-// Per-token routing of token t from its logits s_row[0..N) (shared memory),
-// in compact loops over the experts (the code runs once per tile, so its size
-// matters more than unrolling). Writes the token's candidates and gates and
-// returns its softmax max and denominator in *mx_out, *z_out; the scores are
-// recomputed from them later, bit-identically.
-//
-// The j-th candidate is the largest (key, -e) pair below the (j-1)-th one in
-// the order "key descending, then expert ascending", so no expert needs to be
-// marked as taken; the expanded candidates are the largest pairs of the home
-// group below the k-th top-k pair.
-__device__ __forceinline__ void route_one_token(const RouteArgs& a, int t, const float* s_row,
-                                                float* mx_out, float* z_out) {
+// (key, e) packed so that a larger value is earlier in the order key
+// descending, expert ascending.
+__device__ __forceinline__ unsigned long long pair_of(uint32_t key, int e) {
+  return (static_cast<unsigned long long>(key) << 32) | static_cast<uint32_t>(0xffffffffu - e);
+}
+
+template <int W>
+__device__ __forceinline__ unsigned long long seg_max_u64(unsigned long long v) {
+#pragma unroll
+  for (int o = W / 2; o > 0; o >>= 1) {
+    const unsigned long long w = __shfl_xor_sync(0xffffffffu, v, o, W);
+    v = w > v ? w : v;
+  }
+  return v;
+}
+
+// Segment width and experts per lane for N experts.
+__host__ __device__ constexpr int route_seg_width(int N) { return N <= 8 ? 8 : (N <= 16 ? 16 : 32); }
+
+// Routes token t (valid: t < T; an invalid segment still takes part in the
+// shuffles) whose logits the segment holds in l[0..PER) (lane l: experts
+// l + W*j; entries past N are ignored). Writes scores, expert-choice gates or
+// candidates and gates; adds the token's p into s_cs (shared, nullable).
+template <int W, int PER>
+__device__ __forceinline__ void route_token_seg(const RouteArgs& a, int t, bool valid, float (&l)[PER],
+                                                unsigned long long* s_cs) {
+  const int ls = static_cast<int>(threadIdx.x & 31) % W;  // lane in the segment
   const int N = a.N;
-  float mx = s_row[0];
-  for (int e = 1; e < N; ++e) mx = fmaxf(mx, s_row[e]);
-  float Z = score_exp(__fsub_rn(s_row[0], mx));
-  for (int e = 1; e < N; ++e) Z = __fadd_rn(Z, score_exp(__fsub_rn(s_row[e], mx)));
-  *mx_out = mx;
-  *z_out = Z;
+#pragma unroll
+  for (int j = 0; j < PER; ++j)
+    if (ls + W * j >= N) l[j] = -INFINITY;
+  float mx = l[0];
+#pragma unroll
+  for (int j = 1; j < PER; ++j) mx = fmaxf(mx, l[j]);
+#pragma unroll
+  for (int o = W / 2; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o, W));
+  float u[PER];
+#pragma unroll
+  for (int j = 0; j < PER; ++j) u[j] = (ls + W * j < N) ? score_exp(__fsub_rn(l[j], mx)) : 0.f;
+  float Z = 0.f;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int n_here = min(W, N - W * j);
+    for (int i = 0; i < n_here; ++i) {
+      const float v = __shfl_sync(0xffffffffu, u[j], i, W);
+      Z = (j == 0 && i == 0) ? v : __fadd_rn(Z, v);
+    }
+  }
+  float p[PER];
+#pragma unroll
+  for (int j = 0; j < PER; ++j) p[j] = __fdiv_rn(u[j], Z);
+  if (valid) {
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int e = ls + W * j;
+      if (e < N) {
+        if (a.scores) a.scores[static_cast<size_t>(t) * N + e] = p[j];
+        if (a.ec) a.cand_gate[static_cast<size_t>(t) * N + e] = p[j];
+        if (s_cs) atomicAdd(&s_cs[e], fixed40(p[j]));
+      }
+    }
+  }
   if (a.ec) return;
 
+  // candidates: passes of a segment maximum below the previous pair
+  constexpr int kSlots = 32 / W;  // slots each lane keeps (kc <= 32)
+  uint32_t key[PER];
+#pragma unroll
+  for (int j = 0; j < PER; ++j) key[j] = order_key(l[j]);
   const int k = a.k, kc = a.k + a.m;
-  int32_t* idx_out = a.cand_idx + static_cast<size_t>(t) * kc;
-  float* gate_out = a.cand_gate + static_cast<size_t>(t) * kc;
-  float g[32];
-  uint32_t prev_key = 0xffffffffu;  // pair bound: (prev_key, prev_e); start above all
-  int prev_e = -1;
-  uint32_t kth_key = 0u;
-  int kth_e = -1;
+  unsigned long long bound = ~0ull, kth = 0ull;
   int lo = 0, hi = N;
-  for (int j = 0; j < kc; ++j) {
-    if (j == k) {  // expanded candidates: the home group, below the k-th pair
+  int my_idx[kSlots];
+  float my_gate[kSlots];
+#pragma unroll
+  for (int q = 0; q < kSlots; ++q) {
+    my_idx[q] = -1;
+    my_gate[q] = 0.f;
+  }
+  for (int jj = 0; jj < kc; ++jj) {
+    if (jj == k) {  // expanded candidates: the home group, below the k-th pair
       const int G = N / a.group_size;
-      const int hg = a.home_group ? a.home_group[t]
-                                  : static_cast<int>((static_cast<long long>(t) * G) / a.T);
+      const int tt = valid ? t : 0;
+      const int hg = a.home_group ? a.home_group[tt]
+                                  : static_cast<int>((static_cast<long long>(tt) * G) / a.T);
       lo = hg * a.group_size;
       hi = lo + a.group_size;
-      prev_key = kth_key;
-      prev_e = kth_e;
+      bound = kth;
     }
-    int best = -1;
-    uint32_t bk = 0u;
-    for (int e = lo; e < hi; ++e) {
-      const uint32_t ke = order_key(s_row[e]);
-      // below the bound in (key desc, e asc) order, and above the best so far
-      const bool below = ke < prev_key || (ke == prev_key && e > prev_e);
-      if (below && (best < 0 || ke > bk)) {
-        bk = ke;
-        best = e;
+    unsigned long long best = 0ull;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int e = ls + W * j;
+      if (e >= lo && e < hi && e < N) {
+        const unsigned long long pr = pair_of(key[j], e);
+        if (pr < bound && pr > best) best = pr;
       }
     }
-    idx_out[j] = best;
-    g[j] = best >= 0 ? __fdiv_rn(score_exp(__fsub_rn(s_row[best], mx)), Z) : 0.f;
-    if (best >= 0) {
-      prev_key = bk;
-      prev_e = best;
-    }
-    if (j == k - 1) {
-      kth_key = prev_key;
-      kth_e = prev_e;
-    }
-  }
-  if (a.renorm) {
-    float S = g[0];
-    for (int j = 1; j < kc; ++j) S = __fadd_rn(S, g[j]);
-    for (int j = 0; j < kc; ++j) g[j] = __fdiv_rn(g[j], S);
-  }
-  for (int j = 0; j < kc; ++j) gate_out[j] = g[j];
-}
-
-// Shared memory route_tile needs: the tile's [128, N + 1] fp32 staging array,
-// N u64 column sums (8-byte aligned: 128 * (N + 1) * 4 is a multiple of 8),
-// then each token's softmax max and denominator.
-__host__ __device__ constexpr size_t route_tile_smem(int N) {
-  return static_cast<size_t>(kRouteTile) * (N + 1) * sizeof(float) +
-         static_cast<size_t>(N) * sizeof(unsigned long long) +
-         2 * static_cast<size_t>(kRouteTile) * sizeof(float);
-}
-
-// Calls f(r, e, q) for every element of a [rows, N] tile (q = r * N + e), with
-// consecutive threads on consecutive elements of a row.
-template <typename F>
-__device__ __forceinline__ void for_tile_elements(int rows, int N, F&& f) {
-  const int nt = static_cast<int>(blockDim.x), tid = static_cast<int>(threadIdx.x);
-  if (N <= nt) {
-    const int rpi = nt / N, e = tid % N, r0 = tid / N;
-    if (r0 < rpi)
-      for (int r = r0; r < rows; r += rpi) f(r, e, r * N + e);
-  } else {
-    for (int r = 0; r < rows; ++r)
-      for (int e = tid; e < N; e += nt) f(r, e, r * N + e);
-  }
-}
-
-// Routes tokens [tile*128, tile*128 + 128) (blockDim.x == kRouteTile, one
-// token per thread) from the tile's logit slices, writes logits_out, scores,
-// candidates and gates, and (a.colsum) the tile's column sums of p.
-// s_l: route_tile_smem(N) bytes of shared memory. Call uniformly from every
-// thread of the block.
-__device__ __forceinline__ void route_tile(const RouteArgs& a, int tile, float* s_l) {
-  const int N = a.N, ld = N + 1;
-  const int t0 = tile * kRouteTile;
-  const int rows = min(kRouteTile, a.T - t0);
-  const int nslots =
-      a.seg_ctas ? router_tile_segments(tile, a.seg_kb, a.seg_ctas, a.seg_total) : 1;
-  const float* base = a.partial + static_cast<size_t>(tile) * a.max_slots * kRouteTile * N;
-  const size_t slot_stride = static_cast<size_t>(kRouteTile) * N;
-  // 1. the tile's logits: slices added in slot order, then the bias. With
-  //    N % 4 == 0 each thread sums 4-element vectors, 4 vectors x 4 slices of
-  //    loads in flight per round (the slices were just written by other CTAs
-  //    and are read through L2).
-  if ((N & 3) == 0) {
-    constexpr int kU = 4, kS = 4;
-    const int nvec = rows * N / 4;
-    const float4* b4 = reinterpret_cast<const float4*>(base);
-    const size_t stride4 = slot_stride / 4;
-    for (int v0 = threadIdx.x; v0 < nvec; v0 += blockDim.x * kU) {
-      float4 acc[kU];
-      for (int s0 = 0; s0 < nslots; s0 += kS) {
-        float4 t[kS][kU];
+    best = seg_max_u64<W>(best);
+    const int e_best = best ? static_cast<int>(0xffffffffu - static_cast<uint32_t>(best)) : -1;
+    float pv = 0.f;
+    const int jo = e_best >= 0 ? e_best / W : 0;
 #pragma unroll
-        for (int ss = 0; ss < kS; ++ss)
+    for (int j = 0; j < PER; ++j)
+      if (j == jo) pv = p[j];
+    const float g = __shfl_sync(0xffffffffu, pv, e_best >= 0 ? e_best % W : 0, W);
+    if (e_best >= 0) bound = best;
 #pragma unroll
-          for (int u = 0; u < kU; ++u) {
-            const int v = v0 + u * static_cast<int>(blockDim.x);
-            if (s0 + ss < nslots && v < nvec) t[ss][u] = __ldcg(b4 + (s0 + ss) * stride4 + v);
-          }
-#pragma unroll
-        for (int ss = 0; ss < kS; ++ss)
-#pragma unroll
-          for (int u = 0; u < kU; ++u) {
-            const int v = v0 + u * static_cast<int>(blockDim.x);
-            if (s0 + ss < nslots && v < nvec) {
-              if (s0 + ss == 0) {
-                acc[u] = t[ss][u];
-              } else {
-                acc[u].x = __fadd_rn(acc[u].x, t[ss][u].x);
-                acc[u].y = __fadd_rn(acc[u].y, t[ss][u].y);
-                acc[u].z = __fadd_rn(acc[u].z, t[ss][u].z);
-                acc[u].w = __fadd_rn(acc[u].w, t[ss][u].w);
-              }
-            }
-          }
+    for (int q = 0; q < kSlots; ++q)
+      if (jj == ls + W * q) {
+        my_idx[q] = e_best;
+        my_gate[q] = e_best >= 0 ? g : 0.f;
       }
+    if (jj == k - 1) kth = bound;
+  }
+  if (a.renorm) {  // left-to-right sum of the slot gates
+    float S = 0.f;
 #pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int v = v0 + u * static_cast<int>(blockDim.x);
-        if (v < nvec) {
-          const int q = 4 * v, r = q / N, e = q - r * N;  // 4 elements of one row
-          float4 o = acc[u];
-          if (a.bias) {
-            o.x = __fadd_rn(o.x, a.bias[e]);
-            o.y = __fadd_rn(o.y, a.bias[e + 1]);
-            o.z = __fadd_rn(o.z, a.bias[e + 2]);
-            o.w = __fadd_rn(o.w, a.bias[e + 3]);
-          }
-          if (a.logits_out)
-            *reinterpret_cast<float4*>(a.logits_out + static_cast<size_t>(t0) * N + q) = o;
-          float* dst = s_l + r * ld + e;
-          dst[0] = o.x;
-          dst[1] = o.y;
-          dst[2] = o.z;
-          dst[3] = o.w;
+    for (int q = 0; q < kSlots; ++q)
+      for (int i = 0; i < W; ++i) {
+        const int jj = q * W + i;
+        if (jj < kc) {
+          const float v = __shfl_sync(0xffffffffu, my_gate[q], i, W);
+          S = (jj == 0) ? v : __fadd_rn(S, v);
         }
       }
-    }
-  } else {
-    for_tile_elements(rows, N, [&](int r, int e, int q) {
-      float v = __ldcg(base + q);
-      for (int s = 1; s < nslots; ++s) v = __fadd_rn(v, __ldcg(base + s * slot_stride + q));
-      if (a.bias) v = __fadd_rn(v, a.bias[e]);
-      if (a.logits_out) a.logits_out[static_cast<size_t>(t0) * N + q] = v;
-      s_l[r * ld + e] = v;
-    });
+#pragma unroll
+    for (int q = 0; q < kSlots; ++q) my_gate[q] = __fdiv_rn(my_gate[q], S);
   }
-  __syncthreads();
-  // 2. one token per thread
-  unsigned long long* s_cs = reinterpret_cast<unsigned long long*>(s_l + kRouteTile * ld);
-  float* s_mx = reinterpret_cast<float*>(s_cs + N);
-  float* s_z = s_mx + kRouteTile;
-  if (static_cast<int>(threadIdx.x) < rows)
-    route_one_token(a, t0 + threadIdx.x, s_l + threadIdx.x * ld, s_mx + threadIdx.x,
-                    s_z + threadIdx.x);
-  for (int e = threadIdx.x; e < N; e += blockDim.x) s_cs[e] = 0ull;
-  __syncthreads();
-  // 3. scores p = score_exp(L - max) / Z, recomputed element-wise with
-  //    coalesced stores (scores, expert-choice gates) and kept in s_l for the
-  //    column sums
-  for_tile_elements(rows, N, [&](int r, int e, int q) {
-    const float p = __fdiv_rn(score_exp(__fsub_rn(s_l[r * ld + e], s_mx[r])), s_z[r]);
-    if (a.scores) a.scores[static_cast<size_t>(t0) * N + q] = p;
-    if (a.ec) a.cand_gate[static_cast<size_t>(t0) * N + q] = p;
-    s_l[r * ld + e] = p;
-  });
-  if (a.colsum) {
-    // thread (e, c) sums rows c, c + chunks, ...; the u64 partials meet in
-    // shared memory (integer sums: the order does not matter)
-    __syncthreads();
-    const int chunks = N <= static_cast<int>(blockDim.x) ? static_cast<int>(blockDim.x) / N : 1;
-    for (int e = static_cast<int>(threadIdx.x) % N; e < N; e += static_cast<int>(blockDim.x)) {
-      const int c = static_cast<int>(threadIdx.x) / N;
-      if (c >= chunks) break;
-      unsigned long long acc = 0ull;
-      for (int r = c; r < rows; r += chunks) acc += fixed40(s_l[r * ld + e]);
-      atomicAdd(&s_cs[e], acc);
+  if (valid) {
+#pragma unroll
+    for (int q = 0; q < kSlots; ++q) {
+      const int jj = ls + W * q;
+      if (jj < kc) {
+        a.cand_idx[static_cast<size_t>(t) * kc + jj] = my_idx[q];
+        a.cand_gate[static_cast<size_t>(t) * kc + jj] = my_gate[q];
+      }
     }
-    __syncthreads();
-    for (int e = threadIdx.x; e < N; e += blockDim.x)
-      a.colsum[static_cast<size_t>(tile) * N + e] = s_cs[e];
   }
 }
 

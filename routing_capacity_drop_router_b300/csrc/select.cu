@@ -75,10 +75,21 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
   int n = 0;
   if (expert_choice) {
     n = T;
-    for (int i = threadIdx.x; i < T; i += blockDim.x) {
-      const int flat = i * N + e;
-      lflat[i] = flat;
-      lkey[i] = order_key(cand_gate[flat]);
+    for (int i0 = threadIdx.x; i0 < T; i0 += blockDim.x * kSelRounds) {
+      float gv[kSelRounds];  // all loads in flight before the stores
+#pragma unroll
+      for (int j = 0; j < kSelRounds; ++j) {
+        const int i = i0 + j * static_cast<int>(blockDim.x);
+        gv[j] = i < T ? cand_gate[static_cast<size_t>(i) * N + e] : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < kSelRounds; ++j) {
+        const int i = i0 + j * static_cast<int>(blockDim.x);
+        if (i < T) {
+          lflat[i] = i * N + e;
+          lkey[i] = order_key(gv[j]);
+        }
+      }
     }
   } else {
     // pass: warp w takes entries [base + 256 w, base + 256 w + 256) in 32-entry
@@ -89,11 +100,17 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
     for (int base = 0; base < total; base += kSelPass) {
       const int w0 = base + (static_cast<int>(threadIdx.x) >> 5) * (32 * kSelRounds) + lane;
       int ce[kSelRounds];
+      float gv[kSelRounds];  // gates loaded with the experts: every load in flight at once
       int cnt = 0;
 #pragma unroll
       for (int j = 0; j < kSelRounds; ++j) {
         const int i = w0 + 32 * j;
         ce[j] = (i < total) ? cand_idx[i] : N;  // N: no expert, and not an empty slot
+        gv[j] = (i < total) ? cand_gate[i] : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < kSelRounds; ++j) {
+        const int i = w0 + 32 * j;
         cnt += __popc(__ballot_sync(0xffffffffu, ce[j] == e));
         if (e == 0 && i < total && (ce[j] < 0 || ce[j] >= N)) {  // empty slots: block 0
           slot[i] = -1;
@@ -110,7 +127,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
           const int p = pos + __popc(b & lt);
           if (p < T) {
             lflat[p] = i;
-            lkey[p] = order_key(cand_gate[i]);
+            lkey[p] = order_key(gv[j]);
           } else {  // only if a token lists the same expert twice: not selectable
             slot[i] = -1;
             if (keep) keep[i] = 0;
@@ -257,7 +274,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
     __syncthreads();
     if (s_last) {
       __threadfence();
-      stats_final_block(demand, kept, st.colsum, T, N, st.stats);
+      stats_final_block(demand, kept, st.colsum, st.rows, T, N, st.stats);
     }
   }
 }

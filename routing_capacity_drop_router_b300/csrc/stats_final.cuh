@@ -1,5 +1,5 @@
 // Final step of the load statistics (see stats.cu), run by one block of at
-// least 32 threads; reads demand/kept through L2, since in the selection
+// least 256 threads; reads demand/kept through L2, since in the selection
 // kernel's tail they were written by other blocks of the same launch.
 // Everything up to the last few divisions is integer arithmetic: this part's
 // fp64 pipe is narrow, and one thread does the handful of fp64 operations.
@@ -15,18 +15,36 @@ __device__ __forceinline__ double u128_to_double(unsigned long long hi, unsigned
 }
 
 __device__ __forceinline__ void stats_final_block(const int32_t* demand, const int32_t* kept,
-                                                  const unsigned long long* colsum, int T, int N,
-                                                  double* stats) {
-  // per expert: exact column sum (u64) and demand_i * colsum_i as 128 bits
-  __shared__ unsigned long long s_hi[256], s_lo[256];
+                                                  const unsigned long long* colsum, int rows,
+                                                  int T, int N, double* stats) {
+  // per expert: exact column sum (u64: thread (e, c) adds rows c, c + chunks,
+  // ...; integer sums, so the order does not matter) and demand_i * colsum_i
+  // as 128 bits
+  __shared__ unsigned long long s_sum[256], s_hi[256], s_lo[256];
   __shared__ long long s_P[256], s_D[256], s_mx[256];
-  const int tiles = (T + kRouteTile - 1) / kRouteTile;
+  for (int e = threadIdx.x; e < 256; e += blockDim.x) s_sum[e] = 0ull;
+  __syncthreads();
+  const int chunks = static_cast<int>(blockDim.x) / N;  // >= 1: N <= 256 <= blockDim.x
+  if (static_cast<int>(threadIdx.x) < chunks * N) {
+    const int e = static_cast<int>(threadIdx.x) % N, c = static_cast<int>(threadIdx.x) / N;
+    unsigned long long acc = 0ull;
+    int b = c;
+    for (; b + 3 * chunks < rows; b += 4 * chunks) {  // four loads in flight
+      const unsigned long long v0 = __ldcg(colsum + static_cast<size_t>(b) * N + e);
+      const unsigned long long v1 = __ldcg(colsum + static_cast<size_t>(b + chunks) * N + e);
+      const unsigned long long v2 = __ldcg(colsum + static_cast<size_t>(b + 2 * chunks) * N + e);
+      const unsigned long long v3 = __ldcg(colsum + static_cast<size_t>(b + 3 * chunks) * N + e);
+      acc += v0 + v1 + v2 + v3;
+    }
+    for (; b < rows; b += chunks) acc += __ldcg(colsum + static_cast<size_t>(b) * N + e);
+    atomicAdd(&s_sum[e], acc);
+  }
+  __syncthreads();
   for (int e = threadIdx.x; e < 256; e += blockDim.x) {
     unsigned long long hi = 0ull, lo = 0ull;
     long long kp = 0, dm = 0;
     if (e < N) {
-      unsigned long long acc = 0ull;  // the order of the tiles does not matter
-      for (int b = 0; b < tiles; ++b) acc += __ldcg(colsum + static_cast<size_t>(b) * N + e);
+      const unsigned long long acc = s_sum[e];
       kp = __ldcg(kept + e);
       dm = __ldcg(demand + e);
       const unsigned long long d = static_cast<unsigned long long>(dm);
