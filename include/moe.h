@@ -277,6 +277,20 @@ int moe_grouped_gemm(int32_t dtype, const void* A, const int32_t* offsets, int32
                      void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Failure-detection self-test (the pages have no counterpart): enqueues the
+ * bf16 grouped GEMM of moe_grouped_gemm (same arguments, n_segments >= 1,
+ * rows_max >= 1) with one CTA announcing but never loading one k-block of its
+ * first tile, so the tensor-core issuer's bounded wait (1 s) expires. The
+ * kernel then leaves every loop, drains its copies and MMAs, frees its tensor
+ * memory and records MOE_ERR_DEVICE_TIMEOUT in ws's status word, where
+ * moe_get_device_status reads it; `out` is left partly written. The GPU
+ * context stays usable (clear the status with moe_clear_device_status).
+ */
+int moe_selftest_expired_wait(const void* A, const int32_t* offsets, int32_t n_segments,
+                              int64_t rows_max, int32_t K, int32_t n_out, const void* B,
+                              void* out, void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Gate-weighted combine, the sum of the layer equation ("Understanding
  * Mixture of Experts", y = sum_i G(x)_i E_i(x)):
  *   y[t] = sum over r in tok_rows[t] (ascending) of row_gate[r] * op[r]

@@ -89,6 +89,9 @@ SIGNATURES = {
     "moe_grouped_gemm": (ctypes.c_int, [ctypes.c_int32, _VP, _VP, ctypes.c_int32, ctypes.c_int64,
                                         ctypes.c_int32, ctypes.c_int32, _VP, _VP, _VP,
                                         ctypes.c_size_t, _VP]),
+    "moe_selftest_expired_wait": (ctypes.c_int, [_VP, _VP, ctypes.c_int32, ctypes.c_int64,
+                                                 ctypes.c_int32, ctypes.c_int32, _VP, _VP, _VP,
+                                                 ctypes.c_size_t, _VP]),
     "moe_combine": (ctypes.c_int, [_CFG, _VP, _VP, _VP, _VP, _VP, _VP]),
     "moe_load_stats": (ctypes.c_int, [_CFG, _VP, _VP, _VP, _VP, _VP, ctypes.c_size_t, _VP]),
     "moe_layer_forward": (ctypes.c_int, [_CFG, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
@@ -232,6 +235,17 @@ def moe_grouped_gemm(dtype, A, offsets, n_segments, rows_max, K, n_out, B, out, 
                                   rows_max, K, n_out, _p(B), _p(out), _p(ws),
                                   ws.numel() * ws.element_size(), _stream(stream)),
            "moe_grouped_gemm")
+
+
+def moe_selftest_expired_wait(A, offsets, n_segments, rows_max, K, n_out, B, out, ws,
+                              stream=None) -> None:
+    """Enqueue the bf16 grouped GEMM with one withheld k-block, so that its
+    bounded wait expires and MOE_ERR_DEVICE_TIMEOUT lands in ws's status word
+    (failure-detection self-test)."""
+    _check(lib().moe_selftest_expired_wait(_p(A), _p(offsets), n_segments, rows_max, K, n_out,
+                                           _p(B), _p(out), _p(ws),
+                                           ws.numel() * ws.element_size(), _stream(stream)),
+           "moe_selftest_expired_wait")
 
 
 def moe_combine(cfg, op, row_gate, tok_rows, shared_out, y, stream=None) -> None:

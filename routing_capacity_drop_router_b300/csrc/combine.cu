@@ -3,8 +3,8 @@
 // MoE differs from the Transformer").
 //
 // One warp per token; the token's rows (ascending expert) and gates are staged
-// in shared memory, then each lane walks 16-byte column vectors (four per
-// pass, the loads of up to four rows issued before their FMAs): for every row
+// in shared memory, then each lane walks 16-byte column vectors (two per
+// pass, the loads of two rows issued before their FMAs): for every row
 // an FMA into fp32 accumulators in a fixed order (ascending expert, shared
 // expert last), one rounding to the output dtype at the end.
 #include <cuda_bf16.h>
@@ -19,8 +19,10 @@ namespace {
 constexpr int kCombThreads = 256;
 constexpr int kCombWarps = kCombThreads / 32;
 constexpr int kCombMaxRows = 256;
-constexpr int kU = 4;   // 16-byte column vectors per lane per pass
-constexpr int kRB = 4;  // rows loaded per batch
+constexpr int kU = 2;   // 16-byte column vectors per lane per pass
+constexpr int kRB = 2;  // rows loaded per batch (k = 2 in one batch)
+// few registers, so that 32+ warps per SM keep enough 16-byte loads in flight
+constexpr int kCombMinBlocks = 4;
 
 template <typename E> struct Pack;  // 16 bytes of E <-> fp32
 template <> struct Pack<__nv_bfloat16> {
@@ -55,7 +57,7 @@ template <> struct Pack<float> {
 };
 
 template <typename E>
-__global__ void __launch_bounds__(kCombThreads) combine_kernel(
+__global__ void __launch_bounds__(kCombThreads, kCombMinBlocks) combine_kernel(
     const E* __restrict__ op, const float* __restrict__ row_gate,
     const int32_t* __restrict__ tok_rows, const E* __restrict__ shared_out, E* __restrict__ y,
     int T, int d, int kc, int rows_max) {

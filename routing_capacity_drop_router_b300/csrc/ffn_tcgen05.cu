@@ -67,6 +67,7 @@ struct __align__(8) Ctrl {
   int total_tiles;
   int tile_base[kMaxSegments + 1];  // first tile of each segment
   int mtiles[kMaxSegments];
+  int seg_row[kMaxSegments + 1];    // offsets[], so a tile decodes from shared memory
 };
 constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + static_cast<int>(sizeof(Ctrl));
 
@@ -86,7 +87,8 @@ template <bool SWIGLU>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
     const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB1,
     const __grid_constant__ CUtensorMap tmB3, const int32_t* __restrict__ offsets, int S, int K,
-    int n_out, int rows_max, __nv_bfloat16* __restrict__ out, int32_t* __restrict__ status) {
+    int n_out, int rows_max, __nv_bfloat16* __restrict__ out, int32_t* __restrict__ status,
+    int withhold_kb) {
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -122,7 +124,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
     for (int s0 = 0; s0 < S; s0 += 32) {
       const int s = s0 + lane;
       int mt = 0;
-      if (s < S) mt = (offsets[s + 1] - offsets[s] + kBM - 1) / kBM;
+      int r0 = 0, r1 = 0;
+      if (s < S) {
+        r0 = offsets[s];
+        r1 = offsets[s + 1];
+        mt = (r1 - r0 + kBM - 1) / kBM;
+        ctrl->seg_row[s] = r0;
+        if (s == S - 1) ctrl->seg_row[S] = r1;
+      }
       int incl = mt * n_tiles;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -164,8 +173,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
     const int local = tile - ctrl->tile_base[seg];
     const int mt = ctrl->mtiles[seg];
     const int n_idx = local / mt, m_idx = local - n_idx * mt;
-    row0 = offsets[seg] + m_idx * kBM;
-    row_end = offsets[seg + 1];
+    row0 = ctrl->seg_row[seg] + m_idx * kBM;
+    row_end = ctrl->seg_row[seg + 1];
     col0 = n_idx * tile_n;
   };
 
@@ -188,6 +197,17 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
           break;
         }
         mbar_expect_tx(fb, kStageBytes);
+        if (kb == withhold_kb && tile == 0) {
+          // failure-detection self-test: announce the stage's bytes but load
+          // nothing, so the MMA issuer's bounded wait expires
+          issued[stage] = 1;
+          issued_phase[stage] = phase;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          continue;
+        }
         const uint32_t sa = stage0 + stage * kStageBytes;
         const uint32_t sb = sa + kABytes;
         tma_load_2d(sa, &tmA, kb * kBK, row0, fb);
@@ -335,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
 cudaError_t launch_grouped_gemm_tc_bf16(const void* A, const int32_t* offsets, int S,
                                         int64_t rows_max, int K, int n_out, const void* B1,
                                         const void* B3, void* out, bool swiglu,
-                                        int32_t* status, cudaStream_t s) {
+                                        int32_t* status, cudaStream_t s, int withhold_kb) {
   if (S == 0 || rows_max == 0) return cudaSuccess;
   if (S > kMaxSegments) return cudaErrorInvalidValue;
   CUtensorMap mA, mB1, mB3;
@@ -371,9 +391,11 @@ cudaError_t launch_grouped_gemm_tc_bf16(const void* A, const int32_t* offsets, i
   const int rmax = rows_max > 0x7fffffff ? 0x7fffffff : static_cast<int>(rows_max);
   if (swiglu)
     return launch_pdl(grouped_gemm_tc_kernel<true>, static_cast<unsigned>(grid), kThreads,
-                      kSmemBytes, s, mA, mB1, mB3, offsets, S, K, n_out, rmax, o, status);
+                      kSmemBytes, s, mA, mB1, mB3, offsets, S, K, n_out, rmax, o, status,
+                      withhold_kb);
   return launch_pdl(grouped_gemm_tc_kernel<false>, static_cast<unsigned>(grid), kThreads,
-                    kSmemBytes, s, mA, mB1, mB3, offsets, S, K, n_out, rmax, o, status);
+                    kSmemBytes, s, mA, mB1, mB3, offsets, S, K, n_out, rmax, o, status,
+                    withhold_kb);
 }
 
 }  // namespace moe

@@ -237,7 +237,8 @@ P* at(void* ws, size_t off) {
 }
 
 
-// FFN over expert-contiguous rows; hp is scratch of rows_max * f elements.
+// FFN over expert-contiguous rows; hp is scratch of rows_max * f elements;
+// status is the workspace's status word.
 int run_ffn(int dtype, const void* xp, const int32_t* offsets, int S, int64_t rows_max, int d,
             int f, const void* W1, const void* W3, const void* W2, void* hp, void* op,
             int32_t* status, cudaStream_t s, Tracer* tr = nullptr) {
@@ -245,7 +246,8 @@ int run_ffn(int dtype, const void* xp, const int32_t* offsets, int S, int64_t ro
   if (dtype == MOE_BF16) {
     e = launch_grouped_gemm_tc_bf16(xp, offsets, S, rows_max, d, f, W1, W3, hp, true, status, s);
     if (e != cudaSuccess || (tr && !tr->mark())) return MOE_ERR_LAUNCH;
-    e = launch_grouped_gemm_tc_bf16(hp, offsets, S, rows_max, f, d, W2, nullptr, op, false, status, s);
+    e = launch_grouped_gemm_tc_bf16(hp, offsets, S, rows_max, f, d, W2, nullptr, op, false, status,
+                                    s);
   } else {
     e = launch_grouped_gemm_simt_f32(static_cast<const float*>(xp), offsets, S, rows_max, d, f,
                                      static_cast<const float*>(W1), static_cast<const float*>(W3),
@@ -360,10 +362,9 @@ int moe_expert_ffn(const moe_config* cfg, const void* xp, const int32_t* offsets
       !aligned16(ws))
     return MOE_ERR_ALIGN;
   if (ws_bytes < moe_ffn_workspace_size(rows_max, f, cfg->dtype)) return MOE_ERR_WORKSPACE;
-  int32_t* status = static_cast<int32_t*>(ws);
   void* hp = static_cast<unsigned char*>(ws) + kCtrlBytes;
   return run_ffn(cfg->dtype, xp, offsets, n_segments, rows_max, cfg->d, f, W1, W3, W2, hp, op,
-                 status, as_stream(stream));
+                 static_cast<int32_t*>(ws), as_stream(stream));
 }
 
 int moe_grouped_gemm(int32_t dtype, const void* A, const int32_t* offsets, int32_t n_segments,
@@ -386,6 +387,20 @@ int moe_grouped_gemm(int32_t dtype, const void* A, const int32_t* offsets, int32
                                      K, n_out, static_cast<const float*>(B), nullptr,
                                      static_cast<float*>(out), false, s);
   return status_from(e);
+}
+
+int moe_selftest_expired_wait(const void* A, const int32_t* offsets, int32_t n_segments,
+                              int64_t rows_max, int32_t K, int32_t n_out, const void* B,
+                              void* out, void* ws, size_t ws_bytes, void* stream) {
+  if (K <= 0 || n_out <= 0 || n_segments <= 0 || rows_max <= 0) return MOE_ERR_SHAPE;
+  if (K % 64 || n_out % 64) return MOE_ERR_SHAPE;
+  if (n_segments > kMaxN) return MOE_ERR_UNSUPPORTED;
+  if (!A || !offsets || !B || !out || !ws) return MOE_ERR_NULL;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(out) || !aligned16(ws)) return MOE_ERR_ALIGN;
+  if (ws_bytes < moe_ffn_workspace_size(0, 0, MOE_BF16)) return MOE_ERR_WORKSPACE;
+  return status_from(launch_grouped_gemm_tc_bf16(A, offsets, n_segments, rows_max, K, n_out, B,
+                                                 nullptr, out, false, static_cast<int32_t*>(ws),
+                                                 as_stream(stream), 0));
 }
 
 int moe_combine(const moe_config* cfg, const void* op, const float* row_gate,

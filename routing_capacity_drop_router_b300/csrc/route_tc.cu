@@ -36,8 +36,9 @@ using namespace tc;
 constexpr int kRM = 128;        // tokens per tile (MMA M)
 constexpr int kRK = 64;         // k per stage
 constexpr int kRStages = 4;
-constexpr int kRThreads = 128;  // 4 warps: producer, MMA, then all four drain TMEM
-static_assert(kRM == kRouteTile && kRThreads == kRouteTile, "one drain thread per tile row");
+constexpr int kRThreads = 256;  // warps 0-3: producer, MMA, TMEM drain; all 8 route
+constexpr int kRDrainThreads = 128;  // one TMEM lane (tile row) per drain thread
+static_assert(kRM == kRouteTile && kRDrainThreads == kRM, "one drain thread per tile row");
 constexpr int kRABytes = kRM * kRK * 2;
 constexpr int kRBoxBytes = 64 * kRK * 2;
 constexpr unsigned long long kRWaitNs = 1000000000ull;
@@ -122,7 +123,7 @@ __global__ void __launch_bounds__(kRThreads) router_tc_kernel(
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
-  for (int e = threadIdx.x; e < 256; e += blockDim.x) s_cs[e] = 0ull;
+  for (int e = threadIdx.x; e < 256; e += blockDim.x) s_cs[e] = 0ull;  // blockDim >= 256
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(&ctrl->tmem_base)),
@@ -219,7 +220,7 @@ __global__ void __launch_bounds__(kRThreads) router_tc_kernel(
 
   // ---- drain: TMEM row r of this CTA's partial -> receive buffer of CTA
   //      r / tpc, slot [rank][r % tpc][0..N) ----
-  if (acc_ok) {
+  if (acc_ok && warp < kRDrainThreads / 32) {
     const int r = warp * 32 + lane;
     const uint32_t owner = static_cast<uint32_t>(r / tpc);
     const uint32_t dst_local = base + static_cast<uint32_t>(((rank * tpc) + (r % tpc)) * N * 4);

@@ -82,13 +82,14 @@ __device__ __forceinline__ void route_token_seg(const RouteArgs& a, int t, bool 
   float u[PER];
 #pragma unroll
   for (int j = 0; j < PER; ++j) u[j] = (ls + W * j < N) ? score_exp(__fsub_rn(l[j], mx)) : 0.f;
-  float Z = 0.f;
+  float Z = 0.f;  // the shuffles do not depend on Z: unrolled, they are all in flight at once
 #pragma unroll
   for (int j = 0; j < PER; ++j) {
     const int n_here = min(W, N - W * j);
-    for (int i = 0; i < n_here; ++i) {
+#pragma unroll
+    for (int i = 0; i < W; ++i) {
       const float v = __shfl_sync(0xffffffffu, u[j], i, W);
-      Z = (j == 0 && i == 0) ? v : __fadd_rn(Z, v);
+      if (i < n_here) Z = (j == 0 && i == 0) ? v : __fadd_rn(Z, v);
     }
   }
   float p[PER];
@@ -162,6 +163,7 @@ __device__ __forceinline__ void route_token_seg(const RouteArgs& a, int t, bool 
     float S = 0.f;
 #pragma unroll
     for (int q = 0; q < kSlots; ++q)
+#pragma unroll
       for (int i = 0; i < W; ++i) {
         const int jj = q * W + i;
         if (jj < kc) {

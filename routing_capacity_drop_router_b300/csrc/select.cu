@@ -264,18 +264,18 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
 
   // 4. load statistics: the last block to finish reads every expert's counts
   if (st.stats) {
-    __threadfence();
-    __syncthreads();
+    // thread 0 wrote demand/kept: it alone publishes them before arriving
     if (threadIdx.x == 0) {
+      __threadfence();
       const uint32_t old = atomicAdd(counter, 1u);
       s_last = old == gridDim.x - 1;
-      if (s_last) *counter = 0u;
+      if (s_last) {
+        *counter = 0u;
+        __threadfence();
+      }
     }
     __syncthreads();
-    if (s_last) {
-      __threadfence();
-      stats_final_block(demand, kept, st.colsum, st.rows, T, N, st.stats);
-    }
+    if (s_last) stats_final_block(demand, kept, st.colsum, st.rows, T, N, st.stats);
   }
 }
 

@@ -28,6 +28,8 @@ def _rand(shape, seed, scale=1.0, dtype=torch.bfloat16):
     ([128], 128, 256),
     ([3, 500, 64, 0, 0, 257], 512, 512),
     ([1000], 1024, 192),
+    ([19150, 50], 512, 256),      # 151 tiles: one more than a full round of CTAs
+    ([77, 300, 5], 2048, 512),    # few tiles, long K, ragged rows
 ])
 def test_grouped_gemm_bf16_against_torch(sizes, K, n_out):
     S = len(sizes)
