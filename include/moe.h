@@ -228,7 +228,12 @@ int moe_dispatch(const moe_config* cfg, const void* x, const int32_t* cand_idx,
  *   ws           >= moe_ffn_workspace_size(rows_max, f, dtype) bytes (control
  *                block, then the hidden activations)
  * bf16 runs on the tcgen05 tensor cores (fp32 accumulate in tensor memory);
- * fp32 runs on the fp32 FMA pipes.
+ * fp32 runs on the fp32 FMA pipes. The bf16 GEMMs (here, in moe_grouped_gemm
+ * and in moe_layer_forward) run as CTA pairs (thread-block clusters of 2
+ * sharing each MMA, 256-row tiles) when rows_max >= 256 * n_segments and the
+ * device can co-schedule them, otherwise one CTA per 128-row tile. The
+ * environment variable MOE_GEMM_CTA_PAIRS, read at every launch, overrides
+ * the choice: "0" one CTA per tile, anything else pairs.
  */
 int moe_expert_ffn(const moe_config* cfg, const void* xp, const int32_t* offsets,
                    int32_t n_segments, int64_t rows_max, int32_t f,

@@ -11,27 +11,41 @@
 //   plain  (GEMM2): out[r, n] = A[r] . B[s][:, n]
 // for rows r of segment s = [offsets[s], offsets[s+1]).
 //
-// Design (one CTA per SM, persistent):
-//   tile = 128 rows x 256 accumulator columns; SwiGLU tiles hold 128 columns
-//   of W1 and the same 128 columns of W3 side by side, so one 128x256x16 MMA
-//   produces both halves of a SwiGLU output tile.
-//   warp 0   : TMA producer, 4-stage ring of (A 128x64, B 64x256) bf16 tiles
-//              with 128-byte swizzle; A is K-major, B is read as stored
-//              ([K, n] row-major = MN-major), so weights need no repack.
+// Design (persistent, warp-specialised; one CTA per SM):
+//   tile = 256 rows x 256 accumulator columns computed by a CTA pair (a
+//   cluster of 2 CTAs, tcgen05 cta_group::2): CTA r holds rows 128r..128r+127
+//   of A and columns 128r..128r+127 of B in its shared memory, and its tensor
+//   memory receives its 128 rows of the 256-column accumulator. Each SM thus
+//   loads 32 KiB per 64-deep k-block for 128x256x64 of MMA work instead of
+//   48 KiB, and 6 stages of buffering fit in shared memory. SwiGLU tiles put
+//   128 columns of W1 (CTA 0) next to the same 128 columns of W3 (CTA 1), so
+//   one M=256, N=256 MMA produces both halves of a SwiGLU output tile.
+//   Where clusters cannot be formed the same kernel runs one CTA per tile
+//   (128 rows, both B halves, cta_group::1, 4 stages).
+//   warp 0   : TMA producer of its CTA's operand tiles (128-byte swizzle); A
+//              is K-major, B is read as stored ([K, n] row-major = MN-major),
+//              so weights need no repack. In a pair both producers count
+//              their bytes on CTA 0's full barrier.
 //   warp 1   : allocates 512 TMEM columns (two 256-column accumulators);
-//              lane 0 issues tcgen05.mma and tcgen05.commit.
+//              lane 0 of CTA 0 issues tcgen05.mma and tcgen05.commit, whose
+//              arrivals are multicast to both CTAs' barriers.
 //   warps 2-5: epilogue, TMEM -> registers (tcgen05.ld 32x32b), SwiGLU in
-//              fp32, bf16 stores; warp w reads TMEM lanes 32*(w%4)...
-//   Tiles run segment by segment, n-tile by n-tile, m fastest, so CTAs that
+//              fp32, bf16 stores; warp w reads TMEM lanes 32*(w%4)...; each
+//              warp signals CTA 0's accumulator-empty barrier when done.
+//   Tiles run segment by segment, n-tile by n-tile, m fastest, so units that
 //   run at the same time share the weight tile in L2. Segment sizes are read
 //   on the device: no host synchronisation.
 //   Every mbarrier wait is bounded (1 s of globaltimer); on expiry the CTA
 //   raises a shared abort flag, every role leaves its loop, outstanding TMA
 //   copies and MMAs are drained (bounded), TMEM is freed and
-//   MOE_ERR_DEVICE_TIMEOUT is recorded in the status word.
+//   MOE_ERR_DEVICE_TIMEOUT is recorded in the status word. The cluster
+//   barriers at entry and exit are reached by every thread whatever happened
+//   in between (all waits before them are bounded).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <cstdlib>
 
 #include "device_common.cuh"
 #include "internal.h"
@@ -42,23 +56,39 @@ namespace {
 
 using namespace tc;
 
-constexpr int kBM = 128;
+constexpr int kBM = 128;  // rows per CTA (TMEM lanes)
 constexpr int kBN = 256;  // accumulator columns per tile
 constexpr int kBK = 64;   // one 128-byte swizzle row of bf16
-constexpr int kStages = 4;
 constexpr int kABytes = kBM * kBK * 2;
-constexpr int kBBytes = kBN * kBK * 2;
-constexpr int kBBoxBytes = 64 * kBK * 2;  // one 64-column TMA box of B
-constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kBoxBytes = 64 * kBK * 2;  // one 64-column TMA box of B
 constexpr int kTmemCols = 512;
 constexpr int kThreads = 192;
+constexpr int kEpiWarps = 4;
 constexpr int kMaxSegments = 256;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 constexpr int kErrDeviceTimeout = -7;  // MOE_ERR_DEVICE_TIMEOUT
 
+// Geometry of the pair (PAIR) and single-CTA forms.
+template <bool PAIR>
+struct Geo {
+  static constexpr int kStages = PAIR ? 6 : 4;
+  static constexpr int kBoxes = PAIR ? 2 : 4;  // 64-column B boxes this CTA loads per k-block
+  static constexpr int kStageBytes = kABytes + kBoxes * kBoxBytes;
+  static constexpr int kTileRows = PAIR ? 2 * kBM : kBM;
+  // bytes the MMA issuer's full barrier waits for per k-block (both CTAs)
+  static constexpr uint32_t kTxBytes = (PAIR ? 2u : 1u) * static_cast<uint32_t>(kStageBytes);
+  // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A bf16 (7-9 =
+  // 1), B bf16 (10-12 = 1), A K-major (bit 15 = 0), B MN-major (bit 16 = 1),
+  // N >> 3 in bits 17-22, M >> 4 in bits 24-28 (M = 256 for a pair).
+  static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u << 16) |
+                                     (static_cast<uint32_t>(kBN >> 3) << 17) |
+                                     (static_cast<uint32_t>(kTileRows >> 4) << 24);
+};
+
+template <int STAGES>
 struct __align__(8) Ctrl {
-  unsigned long long full[kStages];
-  unsigned long long empty[kStages];
+  unsigned long long full[STAGES];
+  unsigned long long empty[STAGES];
   unsigned long long tfull[2];
   unsigned long long tempty[2];
   unsigned long long drain;
@@ -69,34 +99,62 @@ struct __align__(8) Ctrl {
   int mtiles[kMaxSegments];
   int seg_row[kMaxSegments + 1];    // offsets[], so a tile decodes from shared memory
 };
-constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + static_cast<int>(sizeof(Ctrl));
-
-// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A bf16 (7-9 = 1),
-// B bf16 (10-12 = 1), A K-major (bit 15 = 0), B MN-major (bit 16 = 1),
-// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u << 16) |
-                            (static_cast<uint32_t>(kBN >> 3) << 17) |
-                            (static_cast<uint32_t>(kBM >> 4) << 24);
+template <bool PAIR>
+constexpr int smem_bytes() {
+  return 1024 /*alignment slack*/ + Geo<PAIR>::kStages * Geo<PAIR>::kStageBytes +
+         static_cast<int>(sizeof(Ctrl<Geo<PAIR>::kStages>));
+}
+static_assert(smem_bytes<true>() <= 227 * 1024, "shared memory");
+static_assert(smem_bytes<false>() <= 227 * 1024, "shared memory");
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-template <bool SWIGLU>
+template <bool PAIR>
+__device__ __forceinline__ void tmem_alloc(uint32_t dst) {
+  if (PAIR) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  } else {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+}
+template <bool PAIR>
+__device__ __forceinline__ void tmem_dealloc(uint32_t base) {
+  if (PAIR)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(base), "r"(kTmemCols)
+                 : "memory");
+  else
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(base), "r"(kTmemCols)
+                 : "memory");
+}
+
+template <bool SWIGLU, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
     const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB1,
     const __grid_constant__ CUtensorMap tmB3, const int32_t* __restrict__ offsets, int S, int K,
     int n_out, int rows_max, __nv_bfloat16* __restrict__ out, int32_t* __restrict__ status,
     int withhold_kb) {
+  using G = Geo<PAIR>;
+  constexpr int kStages = G::kStages;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   unsigned char* smem = smem_raw + (base - raw);
-  Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + kStages * kStageBytes);
+  Ctrl<kStages>* ctrl = reinterpret_cast<Ctrl<kStages>*>(smem + kStages * G::kStageBytes);
   volatile int* abort_flag = &ctrl->abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR ? cluster_rank() : 0u;  // 0 issues the MMAs
+  const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int n_units = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   const int tile_n = SWIGLU ? kBN / 2 : kBN;  // output columns per tile
   const int n_tiles = (n_out + tile_n - 1) / tile_n;
   const int num_kb = (K + kBK - 1) / kBK;
@@ -109,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&ctrl->tfull[b]), 1);
-      mbar_init(smem_u32(&ctrl->tempty[b]), 128);
+      mbar_init(smem_u32(&ctrl->tempty[b]), (PAIR ? 2 : 1) * kEpiWarps);
     }
     mbar_init(smem_u32(&ctrl->drain), 1);
     ctrl->abort_flag = 0;
@@ -128,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
       if (s < S) {
         r0 = offsets[s];
         r1 = offsets[s + 1];
-        mt = (r1 - r0 + kBM - 1) / kBM;
+        mt = (r1 - r0 + G::kTileRows - 1) / G::kTileRows;
         ctrl->seg_row[s] = r0;
         if (s == S - 1) ctrl->seg_row[S] = r1;
       }
@@ -149,15 +207,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
       ctrl->total_tiles = run;
     }
   }
-  if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(&ctrl->tmem_base)),
-                 "r"(kTmemCols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
+  if (warp == 1) tmem_alloc<PAIR>(smem_u32(&ctrl->tmem_base));
   tc_fence_before();
   __syncthreads();
+  if (PAIR) {  // the peer's barriers are initialised before anything targets them
+    __syncwarp();
+    cluster_sync();
+  }
   tc_fence_after();
   const uint32_t tmem_base = ctrl->tmem_base;
   const int total = ctrl->total_tiles;
@@ -173,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
     const int local = tile - ctrl->tile_base[seg];
     const int mt = ctrl->mtiles[seg];
     const int n_idx = local / mt, m_idx = local - n_idx * mt;
-    row0 = ctrl->seg_row[seg] + m_idx * kBM;
+    row0 = ctrl->seg_row[seg] + m_idx * G::kTileRows;
     row_end = ctrl->seg_row[seg + 1];
     col0 = n_idx * tile_n;
   };
@@ -187,65 +243,80 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
     uint32_t issued_phase[kStages];
     for (int s = 0; s < kStages; ++s) issued[s] = 0, issued_phase[s] = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+    for (int tile = unit; ok && tile < total; tile += n_units) {
       int seg, row0, row_end, col0;
       decode(tile, seg, row0, row_end, col0);
+      const int arow = row0 + static_cast<int>(rank) * kBM;
       for (int kb = 0; kb < num_kb; ++kb) {
-        const uint32_t fb = smem_u32(&ctrl->full[stage]);
+        const uint32_t fb_local = smem_u32(&ctrl->full[stage]);
         if (!mbar_wait(smem_u32(&ctrl->empty[stage]), phase ^ 1u, abort_flag, kWaitLimitNs)) {
           ok = false;
           break;
         }
-        mbar_expect_tx(fb, kStageBytes);
-        if (kb == withhold_kb && tile == 0) {
-          // failure-detection self-test: announce the stage's bytes but load
-          // nothing, so the MMA issuer's bounded wait expires
-          issued[stage] = 1;
-          issued_phase[stage] = phase;
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
-          continue;
-        }
-        const uint32_t sa = stage0 + stage * kStageBytes;
-        const uint32_t sb = sa + kABytes;
-        tma_load_2d(sa, &tmA, kb * kBK, row0, fb);
-        if (SWIGLU) {
-          tma_load_3d(sb + 0 * kBBoxBytes, &tmB1, col0, kb * kBK, seg, fb);
-          tma_load_3d(sb + 1 * kBBoxBytes, &tmB1, col0 + 64, kb * kBK, seg, fb);
-          tma_load_3d(sb + 2 * kBBoxBytes, &tmB3, col0, kb * kBK, seg, fb);
-          tma_load_3d(sb + 3 * kBBoxBytes, &tmB3, col0 + 64, kb * kBK, seg, fb);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) tma_load_3d(sb + j * kBBoxBytes, &tmB1, col0 + 64 * j, kb * kBK, seg, fb);
-        }
+        // in a pair every copy counts on CTA 0's barrier, which expects both
+        const uint32_t fb = PAIR ? map_to_rank(fb_local, 0) : fb_local;
+        if (rank == 0) mbar_expect_tx(fb_local, G::kTxBytes);
         issued[stage] = 1;
         issued_phase[stage] = phase;
+        if (!(kb == withhold_kb && tile == 0)) {
+          // (failure-detection self-test: the withheld k-block is announced
+          // but never loaded, so the MMA issuer's bounded wait expires)
+          const uint32_t sa = stage0 + stage * G::kStageBytes;
+          const uint32_t sb = sa + kABytes;
+          if (PAIR) {
+            tma_load_2d_pair(sa, &tmA, kb * kBK, arow, fb);
+            // CTA 0: W1 (or B) columns col0.., CTA 1: W3 columns col0.. (or
+            // B columns col0 + 128..)
+            const CUtensorMap* mb = (SWIGLU && rank == 1) ? &tmB3 : &tmB1;
+            const int c = SWIGLU ? col0 : col0 + static_cast<int>(rank) * 128;
+            tma_load_3d_pair(sb, mb, c, kb * kBK, seg, fb);
+            tma_load_3d_pair(sb + kBoxBytes, mb, c + 64, kb * kBK, seg, fb);
+          } else {
+            tma_load_2d(sa, &tmA, kb * kBK, arow, fb);
+            if (SWIGLU) {
+              tma_load_3d(sb + 0 * kBoxBytes, &tmB1, col0, kb * kBK, seg, fb);
+              tma_load_3d(sb + 1 * kBoxBytes, &tmB1, col0 + 64, kb * kBK, seg, fb);
+              tma_load_3d(sb + 2 * kBoxBytes, &tmB3, col0, kb * kBK, seg, fb);
+              tma_load_3d(sb + 3 * kBoxBytes, &tmB3, col0 + 64, kb * kBK, seg, fb);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                tma_load_3d(sb + j * kBoxBytes, &tmB1, col0 + 64 * j, kb * kBK, seg, fb);
+            }
+          }
+        }
         if (++stage == kStages) {
           stage = 0;
           phase ^= 1u;
         }
       }
     }
-    if (!ok) {  // drain copies in flight before the CTA can exit (bounded)
-      for (int s = 0; s < kStages; ++s) {
-        if (!issued[s]) continue;
+    if (!ok) {  // copies in flight land before the CTA (or its pair) can exit (bounded)
+      if (rank == 0) {
+        for (int s = 0; s < kStages; ++s) {
+          if (!issued[s]) continue;
+          const unsigned long long t0 = global_ns();
+          while (!mbar_try(smem_u32(&ctrl->full[s]), issued_phase[s]))
+            if (global_ns() - t0 > kWaitLimitNs / 10) break;
+        }
+      } else {  // CTA 1 cannot observe CTA 0's barrier: give its copies 2 ms
         const unsigned long long t0 = global_ns();
-        while (!mbar_try(smem_u32(&ctrl->full[s]), issued_phase[s]))
-          if (global_ns() - t0 > kWaitLimitNs / 10) break;
+        while (global_ns() - t0 < 2000000ull) {
+        }
       }
     }
-  } else if (warp == 1 && lane == 0) {
+  } else if (warp == 1 && lane == 0 && rank == 0) {
     // ---------------- MMA issuer ----------------
     int stage = 0;
     uint32_t phase = 0;
     int local = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++local) {
+    for (int tile = unit; ok && tile < total; tile += n_units, ++local) {
       const int buf = local & 1;
       const uint32_t use = static_cast<uint32_t>(local >> 1);
-      if (!mbar_wait(smem_u32(&ctrl->tempty[buf]), (use & 1u) ^ 1u, abort_flag, kWaitLimitNs)) {
+      // the accumulator is free once every epilogue warp (of both CTAs) is done
+      if (!mbar_wait_cluster(smem_u32(&ctrl->tempty[buf]), (use & 1u) ^ 1u, abort_flag,
+                             kWaitLimitNs)) {
         ok = false;
         break;
       }
@@ -257,22 +328,29 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
           break;
         }
         tc_fence_after();
-        const uint32_t sa = stage0 + stage * kStageBytes;
+        const uint32_t sa = stage0 + stage * G::kStageBytes;
         const uint32_t sb = sa + kABytes;
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk)
-          tc_mma(d_tmem, kmajor_desc(sa, kk), mnmajor_desc(sb, kk, kBBoxBytes), kIdesc, (kb | kk) != 0 ? 1u : 0u);
-        tc_commit(smem_u32(&ctrl->empty[stage]));
+        for (int kk = 0; kk < kBK / 16; ++kk) {
+          const uint64_t ad = kmajor_desc(sa, kk), bd = mnmajor_desc(sb, kk, kBoxBytes);
+          const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
+          if (PAIR) tc_mma_pair(d_tmem, ad, bd, G::kIdesc, acc);
+          else tc_mma(d_tmem, ad, bd, G::kIdesc, acc);
+        }
+        if (PAIR) tc_commit_pair_mc(smem_u32(&ctrl->empty[stage]), 0x3);
+        else tc_commit(smem_u32(&ctrl->empty[stage]));
         if (++stage == kStages) {
           stage = 0;
           phase ^= 1u;
         }
       }
       if (!ok) break;
-      tc_commit(smem_u32(&ctrl->tfull[buf]));
+      if (PAIR) tc_commit_pair_mc(smem_u32(&ctrl->tfull[buf]), 0x3);
+      else tc_commit(smem_u32(&ctrl->tfull[buf]));
     }
     // every MMA issued so far completes before this arrives
-    tc_commit(smem_u32(&ctrl->drain));
+    if (PAIR) tc_commit_pair(smem_u32(&ctrl->drain));
+    else tc_commit(smem_u32(&ctrl->drain));
     const unsigned long long t0 = global_ns();
     while (!mbar_try(smem_u32(&ctrl->drain), 0u))
       if (global_ns() - t0 > kWaitLimitNs) {
@@ -282,8 +360,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
   } else if (warp >= 2) {
     // ---------------- epilogue ----------------
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const uint32_t tempty0 = PAIR ? map_to_rank(smem_u32(&ctrl->tempty[0]), 0) : smem_u32(&ctrl->tempty[0]);
     int local = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
+    for (int tile = unit; tile < total; tile += n_units, ++local) {
       const int buf = local & 1;
       const uint32_t use = static_cast<uint32_t>(local >> 1);
       int ok = 1;
@@ -293,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
       tc_fence_after();
       int seg, row0, row_end, col0;
       decode(tile, seg, row0, row_end, col0);
-      const int row = row0 + q * 32 + lane;
+      const int row = row0 + static_cast<int>(rank) * kBM + q * 32 + lane;
       const bool valid = row >= 0 && row < row_end && row < rows_max;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * kBN);
       __nv_bfloat16* orow = out + static_cast<size_t>(row) * n_out;
@@ -334,20 +413,112 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
         }
       }
       tc_fence_before();
-      mbar_arrive(smem_u32(&ctrl->tempty[buf]));
+      __syncwarp();
+      if (lane == 0) {
+        const uint32_t te = tempty0 + static_cast<uint32_t>(buf * sizeof(unsigned long long));
+        if (PAIR) mbar_arrive_cluster(te);
+        else mbar_arrive(te);
+      }
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  if (PAIR) {  // CTA 0's MMAs into this CTA's TMEM and shared memory are done
+    __syncwarp();
+    cluster_sync();
+  }
   tc_fence_after();
   if (threadIdx.x == 0 && *abort_flag) record_status(status, kErrDeviceTimeout);
   if (warp == 1) {
     __syncwarp();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                 "r"(kTmemCols)
-                 : "memory");
+    tmem_dealloc<PAIR>(tmem_base);
   }
+}
+
+// Clusters of 2 that can be resident at once (0: pairs unavailable).
+template <bool SWIGLU>
+int pair_slots(int dev) {
+  static int cached[64] = {};
+  static bool done[64] = {};
+  if (dev < 0 || dev >= 64) return 0;
+  if (done[dev]) return cached[dev];
+  int n = 0;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(device_sm_count() & ~1));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem_bytes<true>();
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_tc_kernel<SWIGLU, true>, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    n = 0;
+  }
+  cached[dev] = n;
+  done[dev] = true;
+  return n;
+}
+
+template <bool SWIGLU, bool PAIR>
+cudaError_t set_smem_attr(int dev) {
+  static bool attr_set[64] = {};
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (attr_set[dev]) return cudaSuccess;
+  const cudaError_t err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<SWIGLU, PAIR>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               smem_bytes<PAIR>());
+  if (err == cudaSuccess) attr_set[dev] = true;
+  return err;
+}
+
+template <bool SWIGLU>
+cudaError_t launch_gemm(const CUtensorMap& mA, const CUtensorMap& mB1, const CUtensorMap& mB3,
+                        const int32_t* offsets, int S, int64_t rows_max, int K, int n_out,
+                        __nv_bfloat16* o, int32_t* status, cudaStream_t s, int withhold_kb) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if ((err = set_smem_attr<SWIGLU, true>(dev)) != cudaSuccess) return err;
+  if ((err = set_smem_attr<SWIGLU, false>(dev)) != cudaSuccess) return err;
+  // Pairs pay off once segments average a 256-row tile; below that (decode
+  // batches) half of every pair tile would be padding.
+  const char* env = getenv("MOE_GEMM_CTA_PAIRS");
+  const bool want_pairs = env ? env[0] != '0' : rows_max >= 2LL * kBM * S;
+  const int slots = want_pairs ? pair_slots<SWIGLU>(dev) : 0;
+  const bool pair = slots > 0;
+  const int tile_rows = pair ? 2 * kBM : kBM;
+  const int tile_n = SWIGLU ? kBN / 2 : kBN;
+  const long long n_tiles = (n_out + tile_n - 1) / tile_n;
+  const long long m_tiles_max = (rows_max + tile_rows - 1) / tile_rows + S;
+  long long units = n_tiles * m_tiles_max;
+  const long long cap = pair ? slots : device_sm_count();
+  if (units > cap) units = cap;
+  const int rmax = rows_max > 0x7fffffff ? 0x7fffffff : static_cast<int>(rows_max);
+
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = pair ? 2 : 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(pair ? 2 * units : units));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = pair ? smem_bytes<true>() : smem_bytes<false>();
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = pair ? 2 : 1;
+  if (pair)
+    return cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<SWIGLU, true>, mA, mB1, mB3, offsets, S,
+                              K, n_out, rmax, o, status, withhold_kb);
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<SWIGLU, false>, mA, mB1, mB3, offsets, S,
+                            K, n_out, rmax, o, status, withhold_kb);
 }
 
 }  // namespace
@@ -367,35 +538,10 @@ cudaError_t launch_grouped_gemm_tc_bf16(const void* A, const int32_t* offsets, i
   } else {
     mB3 = mB1;
   }
-  const int tile_n = swiglu ? kBN / 2 : kBN;
-  const long long n_tiles = (n_out + tile_n - 1) / tile_n;
-  const long long m_tiles_max = (rows_max + kBM - 1) / kBM + S;
-  long long grid = n_tiles * m_tiles_max;
-  const int sms = device_sm_count();
-  if (grid > sms) grid = sms;
-
-  static bool attr_set[64][2] = {};
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
-  if (err != cudaSuccess) return err;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_set[dev][swiglu ? 1 : 0]) {
-    err = swiglu ? cudaFuncSetAttribute(grouped_gemm_tc_kernel<true>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes)
-                 : cudaFuncSetAttribute(grouped_gemm_tc_kernel<false>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (err != cudaSuccess) return err;
-    attr_set[dev][swiglu ? 1 : 0] = true;
-  }
   __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
-  const int rmax = rows_max > 0x7fffffff ? 0x7fffffff : static_cast<int>(rows_max);
   if (swiglu)
-    return launch_pdl(grouped_gemm_tc_kernel<true>, static_cast<unsigned>(grid), kThreads,
-                      kSmemBytes, s, mA, mB1, mB3, offsets, S, K, n_out, rmax, o, status,
-                      withhold_kb);
-  return launch_pdl(grouped_gemm_tc_kernel<false>, static_cast<unsigned>(grid), kThreads,
-                    kSmemBytes, s, mA, mB1, mB3, offsets, S, K, n_out, rmax, o, status,
-                    withhold_kb);
+    return launch_gemm<true>(mA, mB1, mB3, offsets, S, rows_max, K, n_out, o, status, s, withhold_kb);
+  return launch_gemm<false>(mA, mB1, mB3, offsets, S, rows_max, K, n_out, o, status, s, withhold_kb);
 }
 
 }  // namespace moe

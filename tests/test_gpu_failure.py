@@ -20,7 +20,9 @@ def _gemm_inputs(S=2, rows_per=200, K=256, n_out=384):
     return A, B, offs, out, ws, S, rows, K, n_out
 
 
-def test_expired_wait_reports_timeout_and_context_survives():
+@pytest.mark.parametrize("pairs", ["1", "0"], ids=["cta_pairs", "single_cta"])
+def test_expired_wait_reports_timeout_and_context_survives(pairs, monkeypatch):
+    monkeypatch.setenv("MOE_GEMM_CTA_PAIRS", pairs)
     A, B, offs, out, ws, S, rows, K, n_out = _gemm_inputs()
     M.moe_selftest_expired_wait(A, offs, S, rows, K, n_out, B, out, ws)
     torch.cuda.synchronize()

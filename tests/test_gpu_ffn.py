@@ -18,6 +18,14 @@ def _segments(sizes):
     return off
 
 
+@pytest.fixture(params=["cta_pairs", "single_cta"])
+def gemm_form(request, monkeypatch):
+    """Run a bf16 case through both forms of the tcgen05 grouped GEMM: CTA
+    pairs (cta_group::2, 256-row tiles) and one CTA per 128-row tile."""
+    monkeypatch.setenv("MOE_GEMM_CTA_PAIRS", "1" if request.param == "cta_pairs" else "0")
+    return request.param
+
+
 def _rand(shape, seed, scale=1.0, dtype=torch.bfloat16):
     g = torch.Generator().manual_seed(seed)
     return (torch.randn(shape, generator=g) * scale).to(dtype)
@@ -31,7 +39,7 @@ def _rand(shape, seed, scale=1.0, dtype=torch.bfloat16):
     ([19150, 50], 512, 256),      # 151 tiles: one more than a full round of CTAs
     ([77, 300, 5], 2048, 512),    # few tiles, long K, ragged rows
 ])
-def test_grouped_gemm_bf16_against_torch(sizes, K, n_out):
+def test_grouped_gemm_bf16_against_torch(sizes, K, n_out, gemm_form):
     S = len(sizes)
     off = _segments(sizes)
     P = int(off[-1])
@@ -60,7 +68,7 @@ def test_grouped_gemm_bf16_against_torch(sizes, K, n_out):
     ([300, 300], 320, 128),
     ([77], 2048, 1408),
 ])
-def test_expert_ffn_bf16_against_oracle(sizes, d, f):
+def test_expert_ffn_bf16_against_oracle(sizes, d, f, gemm_form):
     S = len(sizes)
     off = _segments(sizes)
     P = int(off[-1])
