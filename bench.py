@@ -236,7 +236,13 @@ def gemm_traffic(w):
 # dram__bytes_read.sum + dram__bytes_write.sum of expert_gemm1_swiglu +
 # expert_gemm2 from one ncu capture per workload (profiles/ has the summary),
 # keyed by the sha256 prefix of the kernel source it was taken on.
-GEMM_TRAFFIC = {}
+GEMM_TRAFFIC = {
+    # profiles/grouped_gemm_tc_pairs_mixtral_gamma1_bf16.md: GEMM1+SwiGLU
+    # 1.973634 GB read + 0.141470 GB written, GEMM2 1.185924 GB + 0.040475 GB
+    "mixtral_bf16_gamma1": {"kernel_sha": "441cef60e131d3bc",
+                            "bytes_per_launch_pair": 1.973634e9 + 0.141470e9 +
+                            1.185924e9 + 0.040475e9},
+}
 
 
 def run_ours(args, rank, world, local_rank):
@@ -351,27 +357,53 @@ def run_ours(args, rank, world, local_rank):
     stage_ms = {name: statistics.mean(row[i].elapsed_time(row[i + 1]) for row in tr)
                 for i, name in enumerate(stages)}
 
-    # ---- end to end through host buffers: H2D x, layer, D2H y every step ----
+    # ---- end to end through host buffers: every step copies its x from
+    # pinned host memory, runs the layer and copies y back to pinned host
+    # memory. Three streams pipeline the steps as a server would: step i+1's
+    # upload and step i-1's download overlap step i's layer (double-buffered
+    # device x and y; events order the reuse of each buffer) ----
     x_host = inp["x"].pin_memory()
-    y_host = torch.empty((w.T, w.d), dtype=dt).pin_memory()
-    x_dev = torch.empty_like(d["x"])
+    y_host = [torch.empty((w.T, w.d), dtype=dt).pin_memory() for _ in range(2)]
+    x_dev = [torch.empty_like(d["x"]) for _ in range(2)]
+    y_dev = [torch.empty_like(y) for _ in range(2)]
+    s_up = torch.cuda.Stream(dev)
+    s_down = torch.cuda.Stream(dev)
+    up_done = [torch.cuda.Event() for _ in range(2)]
+    layer_done = [torch.cuda.Event() for _ in range(2)]
+    down_done = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step():
-        x_dev.copy_(x_host, non_blocking=True)
-        M.moe_layer_forward(cfg, x_dev, d["W_r"], d["bias"], d["W1"], d["W3"], d["W2"],
-                            d.get("Ws1"), d.get("Ws3"), d.get("Ws2"), y, ws, stats=stats,
-                            stream=stream)
-        y_host.copy_(y, non_blocking=True)
+    def e2e_steps(n):
+        for i in range(n):
+            b = i & 1
+            with torch.cuda.stream(s_up):
+                if i >= 2:
+                    s_up.wait_event(layer_done[b])  # step i-2 has read x_dev[b]
+                x_dev[b].copy_(x_host, non_blocking=True)
+                up_done[b].record(s_up)
+            stream.wait_event(up_done[b])
+            if i >= 2:
+                stream.wait_event(down_done[b])  # step i-2's y_dev[b] is on the host
+            M.moe_layer_forward(cfg, x_dev[b], d["W_r"], d["bias"], d["W1"], d["W3"], d["W2"],
+                                d.get("Ws1"), d.get("Ws3"), d.get("Ws2"), y_dev[b], ws,
+                                stats=stats, stream=stream)
+            layer_done[b].record(stream)
+            with torch.cuda.stream(s_down):
+                s_down.wait_event(layer_done[b])
+                y_host[b].copy_(y_dev[b], non_blocking=True)
+                down_done[b].record(s_down)
+        # the region ends when the last download has landed
+        for ev in down_done:
+            stream.wait_event(ev)
 
-    for _ in range(2):
-        e2e_step()
+    e2e_steps(2)
     torch.cuda.synchronize()
     if dist:
         td.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
+    s_up.wait_event(e0)
+    s_down.wait_event(e0)
+    e2e_steps(args.steps)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
@@ -379,6 +411,8 @@ def run_ours(args, rank, world, local_rank):
         t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
         td.all_reduce(t, op=td.ReduceOp.MAX)
         e2e_ms = float(t.item())
+    if not torch.equal(y_host[(args.steps - 1) & 1], y.cpu()):
+        raise RuntimeError("end-to-end output differs from the device-resident run")
     e2e_value = world * w.T * args.steps / (e2e_ms / 1e3)
     sx = 2 if w.dtype == "bf16" else 4
 
@@ -438,10 +472,16 @@ def run_ours(args, rank, world, local_rank):
                      "bound": "tensor", "achieved": ffn_tflops, "peak": peak_tf,
                      "unit": "TFLOP/s", "frac": ffn_tflops / peak_tf,
                      "traffic": gemm_traffic(w),
-                     "peak_source": f"{peak_src} bf16 burst"},
+                     "traffic_unit": "DRAM bytes per step (both GEMM launches), one ncu capture",
+                     "peak_source": f"{peak_src} bf16 burst",
+                     "frac_of_sustained": ffn_tflops / float(peaks.get("bf16_tflops_sustained",
+                                                                       peak_tf))},
         "kernels": kernels,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": w.T * w.d * sx,
-                "d2h_bytes_per_step": w.T * w.d * sx},
+                "d2h_bytes_per_step": w.T * w.d * sx,
+                "pipeline": "pinned host x -> device, layer, device y -> pinned host every "
+                            "step; step i+1's upload and step i-1's download overlap step "
+                            "i's layer (3 streams)"},
         "gpu_launches": len(stages) * args.steps,
         "launch": "programmatic dependent launch; events only around the expert GEMMs",
         "clocks": clk,
