@@ -22,7 +22,9 @@ It is written as a plain, slow, direct reading of the pages it cites:
   (gist.science summary of arXiv 2503.05066), §2① Capacity-Aware Token Drop:
   each expert has capacity C = gamma * N_bar and the tokens beyond it with the
   lowest gating scores are dropped; §2② Capacity-Aware Expanded Drop: a token's
-  candidate set grows by m local experts of the same device.
+  candidate set grows by m local experts of the same device; §2③
+  Device-Level Capacity-Aware Inference: the capacity is held per device, so an
+  expert over its own share keeps its tokens while its device has room.
 * "How to design inference cost with MoE routing" (blog.gillilab.com),
   §"how routing allocates the compute budget": a shared expert that every token
   passes through.
@@ -49,6 +51,12 @@ Readings taken where the pages are silent (each repeated where it is used):
   R8 storage points: bf16 layers keep x, weights, the SwiGLU hidden h, each
      expert output and y in bf16; fp32 layers keep them in fp32; every sum and
      product is taken in fp64 here and rounded only at those points.
+  R13 device-level capacity: a device is the group of `group_size` consecutive
+     experts (as in R7); its capacity is the sum of its experts' capacities,
+     floor(gamma * N_bar * group_size), capped at T * min(kc, group_size);
+     over capacity the device keeps its highest-gate candidates, ties to the
+     lower token, then to the token's earlier candidate slot; tokens are not
+     moved between experts.
 """
 from __future__ import annotations
 
@@ -285,6 +293,46 @@ def capacity_drop(idx, gate, N: int, C: int):
     return keep, demand, kept
 
 
+def device_capacity(gamma: float, k: int, T: int, N: int, group_size: int, kc: int) -> int:
+    """Capacity of one device, a group of `group_size` experts, for
+    device-level capacity-aware inference ("Capacity-Aware Inference", §2③:
+    capacity is managed per device instead of per expert; reading R13): the
+    sum of its experts' capacities, floor(gamma * N_bar * group_size) in fp64
+    with N_bar = k*T/N, capped at the largest possible device demand
+    T * min(kc, group_size); gamma = inf means no limit."""
+    most = T * min(kc, group_size)
+    if math.isinf(gamma):
+        return most
+    nbar = (k * T) / N
+    return int(min(math.floor(gamma * nbar * group_size), most))
+
+
+def device_capacity_drop(idx, gate, N: int, group_size: int, C_dev: int):
+    """Device-level capacity-aware drop ("Capacity-Aware Inference", §2③;
+    reading R13): the candidates of all experts of a device (a group of
+    `group_size` consecutive experts) share one capacity C_dev; an expert may
+    exceed its own share as long as the device has room. Over capacity, the
+    device keeps the C_dev candidates with the highest gating score, ties to
+    the lower token and then to the token's earlier candidate slot.
+
+    Returns keep[T, kc] (bool), demand[N] and kept[N] per expert."""
+    idx = np.asarray(idx)
+    T, kc = idx.shape
+    keep = np.zeros((T, kc), dtype=bool)
+    gk = key32(gate).astype(np.int64)
+    for lo in range(0, N, group_size):
+        ts, js = np.nonzero((idx >= lo) & (idx < lo + group_size))
+        if len(ts) <= C_dev:
+            sel = np.arange(len(ts))
+        else:
+            order = np.lexsort((js, ts, -gk[ts, js]))   # key desc, token asc, slot asc
+            sel = order[:C_dev]
+        keep[ts[sel], js[sel]] = True
+    demand = np.array([(idx == e).sum() for e in range(N)], dtype=np.int64)
+    kept = np.array([((idx == e) & keep).sum() for e in range(N)], dtype=np.int64)
+    return keep, demand, kept
+
+
 def expert_choice(p, c: int):
     """Each expert takes the c tokens with the highest score p[:, e], ties to
     the lower token ("MoE vs MoT", §"Mixture of Tokens"; reading R4).
@@ -337,6 +385,11 @@ def route(L, *, mode: str, k: int, N: int, gamma: float = math.inf, m: int = 0,
     if m > 0:
         idx = expanded_candidates(L, idx, m, group_size, home_group)
     gate = token_gates(p, idx, renorm)
+    if mode == "capacity_drop_device":
+        C = device_capacity(gamma, k, T, N, group_size, idx.shape[1])
+        keep, demand, kept = device_capacity_drop(idx, gate, N, group_size, C)
+        return dict(p=p, idx=idx, gate=gate, keep=keep, demand=demand, kept=kept,
+                    coverage=keep.sum(axis=1).astype(np.int64), C=C)
     C = capacity(gamma, k, T, N) if mode == "capacity_drop" else T
     keep, demand, kept = capacity_drop(idx, gate, N, C)
     return dict(p=p, idx=idx, gate=gate, keep=keep, demand=demand, kept=kept,

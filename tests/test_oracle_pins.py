@@ -198,6 +198,99 @@ def test_gamma_inf_equals_token_choice_and_zero_drops_all():
     assert not z["keep"].any()
 
 
+
+# ------------------------------------------------- device-level capacity (§2③)
+
+def test_device_capacity_values():
+    # finegrained layer: N_bar = 6*8192/64 = 768, a device of 8 experts holds 1.25*768*8
+    assert O.device_capacity(1.25, 6, 8192, 64, 8, 6) == 7680
+    assert O.device_capacity(math.inf, 6, 8192, 64, 8, 6) == 8192 * 6
+    assert O.device_capacity(math.inf, 2, 100, 8, 1, 2) == 100
+    for g in (0.5, 1.0, 1.5):  # one expert per device: the per-expert capacity
+        assert O.device_capacity(g, 2, 4096, 8, 1, 2) == O.capacity(g, 2, 4096, 8)
+    assert O.device_capacity(1e9, 2, 16, 8, 4, 3) == 16 * 3
+
+
+def test_device_drop_with_one_expert_per_device_is_expert_drop():
+    L = W.random_logits(300, 8, seed=31, quantum=0.25).numpy()
+    L[:, 1] += 1.0
+    for gamma in (0.5, 1.0, 1.3):
+        a = O.route(L, mode="capacity_drop_device", k=2, N=8, gamma=gamma, group_size=1)
+        b = O.route(L, mode="capacity_drop", k=2, N=8, gamma=gamma)
+        for key in ("idx", "gate", "keep", "kept", "demand", "C"):
+            assert np.array_equal(a[key], b[key]), key
+
+
+def _brute_keep_device(cands, C):
+    """cands: list of (token, slot, gate). The kept set is the unique C-subset
+    whose members all rank above every non-member, rank = (gate desc, token
+    asc, slot asc)."""
+    if len(cands) <= C:
+        return set((t, j) for t, j, _ in cands)
+    def above(a, b):
+        return (a[2] > b[2]) or (a[2] == b[2] and (a[0], a[1]) < (b[0], b[1]))
+    best = None
+    for sub in itertools.combinations(range(len(cands)), C):
+        inside = [cands[i] for i in sub]
+        outside = [cands[i] for i in range(len(cands)) if i not in sub]
+        if all(above(a, b) for a in inside for b in outside):
+            assert best is None
+            best = set((t, j) for t, j, _ in inside)
+    return best
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_device_drop_brute_force(seed):
+    T, N, k, gs = 8, 4, 2, 2
+    L = W.random_logits(T, N, seed=40 + seed, quantum=0.5).numpy()
+    rt = O.route(L, mode="capacity_drop_device", k=k, N=N, gamma=0.75, group_size=gs)
+    C = rt["C"]
+    assert C == 6  # floor(0.75 * (2*8/4) * 2)
+    for lo in range(0, N, gs):
+        ts, js = np.nonzero((rt["idx"] >= lo) & (rt["idx"] < lo + gs))
+        cands = [(int(t), int(j), float(rt["gate"][t, j])) for t, j in zip(ts, js)]
+        kept = set((int(t), int(j)) for t, j in zip(ts, js) if rt["keep"][t, j])
+        assert kept == _brute_keep_device(cands, C)
+    for e in range(N):
+        assert rt["kept"][e] == (rt["keep"] & (rt["idx"] == e)).sum()
+        assert rt["demand"][e] == (rt["idx"] == e).sum()
+
+
+def test_device_drop_invariants_and_room_sharing():
+    T, N, k, gs = 2000, 16, 2, 4
+    L = W.random_logits(T, N, seed=23, quantum=0.25).numpy()
+    L[:, 0] += 2.0                                      # overload expert 0 of device 0
+    dev = O.route(L, mode="capacity_drop_device", k=k, N=N, gamma=1.0, group_size=gs, renorm=True)
+    per = O.route(L, mode="capacity_drop", k=k, N=N, gamma=1.0, renorm=True)
+    Cd, Ce = dev["C"], per["C"]
+    assert Cd == gs * Ce
+    gk = O.key32(dev["gate"]).astype(np.int64)
+    for lo in range(0, N, gs):
+        ts, js = np.nonzero((dev["idx"] >= lo) & (dev["idx"] < lo + gs))
+        kp = dev["keep"][ts, js]
+        assert kp.sum() == min(len(ts), Cd)
+        if (~kp).any() and kp.any():
+            kk, dk = gk[ts[kp], js[kp]], gk[ts[~kp], js[~kp]]
+            assert kk.min() >= dk.max()
+            thr = kk.min()
+            if (dk == thr).any():  # at the threshold key, kept (token, slot) precede dropped
+                fk = (ts[kp] * k + js[kp])[kk == thr]
+                fd = (ts[~kp] * k + js[~kp])[dk == thr]
+                assert fk.max() < fd.min()
+    # the device keeps at least as many pairs as its experts would alone, and
+    # the overloaded expert uses room its device-mates leave
+    assert dev["kept"].sum() >= per["kept"].sum()
+    assert dev["kept"][0] > Ce and per["kept"][0] == Ce
+    assert np.array_equal(dev["idx"], per["idx"]) and np.array_equal(dev["gate"], per["gate"])
+
+
+def test_device_drop_unlimited_is_token_choice():
+    L = W.random_logits(100, 8, seed=9).numpy()
+    a = O.route(L, mode="capacity_drop_device", k=2, N=8, gamma=math.inf, group_size=4)
+    b = O.route(L, mode="token_choice", k=2, N=8)
+    for key in ("idx", "gate", "keep", "kept", "demand"):
+        assert np.array_equal(a[key], b[key])
+
 @pytest.mark.parametrize("quantum", [None, 0.25])
 def test_expert_choice_invariants(quantum):
     T, N, k = 64, 8, 2
