@@ -13,7 +13,11 @@
  *     drops the candidates with the lowest gating score, optionally with m
  *     extra local candidates per token ("Capacity-Aware Inference: Mitigating
  *     the Straggler Effect in MoE", section 2, (1) Token Drop and (2) Expanded
- *     Drop).
+ *     Drop);
+ *   - device-level capacity-aware drop: the experts of a device (a group of
+ *     group_size consecutive experts) share one capacity, the sum of theirs,
+ *     so an expert over its own share keeps its tokens while its device has
+ *     room (same page, section 2, (3) Device-Level Capacity-Aware Inference).
  *
  * Conventions for every call below:
  *   - Pointers to tensors are DEVICE pointers unless a comment says host.
@@ -65,6 +69,7 @@ extern "C" {
 #define MOE_TOKEN_CHOICE   0
 #define MOE_EXPERT_CHOICE  1
 #define MOE_CAPACITY_DROP  2
+#define MOE_CAPACITY_DROP_DEVICE 3  /* capacity per device group of group_size experts */
 
 #define MOE_F32  0
 #define MOE_BF16 1
@@ -74,7 +79,7 @@ extern "C" {
 
 /* Limits: 1 <= N <= 256, 1 <= k <= N, k + m <= 32, expert choice N <= 256,
  * T <= 24576 (per-expert candidate lists are held in shared memory),
- * capacity-drop/expanded group_size divides N. */
+ * expanded and device-level drop: group_size divides N. */
 
 typedef struct moe_config {
   int32_t T;          /* tokens in the batch */
@@ -82,10 +87,13 @@ typedef struct moe_config {
   int32_t N;          /* routed experts */
   int32_t f;          /* routed expert hidden width */
   int32_t k;          /* experts per token (expert choice: c = floor(k*T/N)) */
-  int32_t mode;       /* MOE_TOKEN_CHOICE / MOE_EXPERT_CHOICE / MOE_CAPACITY_DROP */
-  double  gamma;      /* capacity factor; C = min(T, floor(gamma * k*T/N)); INFINITY = no limit */
+  int32_t mode;       /* MOE_TOKEN_CHOICE / MOE_EXPERT_CHOICE / MOE_CAPACITY_DROP /
+                         MOE_CAPACITY_DROP_DEVICE */
+  double  gamma;      /* capacity factor; C = min(T, floor(gamma * k*T/N)); INFINITY = no limit.
+                         MOE_CAPACITY_DROP_DEVICE: a device holds
+                         min(T * min(kc, group_size), floor(gamma * k*T/N * group_size)) */
   int32_t m;          /* expanded drop: extra local candidates per token (0 = off) */
-  int32_t group_size; /* experts per device group for expanded drop */
+  int32_t group_size; /* experts per device group (expanded drop, device-level drop) */
   int32_t renorm;     /* 1: gates divided by their sum over the token's candidates */
   int32_t f_shared;   /* hidden width of the always-on shared expert (0 = none) */
   int32_t dtype;      /* MOE_BF16 or MOE_F32 */
@@ -95,7 +103,8 @@ typedef struct moe_config {
 /* Derived sizes of a config (host values). */
 typedef struct moe_sizes_t {
   int32_t kc;          /* candidate slots per token */
-  int32_t capacity;    /* C (capacity drop), c (expert choice) or T (token choice) */
+  int32_t capacity;    /* C (capacity drop), a device's capacity (device-level drop),
+                          c (expert choice) or T (token choice) */
   int64_t rows_max;    /* upper bound of P: row capacity of xp/op/row_token/row_gate */
   size_t  workspace;   /* bytes moe_layer_forward needs */
   size_t  ffn_workspace; /* bytes moe_expert_ffn needs for rows_max rows */
@@ -174,7 +183,11 @@ int moe_route(const moe_config* cfg, const void* x, const void* W_router, const 
  * and drops the rest. Under expert choice every token is a candidate of every
  * expert with gate p[t, e] and exactly c = min(T, floor(k*T/N)) are kept
  * ("MoE vs MoT", section "Mixture of Tokens"). Under token choice nothing is
- * dropped and only the ranks below are produced.
+ * dropped and only the ranks below are produced. Under MOE_CAPACITY_DROP_DEVICE
+ * ("Capacity-Aware Inference", section 2 (3)) the candidates of the experts of
+ * one device group compete for the device's capacity (moe_sizes().capacity):
+ * the highest gates are kept, ties to the lower token and then to the lower
+ * candidate slot; an expert may keep more than C while the device has room.
  *
  *   cand_idx  [T, kc] int32 (ignored under expert choice)
  *   cand_gate [T, kc] fp32

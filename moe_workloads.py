@@ -32,6 +32,7 @@ import torch
 TOKEN_CHOICE = "token_choice"
 EXPERT_CHOICE = "expert_choice"
 CAPACITY_DROP = "capacity_drop"
+CAPACITY_DROP_DEVICE = "capacity_drop_device"
 
 
 @dataclasses.dataclass(frozen=True)
@@ -65,6 +66,8 @@ class Workload:
              f"mode={self.mode} dtype={self.dtype}")
         if self.mode == CAPACITY_DROP:
             s += f" gamma={self.gamma}"
+        if self.mode == CAPACITY_DROP_DEVICE:
+            s += f" gamma={self.gamma} device={self.group_size} experts"
         if self.m:
             s += f" expanded m={self.m} group={self.group_size}"
         if self.renorm:
@@ -99,8 +102,15 @@ def fine_expanded() -> Workload:
     return FINE_BF16.replace(name="finegrained_bf16_expanded", m=4, group_size=8)
 
 
+def fine_device() -> Workload:
+    """The fine-grained layer with device-level capacity: 8 devices of 8
+    experts, each holding 8 x 960 = 7680 candidates."""
+    return FINE_BF16.replace(name="finegrained_bf16_device", mode=CAPACITY_DROP_DEVICE,
+                             group_size=8)
+
+
 ALL = {w.name: w for w in (TINY_F32, EC_BF16, MIXTRAL_BF16, mixtral(1.0), mixtral(1.5),
-                           FINE_BF16, fine_expanded(), DECODE_BF16)}
+                           FINE_BF16, fine_expanded(), fine_device(), DECODE_BF16)}
 
 
 def zipf_log_probs(N: int, s: float) -> np.ndarray:

@@ -30,6 +30,7 @@ MOE_ERR_DEVICE_BOUNDS = -8
 MOE_TOKEN_CHOICE = 0
 MOE_EXPERT_CHOICE = 1
 MOE_CAPACITY_DROP = 2
+MOE_CAPACITY_DROP_DEVICE = 3
 MOE_F32 = 0
 MOE_BF16 = 1
 MOE_LOGITS_GIVEN = 1
@@ -38,7 +39,7 @@ MOE_CTRL_BYTES = 1024
 MOE_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 MODES = {"token_choice": MOE_TOKEN_CHOICE, "expert_choice": MOE_EXPERT_CHOICE,
-         "capacity_drop": MOE_CAPACITY_DROP}
+         "capacity_drop": MOE_CAPACITY_DROP, "capacity_drop_device": MOE_CAPACITY_DROP_DEVICE}
 DTYPES = {"f32": MOE_F32, "bf16": MOE_BF16}
 
 

@@ -90,11 +90,12 @@ cudaError_t launch_stats_final(const int32_t* demand, const int32_t* kept,
                                double* stats, cudaStream_t s);
 
 // Per-expert selection (token choice: rank only; capacity drop: top-cap by
-// gate; expert choice: top-cap tokens by score). With st.stats set, the last
-// block to finish also writes the load statistics (counter: the control
+// gate; expert choice: top-cap tokens by score; group_size > 0: the experts of
+// each group of group_size share the capacity cap). With st.stats set, the
+// last block to finish also writes the load statistics (counter: the control
 // block's select counter).
 cudaError_t launch_select(const int32_t* cand_idx, const float* cand_gate, int T, int kc, int N,
-                          int expert_choice, int cap, int32_t* slot, uint8_t* keep,
+                          int expert_choice, int cap, int group_size, int32_t* slot, uint8_t* keep,
                           int32_t* demand, int32_t* kept, const StatsArgs& st,
                           uint32_t* counter, cudaStream_t s);
 int select_max_tokens();

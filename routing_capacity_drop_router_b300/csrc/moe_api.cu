@@ -41,7 +41,8 @@ __global__ void clear_ctrl_kernel(int32_t* ctrl) {
 
 struct Derived {
   int kc = 0;
-  int cap = 0;            // C, c or T
+  int cap = 0;            // C, c, a device's C or T
+  int device_group = 0;   // experts sharing one capacity (device-level drop), else 0
   int64_t rows_max = 0;
   int sx = 0;             // bytes per activation element
   bool ec = false;
@@ -59,12 +60,15 @@ bool have(const void* p, int64_t count) { return p != nullptr || count == 0; }
 int validate(const moe_config* c, Derived* dv) {
   if (!c) return MOE_ERR_NULL;
   if (c->T < 0 || c->d <= 0 || c->N <= 0 || c->f <= 0 || c->k <= 0) return MOE_ERR_SHAPE;
-  if (c->mode != MOE_TOKEN_CHOICE && c->mode != MOE_EXPERT_CHOICE && c->mode != MOE_CAPACITY_DROP)
+  if (c->mode != MOE_TOKEN_CHOICE && c->mode != MOE_EXPERT_CHOICE && c->mode != MOE_CAPACITY_DROP &&
+      c->mode != MOE_CAPACITY_DROP_DEVICE)
     return MOE_ERR_SHAPE;
+  const bool device_drop = c->mode == MOE_CAPACITY_DROP_DEVICE;
   if (c->dtype != MOE_BF16 && c->dtype != MOE_F32) return MOE_ERR_SHAPE;
   if (c->k > c->N || c->m < 0 || c->f_shared < 0) return MOE_ERR_SHAPE;
   if (std::isnan(c->gamma) || c->gamma < 0) return MOE_ERR_SHAPE;
-  if (c->m > 0 && (c->group_size <= 0 || c->N % c->group_size != 0)) return MOE_ERR_SHAPE;
+  if ((c->m > 0 || device_drop) && (c->group_size <= 0 || c->N % c->group_size != 0))
+    return MOE_ERR_SHAPE;
   if (c->N > kMaxN) return MOE_ERR_UNSUPPORTED;
   if (c->T > select_max_tokens()) return MOE_ERR_UNSUPPORTED;
   const bool ec = c->mode == MOE_EXPERT_CHOICE;
@@ -83,6 +87,20 @@ int validate(const moe_config* c, Derived* dv) {
   if (ec) {
     d.cap = static_cast<int>(std::min<int64_t>(T, (static_cast<int64_t>(c->k) * T) / N));
     d.rows_max = N * d.cap;
+  } else if (device_drop) {
+    // a device of group_size experts holds the sum of their capacities
+    const int64_t gs = c->group_size;
+    const int64_t most = T * std::min<int64_t>(d.kc, gs);
+    int64_t cap = most;
+    if (!std::isinf(c->gamma)) {
+      const double nbar =
+          static_cast<double>(static_cast<int64_t>(c->k) * T) / static_cast<double>(N);
+      const double cf = std::floor(c->gamma * nbar * static_cast<double>(gs));
+      cap = cf >= static_cast<double>(most) ? most : static_cast<int64_t>(cf);
+    }
+    d.cap = static_cast<int>(cap);
+    d.device_group = static_cast<int>(gs);
+    d.rows_max = std::min<int64_t>(T * d.kc, (N / gs) * cap);
   } else if (c->mode == MOE_CAPACITY_DROP && !std::isinf(c->gamma)) {
     const double nbar = static_cast<double>(static_cast<int64_t>(c->k) * T) / static_cast<double>(N);
     const double cf = std::floor(c->gamma * nbar);
@@ -325,7 +343,7 @@ int moe_capacity_drop(const moe_config* cfg, const int32_t* cand_idx, const floa
   const int64_t T = cfg->T;
   if (!have(cand_gate, T) || !have(slot, T) || !demand || !kept || (!d.ec && !have(cand_idx, T)))
     return MOE_ERR_NULL;
-  return status_from(launch_select(cand_idx, cand_gate, cfg->T, d.kc, cfg->N, d.ec ? 1 : 0, d.cap,
+  return status_from(launch_select(cand_idx, cand_gate, cfg->T, d.kc, cfg->N, d.ec ? 1 : 0, d.cap, d.device_group,
                                    slot, keep, demand, kept, StatsArgs{}, nullptr,
                                    as_stream(stream)));
 }
@@ -482,7 +500,7 @@ int moe_layer_forward(const moe_config* cfg, const void* x, const void* W_router
   sa.colsum = colsum;
   sa.rows = colsum_rows;
   sa.stats = stats;
-  if (launch_select(cand_idx, cand_gate, c.T, d.kc, c.N, d.ec ? 1 : 0, d.cap, slot, keep, demand,
+  if (launch_select(cand_idx, cand_gate, c.T, d.kc, c.N, d.ec ? 1 : 0, d.cap, d.device_group, slot, keep, demand,
                     kept, sa, reinterpret_cast<uint32_t*>(ctrl + kCtrlSelectCounter),
                     s) != cudaSuccess ||
       !tr.mark(1))

@@ -15,6 +15,13 @@
 //  3. an ordered pass writes each candidate's rank among the kept (ascending
 //     token) or -1;
 //  4. optionally, the last CTA to finish writes the layer's load statistics.
+//
+// Device-level capacity ("Capacity-Aware Inference", section 2 (3)): the
+// experts of a device, a group of group_size consecutive experts, share one
+// capacity. Every CTA of the group finds the group's threshold key and the
+// last kept candidate among those equal to it (in (token, slot) order) by the
+// same radix passes, streamed from the candidate table instead of its own
+// list, then keeps its own candidates above that boundary.
 // Keys are distinct up to ties of equal gates, and ties are settled by list
 // (token) order, so the kept set is unique and independent of thread timing.
 #include <cuda_runtime.h>
@@ -54,17 +61,53 @@ __device__ __forceinline__ int warp_exclusive_offset(int warp_total, int* warp_s
   return excl;
 }
 
+// Warp 0: given a 256-bin histogram and `need` (>= 1) keys still to place,
+// find the bin that holds the need-th largest key and how many of the keys to
+// place fall in it (s_bin, s_need).
+__device__ __forceinline__ void radix_pick(const unsigned* hist, int need, int* s_bin, int* s_need) {
+  const int lane = threadIdx.x & 31;
+  // lane owns bins [8*lane, 8*lane + 8); walk down from bin 255
+  unsigned c[8], sum = 0u;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    c[q] = hist[8 * lane + q];
+    sum += c[q];
+  }
+  unsigned suf = sum;  // inclusive suffix over lanes >= lane
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned v = __shfl_down_sync(0xffffffffu, suf, o);
+    if (lane + o < 32) suf += v;
+  }
+  const unsigned above = suf - sum;  // keys in bins of higher lanes
+  const bool hit = above < static_cast<unsigned>(need) && static_cast<unsigned>(need) <= suf;
+  const unsigned hb = __ballot_sync(0xffffffffu, hit);
+  if (lane == __ffs(hb) - 1) {
+    unsigned cum = above;
+    int bin = 8 * lane;
+    for (int q = 7; q >= 0; --q) {
+      if (cum + c[q] >= static_cast<unsigned>(need)) {
+        bin = 8 * lane + q;
+        break;
+      }
+      cum += c[q];
+    }
+    *s_bin = bin;
+    *s_need = need - static_cast<int>(cum);
+  }
+}
+
 __global__ void __launch_bounds__(kSelThreads) select_kernel(
     const int32_t* __restrict__ cand_idx, const float* __restrict__ cand_gate, int T, int kc,
-    int N, int expert_choice, int cap, int32_t* __restrict__ slot, uint8_t* __restrict__ keep,
-    int32_t* __restrict__ demand, int32_t* __restrict__ kept, const StatsArgs st,
-    uint32_t* __restrict__ counter) {
+    int N, int expert_choice, int cap, int group_size, int32_t* __restrict__ slot,
+    uint8_t* __restrict__ keep, int32_t* __restrict__ demand, int32_t* __restrict__ kept,
+    const StatsArgs st, uint32_t* __restrict__ counter) {
   extern __shared__ __align__(16) unsigned char sel_smem[];
   int32_t* lflat = reinterpret_cast<int32_t*>(sel_smem);
   uint32_t* lkey = reinterpret_cast<uint32_t*>(lflat + T);
   __shared__ int warp_sums[32];
   __shared__ unsigned hist[256];
-  __shared__ int s_bin, s_need, s_last;
+  __shared__ int s_bin, s_need, s_last, s_bound, s_fits;
 
   const int e = blockIdx.x;
   const int lane = threadIdx.x & 31;
@@ -141,8 +184,128 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
   __syncthreads();
   const int n_all = n;  // candidates counted, reported as demand
   if (n > T) n = T;
+  int k_e = n < cap ? n : (cap > 0 ? cap : 0);  // kept by expert e
 
-  if (n <= cap) {
+  if (group_size > 0) {
+    // ---- device-level capacity: threshold of the whole group ----
+    const int lo = (e / group_size) * group_size, hi = lo + group_size;
+    const int total = T * kc;
+    uint32_t prefix = 0u, pmask = 0u;
+    int need = cap;
+    bool all_kept = false;
+    if (cap > 0) {
+      for (int shift = 24; shift >= 0; shift -= 8) {
+        for (int b = threadIdx.x; b < 256; b += blockDim.x) hist[b] = 0u;
+        __syncthreads();
+        for (int i0 = 0; i0 < total; i0 += blockDim.x * 4) {  // uniform trip count
+          int ce[4];
+          float gv[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int i = i0 + j * static_cast<int>(blockDim.x) + static_cast<int>(threadIdx.x);
+            ce[j] = i < total ? cand_idx[i] : -1;
+            gv[j] = i < total ? cand_gate[i] : 0.f;
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            int bin = -1;
+            if (ce[j] >= lo && ce[j] < hi) {
+              const uint32_t kk = order_key(gv[j]);
+              if ((kk & pmask) == prefix) bin = static_cast<int>((kk >> shift) & 255u);
+            }
+            const unsigned peers = __match_any_sync(0xffffffffu, bin);
+            if (bin >= 0 && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+          }
+        }
+        __syncthreads();
+        if (shift == 24) {  // the group's demand: everything fits?
+          if (threadIdx.x < 32) {
+            unsigned t8 = 0u;
+            for (int q = 0; q < 8; ++q) t8 += hist[8 * lane + q];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) t8 += __shfl_xor_sync(0xffffffffu, t8, o);
+            if (lane == 0) s_fits = t8 <= static_cast<unsigned>(cap);
+          }
+          __syncthreads();
+          all_kept = s_fits != 0;
+          __syncthreads();
+          if (all_kept) break;
+        }
+        if (threadIdx.x < 32) radix_pick(hist, need, &s_bin, &s_need);
+        __syncthreads();
+        prefix |= static_cast<uint32_t>(s_bin) << shift;
+        pmask |= 255u << shift;
+        need = s_need;
+        __syncthreads();
+      }
+    }
+    const uint32_t thr = prefix;
+    // the need-th candidate equal to thr in table order is the last one kept
+    if (threadIdx.x == 0) s_bound = -1;
+    __syncthreads();
+    if (cap > 0 && !all_kept && need > 0) {
+      const unsigned lt = (1u << lane) - 1u;
+      int before = 0;
+      for (int base = 0; base < total; base += kSelPass) {
+        const int w0 = base + (static_cast<int>(threadIdx.x) >> 5) * (32 * kSelRounds) + lane;
+        bool eq[kSelRounds];
+        int cnt = 0;
+#pragma unroll
+        for (int j = 0; j < kSelRounds; ++j) {
+          const int i = w0 + 32 * j;
+          const int c = i < total ? cand_idx[i] : -1;
+          const float g = i < total ? cand_gate[i] : 0.f;
+          eq[j] = c >= lo && c < hi && order_key(g) == thr;
+          cnt += __popc(__ballot_sync(0xffffffffu, eq[j]));
+        }
+        int tot;
+        int run = before + warp_exclusive_offset(cnt, warp_sums, tot);
+#pragma unroll
+        for (int j = 0; j < kSelRounds; ++j) {
+          const unsigned b = __ballot_sync(0xffffffffu, eq[j]);
+          if (eq[j] && run + __popc(b & lt) + 1 == need) s_bound = w0 + 32 * j;
+          run += __popc(b);
+        }
+        before += tot;
+        if (before >= need) break;  // uniform: every thread holds the same count
+      }
+      __syncthreads();
+    }
+    const int bound = s_bound;
+    // ordered keep pass over the own list; slot = kept candidates before it
+    const unsigned lt = (1u << lane) - 1u;
+    int k_base = 0;
+    for (int base = 0; base < n; base += kSelPass) {
+      const int w0 = base + (static_cast<int>(threadIdx.x) >> 5) * (32 * kSelRounds) + lane;
+      bool kp[kSelRounds];
+      int cnt = 0;
+#pragma unroll
+      for (int j = 0; j < kSelRounds; ++j) {
+        const int i = w0 + 32 * j;
+        bool v = false;
+        if (i < n && cap > 0) {
+          const uint32_t kk = lkey[i];
+          v = all_kept || kk > thr || (kk == thr && lflat[i] <= bound);
+        }
+        kp[j] = v;
+        cnt += __popc(__ballot_sync(0xffffffffu, v));
+      }
+      int tot;
+      int run = k_base + warp_exclusive_offset(cnt, warp_sums, tot);
+#pragma unroll
+      for (int j = 0; j < kSelRounds; ++j) {
+        const int i = w0 + 32 * j;
+        const unsigned b = __ballot_sync(0xffffffffu, kp[j]);
+        if (i < n) {
+          slot[lflat[i]] = kp[j] ? run + __popc(b & lt) : -1;
+          if (keep) keep[lflat[i]] = kp[j] ? 1 : 0;
+        }
+        run += __popc(b);
+      }
+      k_base += tot;
+    }
+    k_e = k_base;
+  } else if (n <= cap) {
     for (int i = threadIdx.x; i < n; i += blockDim.x) {
       slot[lflat[i]] = i;
       if (keep) keep[lflat[i]] = 1;
@@ -168,37 +331,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
           if (bin >= 0 && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
         }
         __syncthreads();
-        if (threadIdx.x < 32) {
-          // lane owns bins [8*lane, 8*lane + 8); walk down from bin 255
-          unsigned c[8], sum = 0u;
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            c[q] = hist[8 * lane + q];
-            sum += c[q];
-          }
-          unsigned suf = sum;  // inclusive suffix over lanes >= lane
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const unsigned v = __shfl_down_sync(0xffffffffu, suf, o);
-            if (lane + o < 32) suf += v;
-          }
-          const unsigned above = suf - sum;  // keys in bins of higher lanes
-          const bool hit = above < static_cast<unsigned>(need) && static_cast<unsigned>(need) <= suf;
-          const unsigned hb = __ballot_sync(0xffffffffu, hit);
-          if (lane == __ffs(hb) - 1) {
-            unsigned cum = above;
-            int bin = 8 * lane;
-            for (int q = 7; q >= 0; --q) {
-              if (cum + c[q] >= static_cast<unsigned>(need)) {
-                bin = 8 * lane + q;
-                break;
-              }
-              cum += c[q];
-            }
-            s_bin = bin;
-            s_need = need - static_cast<int>(cum);
-          }
-        }
+        if (threadIdx.x < 32) radix_pick(hist, need, &s_bin, &s_need);
         __syncthreads();
         prefix |= static_cast<uint32_t>(s_bin) << shift;
         pmask |= 255u << shift;
@@ -256,7 +389,6 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
     }
   }
   if (threadIdx.x == 0) {
-    const int k_e = n < cap ? n : (cap > 0 ? cap : 0);
     // expert choice drops nothing: an expert's demand is the c tokens it takes
     demand[e] = expert_choice ? k_e : n_all;
     kept[e] = k_e;
@@ -284,7 +416,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
 int select_max_tokens() { return kSelMaxTokens; }
 
 cudaError_t launch_select(const int32_t* cand_idx, const float* cand_gate, int T, int kc, int N,
-                          int expert_choice, int cap, int32_t* slot, uint8_t* keep,
+                          int expert_choice, int cap, int group_size, int32_t* slot, uint8_t* keep,
                           int32_t* demand, int32_t* kept, const StatsArgs& st, uint32_t* counter,
                           cudaStream_t s) {
   if (st.stats && !counter) return cudaErrorInvalidValue;
@@ -301,7 +433,7 @@ cudaError_t launch_select(const int32_t* cand_idx, const float* cand_gate, int T
     attr_set[dev] = true;
   }
   return launch_pdl(select_kernel, N, kSelThreads, smem, s, cand_idx, cand_gate, T, kc, N,
-                    expert_choice, cap, slot, keep, demand, kept, st, counter);
+                    expert_choice, cap, group_size, slot, keep, demand, kept, st, counter);
 }
 
 }  // namespace moe

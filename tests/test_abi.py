@@ -48,9 +48,32 @@ def test_sizes_follow_capacity_formulas(w):
         C = O.capacity(w.gamma, w.k, w.T, w.N)
         assert (s.kc, s.capacity) == (w.k + w.m, C)
         assert s.rows_max == min(w.T * (w.k + w.m), w.N * C)
+    elif w.mode == W.CAPACITY_DROP_DEVICE:
+        kc = w.k + w.m
+        C = O.device_capacity(w.gamma, w.k, w.T, w.N, w.group_size, kc)
+        assert (s.kc, s.capacity) == (kc, C)
+        assert s.rows_max == min(w.T * kc, (w.N // w.group_size) * C)
     else:
         assert (s.kc, s.capacity, s.rows_max) == (w.k + w.m, w.T, w.T * (w.k + w.m))
     assert s.workspace > 0 and M.workspace_size(M.config_from_workload(w)) == s.workspace
+
+
+@pytest.mark.parametrize("gamma", [0.0, 0.7, 1.0, 1.25, 3.0, math.inf])
+@pytest.mark.parametrize("gs", [1, 2, 4, 8])
+def test_device_capacity_matches_oracle(gamma, gs):
+    w = W.Workload("dev", T=1000, d=64, N=8, f=64, k=3, mode=W.CAPACITY_DROP_DEVICE,
+                   gamma=gamma, group_size=gs, m=1)
+    s = M.sizes(M.config_from_workload(w))
+    assert s.capacity == O.device_capacity(gamma, 3, 1000, 8, gs, 4)
+
+
+def test_device_drop_needs_a_group_that_divides_N():
+    for gs in (0, 3, 16):
+        cfg = M.make_config(T=64, d=64, N=8, f=64, k=2, mode="capacity_drop_device", gamma=1.0,
+                            group_size=gs)
+        with pytest.raises(M.MoeError) as ei:
+            M.sizes(cfg)
+        assert ei.value.status == M.MOE_ERR_SHAPE
 
 
 def test_workload_capacities_match_the_pages_formulas():

@@ -26,6 +26,8 @@ SMALL = [
                gamma=1.25, m=2, group_size=4, f_shared=192, zipf_s=1.0),
     W.Workload("small_f32", T=300, d=64, N=4, f=96, k=2, dtype="f32", mode=W.CAPACITY_DROP,
                gamma=1.0),
+    W.Workload("small_device_shared", T=500, d=128, N=16, f=128, k=3,
+               mode=W.CAPACITY_DROP_DEVICE, gamma=1.0, group_size=4, f_shared=192, zipf_s=1.0),
 ]
 
 

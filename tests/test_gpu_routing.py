@@ -46,6 +46,19 @@ SMALL = [
     W.Workload("one_expert", T=300, d=64, N=1, f=64, k=1),
     W.Workload("many_experts", T=513, d=64, N=256, f=64, k=8, mode=W.CAPACITY_DROP, gamma=1.0),
     W.Workload("ec_many_experts", T=300, d=64, N=64, f=64, k=2, mode=W.EXPERT_CHOICE),
+    # device-level capacity ("Capacity-Aware Inference", section 2 (3))
+    W.Workload("device_ties", T=1000, d=64, N=16, f=64, k=4, mode=W.CAPACITY_DROP_DEVICE,
+               gamma=1.0, group_size=4),
+    W.Workload("device_expanded_renorm", T=1001, d=64, N=32, f=64, k=3,
+               mode=W.CAPACITY_DROP_DEVICE, gamma=0.8, m=3, group_size=8, renorm=True),
+    W.Workload("device_one_expert_each", T=777, d=64, N=8, f=64, k=2,
+               mode=W.CAPACITY_DROP_DEVICE, gamma=0.75, group_size=1),
+    W.Workload("device_single_group", T=513, d=64, N=16, f=64, k=4, mode=W.CAPACITY_DROP_DEVICE,
+               gamma=0.5, group_size=16),
+    W.Workload("device_zero_capacity", T=100, d=64, N=8, f=64, k=2, mode=W.CAPACITY_DROP_DEVICE,
+               gamma=0.0, group_size=4),
+    W.Workload("device_max_tokens", T=24576, d=64, N=64, f=64, k=8, mode=W.CAPACITY_DROP_DEVICE,
+               gamma=1.0, group_size=8),
 ]
 
 
