@@ -18,10 +18,14 @@
 //
 // Device-level capacity ("Capacity-Aware Inference", section 2 (3)): the
 // experts of a device, a group of group_size consecutive experts, share one
-// capacity. Every CTA of the group finds the group's threshold key and the
-// last kept candidate among those equal to it (in (token, slot) order) by the
-// same radix passes, streamed from the candidate table instead of its own
-// list, then keeps its own candidates above that boundary.
+// capacity. With group_size <= 16 the group's CTAs form a thread-block
+// cluster: every radix pass sums the CTAs' histograms of their own lists
+// through distributed shared memory, and a candidate equal to the threshold
+// key learns its rank among the group's equal candidates in (token, slot)
+// order by binary searches in the other CTAs' tie lists. Without a cluster
+// (larger groups, or more than kTieMax ties in one CTA) every CTA of the group
+// streams the candidate table through the same radix passes and finds the
+// last kept equal candidate by an ordered scan of the table.
 // Keys are distinct up to ties of equal gates, and ties are settled by list
 // (token) order, so the kept set is unique and independent of thread timing.
 #include <cuda_runtime.h>
@@ -29,14 +33,28 @@
 #include "device_common.cuh"
 #include "internal.h"
 #include "stats_final.cuh"
+#include "tc_ptx.cuh"
 
 namespace moe {
 namespace {
+
+using tc::cluster_rank;
+using tc::cluster_sync;
+using tc::map_to_rank;
+using tc::smem_u32;
 
 constexpr int kSelThreads = 1024;
 constexpr int kSelRounds = 8;             // 32-entry rounds per warp per pass
 constexpr int kSelPass = kSelThreads * kSelRounds;  // list entries per block pass
 constexpr int kSelMaxTokens = 24576;      // 8 bytes of shared memory per list entry
+constexpr int kTieMax = 4096;             // tie list of a clustered device group (4 bytes each)
+constexpr int kMaxClusterGroup = 16;
+
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
 
 // Exclusive prefix over warps of each warp's total (lane-uniform input);
 // `total` receives the block's sum. Contains __syncthreads: call uniformly.
@@ -99,7 +117,7 @@ __device__ __forceinline__ void radix_pick(const unsigned* hist, int need, int* 
 
 __global__ void __launch_bounds__(kSelThreads) select_kernel(
     const int32_t* __restrict__ cand_idx, const float* __restrict__ cand_gate, int T, int kc,
-    int N, int expert_choice, int cap, int group_size, int32_t* __restrict__ slot,
+    int N, int expert_choice, int cap, int group_size, int clustered, int32_t* __restrict__ slot,
     uint8_t* __restrict__ keep, int32_t* __restrict__ demand, int32_t* __restrict__ kept,
     const StatsArgs st, uint32_t* __restrict__ counter) {
   extern __shared__ __align__(16) unsigned char sel_smem[];
@@ -107,7 +125,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
   uint32_t* lkey = reinterpret_cast<uint32_t*>(lflat + T);
   __shared__ int warp_sums[32];
   __shared__ unsigned hist[256];
-  __shared__ int s_bin, s_need, s_last, s_bound, s_fits;
+  __shared__ unsigned hsum[256];
+  __shared__ int s_bin, s_need, s_last, s_bound, s_fits, s_count, s_over;
 
   const int e = blockIdx.x;
   const int lane = threadIdx.x & 31;
@@ -193,45 +212,84 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
     uint32_t prefix = 0u, pmask = 0u;
     int need = cap;
     bool all_kept = false;
-    if (cap > 0) {
+    if (cap > 0 && clustered) {  // the group's demand: everything fits?
+      if (threadIdx.x == 0) s_count = n;
+      __syncthreads();
+      cluster_sync();
+      if (threadIdx.x == 0) {
+        unsigned sum = 0u;
+        for (int r = 0; r < group_size; ++r)
+          sum += ld_cluster_u32(map_to_rank(smem_u32(&s_count), r));
+        s_fits = sum <= static_cast<unsigned>(cap);
+      }
+      __syncthreads();
+      all_kept = s_fits != 0;
+      cluster_sync();  // s_count is reused below
+    }
+    if (cap > 0 && !all_kept) {
       for (int shift = 24; shift >= 0; shift -= 8) {
         for (int b = threadIdx.x; b < 256; b += blockDim.x) hist[b] = 0u;
         __syncthreads();
-        for (int i0 = 0; i0 < total; i0 += blockDim.x * 4) {  // uniform trip count
-          int ce[4];
-          float gv[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int i = i0 + j * static_cast<int>(blockDim.x) + static_cast<int>(threadIdx.x);
-            ce[j] = i < total ? cand_idx[i] : -1;
-            gv[j] = i < total ? cand_gate[i] : 0.f;
-          }
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
+        if (clustered) {  // this CTA's own list
+          for (int i0 = 0; i0 < n; i0 += blockDim.x) {  // uniform trip count per warp
+            const int i = i0 + static_cast<int>(threadIdx.x);
             int bin = -1;
-            if (ce[j] >= lo && ce[j] < hi) {
-              const uint32_t kk = order_key(gv[j]);
+            if (i < n) {
+              const uint32_t kk = lkey[i];
               if ((kk & pmask) == prefix) bin = static_cast<int>((kk >> shift) & 255u);
             }
             const unsigned peers = __match_any_sync(0xffffffffu, bin);
             if (bin >= 0 && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
           }
-        }
-        __syncthreads();
-        if (shift == 24) {  // the group's demand: everything fits?
-          if (threadIdx.x < 32) {
-            unsigned t8 = 0u;
-            for (int q = 0; q < 8; ++q) t8 += hist[8 * lane + q];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) t8 += __shfl_xor_sync(0xffffffffu, t8, o);
-            if (lane == 0) s_fits = t8 <= static_cast<unsigned>(cap);
+          __syncthreads();
+          cluster_sync();  // every CTA's histogram is complete
+          if (threadIdx.x < 256) {
+            unsigned sum = 0u;
+            for (int r = 0; r < group_size; ++r)
+              sum += ld_cluster_u32(map_to_rank(smem_u32(&hist[threadIdx.x]), r));
+            hsum[threadIdx.x] = sum;
           }
           __syncthreads();
-          all_kept = s_fits != 0;
+          if (threadIdx.x < 32) radix_pick(hsum, need, &s_bin, &s_need);
           __syncthreads();
-          if (all_kept) break;
+          cluster_sync();  // the peers have read this CTA's histogram
+        } else {  // the whole candidate table
+          for (int i0 = 0; i0 < total; i0 += blockDim.x * 4) {  // uniform trip count
+            int ce[4];
+            float gv[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int i = i0 + j * static_cast<int>(blockDim.x) + static_cast<int>(threadIdx.x);
+              ce[j] = i < total ? cand_idx[i] : -1;
+              gv[j] = i < total ? cand_gate[i] : 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              int bin = -1;
+              if (ce[j] >= lo && ce[j] < hi) {
+                const uint32_t kk = order_key(gv[j]);
+                if ((kk & pmask) == prefix) bin = static_cast<int>((kk >> shift) & 255u);
+              }
+              const unsigned peers = __match_any_sync(0xffffffffu, bin);
+              if (bin >= 0 && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+            }
+          }
+          __syncthreads();
+          if (shift == 24) {  // the group's demand: everything fits?
+            if (threadIdx.x < 32) {
+              unsigned t8 = 0u;
+              for (int q = 0; q < 8; ++q) t8 += hist[8 * lane + q];
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) t8 += __shfl_xor_sync(0xffffffffu, t8, o);
+              if (lane == 0) s_fits = t8 <= static_cast<unsigned>(cap);
+            }
+            __syncthreads();
+            all_kept = s_fits != 0;
+            __syncthreads();
+            if (all_kept) break;
+          }
+          if (threadIdx.x < 32) radix_pick(hist, need, &s_bin, &s_need);
         }
-        if (threadIdx.x < 32) radix_pick(hist, need, &s_bin, &s_need);
         __syncthreads();
         prefix |= static_cast<uint32_t>(s_bin) << shift;
         pmask |= 255u << shift;
@@ -240,38 +298,110 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
       }
     }
     const uint32_t thr = prefix;
-    // the need-th candidate equal to thr in table order is the last one kept
-    if (threadIdx.x == 0) s_bound = -1;
-    __syncthreads();
-    if (cap > 0 && !all_kept && need > 0) {
-      const unsigned lt = (1u << lane) - 1u;
-      int before = 0;
-      for (int base = 0; base < total; base += kSelPass) {
-        const int w0 = base + (static_cast<int>(threadIdx.x) >> 5) * (32 * kSelRounds) + lane;
-        bool eq[kSelRounds];
-        int cnt = 0;
+    // ties: of the group's candidates equal to thr, the first `need` in
+    // (token, slot) order stay; the others are marked by a zero key
+    if (cap > 0 && !all_kept) {
+      bool scan_table = !clustered;
+      if (clustered) {
+        // ordered compaction of this CTA's equal entries (list positions)
+        int32_t* ties = reinterpret_cast<int32_t*>(lkey + T);
+        const unsigned lt = (1u << lane) - 1u;
+        int n_eq = 0;
+        for (int base = 0; base < n; base += kSelPass) {
+          const int w0 = base + (static_cast<int>(threadIdx.x) >> 5) * (32 * kSelRounds) + lane;
+          bool eq[kSelRounds];
+          int cnt = 0;
 #pragma unroll
-        for (int j = 0; j < kSelRounds; ++j) {
-          const int i = w0 + 32 * j;
-          const int c = i < total ? cand_idx[i] : -1;
-          const float g = i < total ? cand_gate[i] : 0.f;
-          eq[j] = c >= lo && c < hi && order_key(g) == thr;
-          cnt += __popc(__ballot_sync(0xffffffffu, eq[j]));
-        }
-        int tot;
-        int run = before + warp_exclusive_offset(cnt, warp_sums, tot);
+          for (int j = 0; j < kSelRounds; ++j) {
+            const int i = w0 + 32 * j;
+            eq[j] = i < n && lkey[i] == thr;
+            cnt += __popc(__ballot_sync(0xffffffffu, eq[j]));
+          }
+          int tot;
+          int run = n_eq + warp_exclusive_offset(cnt, warp_sums, tot);
 #pragma unroll
-        for (int j = 0; j < kSelRounds; ++j) {
-          const unsigned b = __ballot_sync(0xffffffffu, eq[j]);
-          if (eq[j] && run + __popc(b & lt) + 1 == need) s_bound = w0 + 32 * j;
-          run += __popc(b);
+          for (int j = 0; j < kSelRounds; ++j) {
+            const unsigned b = __ballot_sync(0xffffffffu, eq[j]);
+            const int q = run + __popc(b & lt);
+            if (eq[j] && q < kTieMax) ties[q] = w0 + 32 * j;
+            run += __popc(b);
+          }
+          n_eq += tot;
         }
-        before += tot;
-        if (before >= need) break;  // uniform: every thread holds the same count
+        if (threadIdx.x == 0) s_count = n_eq;
+        __syncthreads();
+        cluster_sync();
+        if (threadIdx.x == 0) {
+          int over = 0;
+          for (int r = 0; r < group_size; ++r)
+            over |= static_cast<int>(ld_cluster_u32(map_to_rank(smem_u32(&s_count), r))) > kTieMax;
+          s_over = over;
+        }
+        __syncthreads();
+        scan_table = s_over != 0;
+        if (!scan_table) {
+          const uint32_t me = cluster_rank();
+          for (int q = threadIdx.x; q < n_eq; q += blockDim.x) {
+            const int pos = ties[q];
+            const int f = lflat[pos];
+            int rank = q;  // equal entries of this CTA before it
+            for (int r = 0; r < group_size; ++r) {
+              if (r == static_cast<int>(me)) continue;
+              const int n_r = static_cast<int>(ld_cluster_u32(map_to_rank(smem_u32(&s_count), r)));
+              int a = 0, b = n_r;  // entries of CTA r with flat index below f
+              while (a < b) {
+                const int mid = (a + b) >> 1;
+                const uint32_t pr = ld_cluster_u32(map_to_rank(smem_u32(&ties[mid]), r));
+                const int fr = static_cast<int>(
+                    ld_cluster_u32(map_to_rank(smem_u32(&lflat[pr]), r)));
+                if (fr < f) a = mid + 1;
+                else b = mid;
+              }
+              rank += a;
+            }
+            if (rank >= need) lkey[pos] = 0u;  // below every gate's key
+          }
+        }
+        // the peers have finished reading this CTA's lists
+        __syncthreads();
+        cluster_sync();
       }
-      __syncthreads();
+      if (scan_table) {
+        // the need-th candidate equal to thr in table order is the last one kept
+        if (threadIdx.x == 0) s_bound = -1;
+        __syncthreads();
+        const unsigned lt = (1u << lane) - 1u;
+        int before = 0;
+        for (int base = 0; base < total; base += kSelPass) {
+          const int w0 = base + (static_cast<int>(threadIdx.x) >> 5) * (32 * kSelRounds) + lane;
+          bool eq[kSelRounds];
+          int cnt = 0;
+#pragma unroll
+          for (int j = 0; j < kSelRounds; ++j) {
+            const int i = w0 + 32 * j;
+            const int c = i < total ? cand_idx[i] : -1;
+            const float g = i < total ? cand_gate[i] : 0.f;
+            eq[j] = c >= lo && c < hi && order_key(g) == thr;
+            cnt += __popc(__ballot_sync(0xffffffffu, eq[j]));
+          }
+          int tot;
+          int run = before + warp_exclusive_offset(cnt, warp_sums, tot);
+#pragma unroll
+          for (int j = 0; j < kSelRounds; ++j) {
+            const unsigned b = __ballot_sync(0xffffffffu, eq[j]);
+            if (eq[j] && run + __popc(b & lt) + 1 == need) s_bound = w0 + 32 * j;
+            run += __popc(b);
+          }
+          before += tot;
+          if (before >= need) break;  // uniform: every thread holds the same count
+        }
+        __syncthreads();
+        const int bound = s_bound;
+        for (int i = threadIdx.x; i < n; i += blockDim.x)
+          if (lkey[i] == thr && lflat[i] > bound) lkey[i] = 0u;
+        __syncthreads();
+      }
     }
-    const int bound = s_bound;
     // ordered keep pass over the own list; slot = kept candidates before it
     const unsigned lt = (1u << lane) - 1u;
     int k_base = 0;
@@ -285,7 +415,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
         bool v = false;
         if (i < n && cap > 0) {
           const uint32_t kk = lkey[i];
-          v = all_kept || kk > thr || (kk == thr && lflat[i] <= bound);
+          v = all_kept || kk >= thr;
         }
         kp[j] = v;
         cnt += __popc(__ballot_sync(0xffffffffu, v));
@@ -415,12 +545,47 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
 
 int select_max_tokens() { return kSelMaxTokens; }
 
+namespace {
+
+constexpr size_t kSelSmemMax = static_cast<size_t>(kSelMaxTokens) * 8 + kTieMax * 4;
+
+// Whether a device group of `gs` selection CTAs can run as one cluster.
+bool group_cluster_ok(int dev, int gs) {
+  static int cached[64][kMaxClusterGroup + 1] = {};  // 0 unknown, 1 yes, 2 no
+  if (dev < 0 || dev >= 64 || gs < 1 || gs > kMaxClusterGroup) return false;
+  if (cached[dev][gs] == 0) {
+    bool ok = true;
+    if (gs > 8)
+      ok = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+           cudaSuccess;
+    int n = 0;
+    if (ok) {
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = static_cast<unsigned>(gs);
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned>(gs));
+      cfg.blockDim = dim3(kSelThreads);
+      cfg.dynamicSmemBytes = kSelSmemMax;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      ok = cudaOccupancyMaxActiveClusters(&n, select_kernel, &cfg) == cudaSuccess && n >= 1;
+    }
+    if (!ok) (void)cudaGetLastError();
+    cached[dev][gs] = ok ? 1 : 2;
+  }
+  return cached[dev][gs] == 1;
+}
+
+}  // namespace
+
 cudaError_t launch_select(const int32_t* cand_idx, const float* cand_gate, int T, int kc, int N,
                           int expert_choice, int cap, int group_size, int32_t* slot, uint8_t* keep,
                           int32_t* demand, int32_t* kept, const StatsArgs& st, uint32_t* counter,
                           cudaStream_t s) {
   if (st.stats && !counter) return cudaErrorInvalidValue;
-  const size_t smem = static_cast<size_t>(T) * 8;
   static bool attr_set[64] = {};  // per device; setting it twice is harmless
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -428,12 +593,28 @@ cudaError_t launch_select(const int32_t* cand_idx, const float* cand_gate, int T
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
     err = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kSelMaxTokens * 8);
+                               static_cast<int>(kSelSmemMax));
     if (err != cudaSuccess) return err;
     attr_set[dev] = true;
   }
-  return launch_pdl(select_kernel, N, kSelThreads, smem, s, cand_idx, cand_gate, T, kc, N,
-                    expert_choice, cap, group_size, slot, keep, demand, kept, st, counter);
+  const int clustered = group_size > 0 && group_cluster_ok(dev, group_size) ? 1 : 0;
+  const size_t smem = static_cast<size_t>(T) * 8 + (clustered ? kTieMax * 4 : 0);
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = clustered ? static_cast<unsigned>(group_size) : 1u;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(N));
+  cfg.blockDim = dim3(kSelThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = clustered ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, select_kernel, cand_idx, cand_gate, T, kc, N, expert_choice, cap,
+                            group_size, clustered, slot, keep, demand, kept, st, counter);
 }
 
 }  // namespace moe

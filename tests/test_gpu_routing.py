@@ -59,6 +59,8 @@ SMALL = [
                gamma=0.0, group_size=4),
     W.Workload("device_max_tokens", T=24576, d=64, N=64, f=64, k=8, mode=W.CAPACITY_DROP_DEVICE,
                gamma=1.0, group_size=8),
+    W.Workload("device_group_of_32", T=3000, d=64, N=64, f=64, k=4, mode=W.CAPACITY_DROP_DEVICE,
+               gamma=0.8, group_size=32),  # larger than a cluster: table passes
 ]
 
 
@@ -77,6 +79,19 @@ def test_all_equal_logits_and_signed_zeros():
     g = G.gpu_routing(w, L)
     G.compare_routing(w, g, L.numpy())
     assert (g["cand_idx"] == np.array([0, 1, 2])).all()
+
+
+@pytest.mark.parametrize("gs", [4, 16])
+def test_device_drop_with_every_gate_equal(gs):
+    """All logits equal: every token's candidates are the lowest experts with
+    equal gates, so one device holds thousands of ties (more than a CTA's tie
+    list) and the kept set is decided by (token, slot) order alone."""
+    w = W.Workload("device_flat", T=12000, d=64, N=16, f=64, k=2, mode=W.CAPACITY_DROP_DEVICE,
+                   gamma=0.5, group_size=gs)
+    L = torch.zeros((w.T, w.N))
+    g = G.gpu_routing(w, L)
+    G.compare_routing(w, g, L.numpy())
+    assert 0 < g["keep"].sum() < w.T * 2
 
 
 def test_given_home_groups():
