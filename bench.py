@@ -566,6 +566,84 @@ def run_stage(args):
     print(json.dumps(out), flush=True)
 
 
+def run_ep_sim(args):
+    """--ep-sim: expert parallelism simulated on one GPU ("Capacity-Aware
+    Inference", section 1: under expert parallelism the layer waits for the
+    most loaded device). The experts are split into `devices` groups of
+    consecutive experts; after one routed layer step, each group's expert FFN
+    runs alone on sm_count // devices SMs (moe_expert_ffn_on_sms) and is timed
+    with CUDA events. The straggler time is the maximum over groups. The
+    all-to-all exchange and the shared expert (the same on every device) are
+    not part of the timing, and each group runs alone, so it does not share
+    HBM with the others as it would inside one GPU."""
+    import routing_capacity_drop_router_b300 as M
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    devices = args.ep_devices
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    per = sms // devices
+    inf = math.inf
+    cases = [(W.MIXTRAL_BF16, dict(mode=W.CAPACITY_DROP, gamma=g)) for g in (inf, 2.0, 1.5, 1.0)]
+    fine = W.FINE_BF16
+    cases += [(fine, dict(mode=W.CAPACITY_DROP, gamma=g)) for g in (inf, 1.5, 1.25, 1.0)]
+    cases += [(fine, dict(mode=W.CAPACITY_DROP, gamma=1.25, m=4, group_size=fine.N // devices)),
+              (fine, dict(mode=W.CAPACITY_DROP_DEVICE, gamma=1.25, group_size=fine.N // devices))]
+    rows, inputs = [], {}
+    for base, kw in cases:
+        w = base.replace(name=base.name + "_epsim", **kw)
+        if base.name not in inputs:
+            inputs.clear()
+            inp = W.make_inputs(base)
+            inputs[base.name] = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
+        d = inputs[base.name]
+        cfg = M.config_from_workload(w)
+        sz = M.sizes(cfg)
+        ws = torch.zeros(sz.workspace, dtype=torch.uint8, device=dev)
+        y = torch.empty((w.T, w.d), dtype=torch.bfloat16, device=dev)
+        M.moe_layer_forward(cfg, d["x"], d["W_r"], d["bias"], d["W1"], d["W3"], d["W2"],
+                            d.get("Ws1"), d.get("Ws3"), d.get("Ws2"), y, ws)
+        torch.cuda.synchronize()
+        v = M.moe_workspace_views(cfg, ws)
+        k0 = v.kept - ws.data_ptr()  # the per-expert kept counts live in the workspace
+        kept_h = ws[k0:k0 + 4 * w.N].view(torch.int32).cpu().numpy()
+        gs = w.N // devices
+        fws = torch.zeros(M.ffn_workspace_size(sz.rows_max, w.f, w.dtype), dtype=torch.uint8,
+                          device=dev)
+        times = []
+        for g in range(devices):
+            lo = g * gs
+            call = lambda: M.moe_expert_ffn_on_sms(
+                cfg, v.xp, v.expert_offsets + 4 * lo, gs, sz.rows_max, w.f,
+                d["W1"][lo].data_ptr(), d["W3"][lo].data_ptr(), d["W2"][lo].data_ptr(), v.op,
+                per, fws)
+            for _ in range(2):
+                call()
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.ep_reps)]
+            for a, b in evs:
+                a.record()
+                call()
+                b.record()
+            torch.cuda.synchronize()
+            times.append(statistics.median(a.elapsed_time(b) for a, b in evs))
+        if M.moe_get_device_status(fws) != M.MOE_OK:
+            raise RuntimeError("device status error in the expert-parallel simulation")
+        loads = [int(kept_h[g * gs:(g + 1) * gs].sum()) for g in range(devices)]
+        rows.append({"workload": base.name, "mode": w.mode,
+                     "gamma": None if math.isinf(w.gamma) else w.gamma, "m": w.m,
+                     "device_loads": loads,
+                     "max_over_mean_load": max(loads) / (sum(loads) / devices),
+                     "straggler_ms": max(times), "mean_device_ms": sum(times) / devices,
+                     "device_ms": [round(t, 4) for t in times]})
+        del ws, fws
+    for r in rows:  # speed-up of the straggler against the same layer without a capacity
+        ref = next(q for q in rows if q["workload"] == r["workload"] and q["gamma"] is None)
+        r["straggler_speedup_vs_no_capacity"] = ref["straggler_ms"] / r["straggler_ms"]
+    print(json.dumps({"metric": "simulated expert-parallel straggler time of the routed experts",
+                      "unit": "ms", "higher_is_better": False, "devices": devices,
+                      "sms_per_device": per, "reps": args.ep_reps, "rows": rows}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -583,9 +661,17 @@ def main():
     ap.add_argument("--kernel", choices=["route", "select", "dispatch", "combine"],
                     help="time one stage alone instead of the layer")
     ap.add_argument("--T", type=int, default=0, help="token count override for --kernel")
+    ap.add_argument("--ep-sim", action="store_true",
+                    help="simulate expert parallelism: time each device group's experts on "
+                         "its share of the SMs and report the straggler")
+    ap.add_argument("--ep-devices", type=int, default=8)
+    ap.add_argument("--ep-reps", type=int, default=10)
     args = ap.parse_args()
     if args.kernel:
         run_stage(args)
+        return
+    if args.ep_sim:
+        run_ep_sim(args)
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

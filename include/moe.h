@@ -285,6 +285,22 @@ int moe_expert_ffn_noalloc(const moe_config* cfg, const void* xp, const int32_t*
                            void* stream);
 
 /*
+ * moe_expert_ffn confined to a slice of the GPU: its two persistent GEMMs
+ * launch on at most max_sms streaming multiprocessors (bf16 only; f32 returns
+ * MOE_ERR_UNSUPPORTED). Same arguments and result as moe_expert_ffn.
+ * One call per device group, each on the SMs one device would have, times
+ * the experts as expert parallelism would run them, where the layer waits
+ * for the most loaded device ("Capacity-Aware Inference: Mitigating the
+ * Straggler Effect in MoE", section 1: the straggler sets the latency).
+ * offsets may point into a larger offsets array (row indices stay absolute
+ * in xp); W1/W3/W2 then point at the group's first expert.
+ */
+int moe_expert_ffn_on_sms(const moe_config* cfg, const void* xp, const int32_t* offsets,
+                          int32_t n_segments, int64_t rows_max, int32_t f, const void* W1,
+                          const void* W3, const void* W2, void* op, int32_t max_sms, void* ws,
+                          size_t ws_bytes, void* stream);
+
+/*
  * One grouped GEMM, out[r] = A[r] B[s] for rows r of segment s, the second
  * half of the expert FFN on its own. A [rows_max, K], B [n_segments, K, n_out],
  * out [rows_max, n_out], all dtype; K and n_out multiples of 64 (bf16).

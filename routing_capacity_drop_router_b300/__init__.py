@@ -87,6 +87,9 @@ SIGNATURES = {
                                       _VP]),
     "moe_expert_ffn_noalloc": (ctypes.c_int, [_CFG, _VP, _VP, ctypes.c_int32, ctypes.c_int64,
                                               ctypes.c_int32, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "moe_expert_ffn_on_sms": (ctypes.c_int, [_CFG, _VP, _VP, ctypes.c_int32, ctypes.c_int64,
+                                             ctypes.c_int32, _VP, _VP, _VP, _VP, ctypes.c_int32,
+                                             _VP, ctypes.c_size_t, _VP]),
     "moe_grouped_gemm": (ctypes.c_int, [ctypes.c_int32, _VP, _VP, ctypes.c_int32, ctypes.c_int64,
                                         ctypes.c_int32, ctypes.c_int32, _VP, _VP, _VP,
                                         ctypes.c_size_t, _VP]),
@@ -216,6 +219,16 @@ def moe_expert_ffn(cfg, xp, offsets, n_segments, rows_max, f, W1, W3, W2, op, ws
     _check(lib().moe_expert_ffn(ctypes.byref(cfg), _p(xp), _p(offsets), n_segments, rows_max, f,
                                 _p(W1), _p(W3), _p(W2), _p(op), _p(ws), ws.numel() * ws.element_size(),
                                 _stream(stream)), "moe_expert_ffn")
+
+
+def moe_expert_ffn_on_sms(cfg, xp, offsets, n_segments, rows_max, f, W1, W3, W2, op, max_sms, ws,
+                          stream=None) -> None:
+    """moe_expert_ffn on at most ``max_sms`` SMs (bf16). ``offsets``, ``W1``,
+    ``W3``, ``W2`` may be raw device addresses (int) into larger arrays."""
+    _check(lib().moe_expert_ffn_on_sms(ctypes.byref(cfg), _p(xp), _p(offsets), n_segments,
+                                       rows_max, f, _p(W1), _p(W3), _p(W2), _p(op), max_sms,
+                                       _p(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "moe_expert_ffn_on_sms")
 
 
 def moe_expert_ffn_noalloc(cfg, xp, offsets, n_segments, rows_max, f, W1, W3, W2, op,

@@ -479,7 +479,8 @@ cudaError_t set_smem_attr(int dev) {
 template <bool SWIGLU>
 cudaError_t launch_gemm(const CUtensorMap& mA, const CUtensorMap& mB1, const CUtensorMap& mB3,
                         const int32_t* offsets, int S, int64_t rows_max, int K, int n_out,
-                        __nv_bfloat16* o, int32_t* status, cudaStream_t s, int withhold_kb) {
+                        __nv_bfloat16* o, int32_t* status, cudaStream_t s, int withhold_kb,
+                        int max_sms) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
@@ -489,14 +490,17 @@ cudaError_t launch_gemm(const CUtensorMap& mA, const CUtensorMap& mB1, const CUt
   // batches) half of every pair tile would be padding.
   const char* env = getenv("MOE_GEMM_CTA_PAIRS");
   const bool want_pairs = env ? env[0] != '0' : rows_max >= 2LL * kBM * S;
-  const int slots = want_pairs ? pair_slots<SWIGLU>(dev) : 0;
+  int sms = device_sm_count();
+  if (max_sms > 0 && max_sms < sms) sms = max_sms;  // confined to a slice of the GPU
+  int slots = want_pairs ? pair_slots<SWIGLU>(dev) : 0;
+  if (slots > sms / 2) slots = sms / 2;
   const bool pair = slots > 0;
   const int tile_rows = pair ? 2 * kBM : kBM;
   const int tile_n = SWIGLU ? kBN / 2 : kBN;
   const long long n_tiles = (n_out + tile_n - 1) / tile_n;
   const long long m_tiles_max = (rows_max + tile_rows - 1) / tile_rows + S;
   long long units = n_tiles * m_tiles_max;
-  const long long cap = pair ? slots : device_sm_count();
+  const long long cap = pair ? slots : sms;
   if (units > cap) units = cap;
   const int rmax = rows_max > 0x7fffffff ? 0x7fffffff : static_cast<int>(rows_max);
 
@@ -526,7 +530,8 @@ cudaError_t launch_gemm(const CUtensorMap& mA, const CUtensorMap& mB1, const CUt
 cudaError_t launch_grouped_gemm_tc_bf16(const void* A, const int32_t* offsets, int S,
                                         int64_t rows_max, int K, int n_out, const void* B1,
                                         const void* B3, void* out, bool swiglu,
-                                        int32_t* status, cudaStream_t s, int withhold_kb) {
+                                        int32_t* status, cudaStream_t s, int withhold_kb,
+                                        int max_sms) {
   if (S == 0 || rows_max == 0) return cudaSuccess;
   if (S > kMaxSegments) return cudaErrorInvalidValue;
   CUtensorMap mA, mB1, mB3;
@@ -540,8 +545,10 @@ cudaError_t launch_grouped_gemm_tc_bf16(const void* A, const int32_t* offsets, i
   }
   __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
   if (swiglu)
-    return launch_gemm<true>(mA, mB1, mB3, offsets, S, rows_max, K, n_out, o, status, s, withhold_kb);
-  return launch_gemm<false>(mA, mB1, mB3, offsets, S, rows_max, K, n_out, o, status, s, withhold_kb);
+    return launch_gemm<true>(mA, mB1, mB3, offsets, S, rows_max, K, n_out, o, status, s, withhold_kb,
+                             max_sms);
+  return launch_gemm<false>(mA, mB1, mB3, offsets, S, rows_max, K, n_out, o, status, s, withhold_kb,
+                            max_sms);
 }
 
 }  // namespace moe

@@ -112,12 +112,14 @@ cudaError_t launch_grouped_gemm_simt_f32(const float* A, const int32_t* offsets,
                                          int64_t rows_max, int K, int n_out, const float* B1,
                                          const float* B3, float* out, bool swiglu,
                                          cudaStream_t s);
-// withhold_kb >= 0 (self-test only): CTA 0 announces but never loads its
-// first tile's k-block withhold_kb, so a bounded wait expires.
+// withhold_kb >= 0 (self-test only): the first tile announces but never
+// loads its k-block withhold_kb, so a bounded wait expires. max_sms > 0 caps
+// the persistent grid at that many SMs.
 cudaError_t launch_grouped_gemm_tc_bf16(const void* A, const int32_t* offsets, int S,
                                         int64_t rows_max, int K, int n_out, const void* B1,
                                         const void* B3, void* out, bool swiglu,
-                                        int32_t* status, cudaStream_t s, int withhold_kb = -1);
+                                        int32_t* status, cudaStream_t s, int withhold_kb = -1,
+                                        int max_sms = 0);
 
 // y[t] = sum_r gate_r op[r] (+ shared[t]).
 cudaError_t launch_combine(int dtype, const void* op, const float* row_gate,

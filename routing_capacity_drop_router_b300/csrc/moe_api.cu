@@ -259,13 +259,14 @@ P* at(void* ws, size_t off) {
 // status is the workspace's status word.
 int run_ffn(int dtype, const void* xp, const int32_t* offsets, int S, int64_t rows_max, int d,
             int f, const void* W1, const void* W3, const void* W2, void* hp, void* op,
-            int32_t* status, cudaStream_t s, Tracer* tr = nullptr) {
+            int32_t* status, cudaStream_t s, Tracer* tr = nullptr, int max_sms = 0) {
   cudaError_t e;
   if (dtype == MOE_BF16) {
-    e = launch_grouped_gemm_tc_bf16(xp, offsets, S, rows_max, d, f, W1, W3, hp, true, status, s);
+    e = launch_grouped_gemm_tc_bf16(xp, offsets, S, rows_max, d, f, W1, W3, hp, true, status, s, -1,
+                                    max_sms);
     if (e != cudaSuccess || (tr && !tr->mark())) return MOE_ERR_LAUNCH;
     e = launch_grouped_gemm_tc_bf16(hp, offsets, S, rows_max, f, d, W2, nullptr, op, false, status,
-                                    s);
+                                    s, -1, max_sms);
   } else {
     e = launch_grouped_gemm_simt_f32(static_cast<const float*>(xp), offsets, S, rows_max, d, f,
                                      static_cast<const float*>(W1), static_cast<const float*>(W3),
@@ -383,6 +384,26 @@ int moe_expert_ffn(const moe_config* cfg, const void* xp, const int32_t* offsets
   void* hp = static_cast<unsigned char*>(ws) + kCtrlBytes;
   return run_ffn(cfg->dtype, xp, offsets, n_segments, rows_max, cfg->d, f, W1, W3, W2, hp, op,
                  static_cast<int32_t*>(ws), as_stream(stream));
+}
+
+int moe_expert_ffn_on_sms(const moe_config* cfg, const void* xp, const int32_t* offsets,
+                          int32_t n_segments, int64_t rows_max, int32_t f, const void* W1,
+                          const void* W3, const void* W2, void* op, int32_t max_sms, void* ws,
+                          size_t ws_bytes, void* stream) {
+  if (!cfg) return MOE_ERR_NULL;
+  if (cfg->dtype != MOE_BF16) return cfg->dtype == MOE_F32 ? MOE_ERR_UNSUPPORTED : MOE_ERR_SHAPE;
+  if (max_sms <= 0) return MOE_ERR_SHAPE;
+  if (cfg->d <= 0 || f <= 0 || n_segments < 0 || rows_max < 0) return MOE_ERR_SHAPE;
+  if (cfg->d % 64 || f % 64) return MOE_ERR_SHAPE;
+  if (n_segments > kMaxN) return MOE_ERR_UNSUPPORTED;
+  if (!xp || !offsets || !W1 || !W3 || !W2 || !op || !ws) return MOE_ERR_NULL;
+  if (!aligned16(xp) || !aligned16(W1) || !aligned16(W3) || !aligned16(W2) || !aligned16(op) ||
+      !aligned16(ws))
+    return MOE_ERR_ALIGN;
+  if (ws_bytes < moe_ffn_workspace_size(rows_max, f, cfg->dtype)) return MOE_ERR_WORKSPACE;
+  void* hp = static_cast<unsigned char*>(ws) + kCtrlBytes;
+  return run_ffn(cfg->dtype, xp, offsets, n_segments, rows_max, cfg->d, f, W1, W3, W2, hp, op,
+                 static_cast<int32_t*>(ws), as_stream(stream), nullptr, max_sms);
 }
 
 int moe_grouped_gemm(int32_t dtype, const void* A, const int32_t* offsets, int32_t n_segments,

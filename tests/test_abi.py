@@ -150,6 +150,24 @@ def test_misaligned_and_small_workspace_rejected_before_any_launch():
                                 None) == M.MOE_ERR_SHAPE
 
 
+def test_expert_ffn_on_sms_host_checks():
+    lib = M.lib()
+    fake = ctypes.c_void_p(1 << 20)
+    bf = M.make_config(T=8, d=64, N=2, f=64, k=1, dtype="bf16")
+    f32 = M.make_config(T=8, d=64, N=2, f=64, k=1, dtype="f32")
+    args = [fake, fake, 2, 8, 64, fake, fake, fake, fake]
+    need = M.ffn_workspace_size(8, 64, "bf16")
+    assert lib.moe_expert_ffn_on_sms(ctypes.byref(f32), *args, 4, fake, need, None) == \
+        M.MOE_ERR_UNSUPPORTED
+    assert lib.moe_expert_ffn_on_sms(ctypes.byref(bf), *args, 0, fake, need, None) == \
+        M.MOE_ERR_SHAPE
+    assert lib.moe_expert_ffn_on_sms(ctypes.byref(bf), *args, 4, None, need, None) == \
+        M.MOE_ERR_NULL
+    assert lib.moe_expert_ffn_on_sms(ctypes.byref(bf), *args, 4, fake, need - 1, None) == \
+        M.MOE_ERR_WORKSPACE
+    assert lib.moe_expert_ffn_on_sms(None, *args, 4, fake, need, None) == M.MOE_ERR_NULL
+
+
 def test_status_strings():
     for code in range(-8, 1):
         assert M.status_string(code) and M.status_string(code) != "unknown status"

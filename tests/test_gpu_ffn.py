@@ -94,6 +94,50 @@ def test_expert_ffn_bf16_against_oracle(sizes, d, f, gemm_form):
         G.assert_output_close(got[a:b], ref, "bf16", f"segment {s}")
 
 
+def test_expert_ffn_on_a_slice_of_the_gpu():
+    """moe_expert_ffn_on_sms: the same rows as moe_expert_ffn on any number of
+    SMs, and a device group's call (offsets and weights pointing at its first
+    expert) reproduces that group's rows of the whole-layer call."""
+    sizes, d, f = [700, 0, 260, 1, 513, 90], 256, 384
+    S = len(sizes)
+    off = _segments(sizes)
+    P = int(off[-1])
+    rows_max = P + 3
+    xp = _rand((rows_max, d), 13)
+    W1 = _rand((S, d, f), 14, d ** -0.5)
+    W3 = _rand((S, d, f), 15, d ** -0.5)
+    W2 = _rand((S, f, d), 16, f ** -0.5)
+    cfg = M.make_config(T=1, d=d, N=S, f=f, k=1, dtype="bf16")
+    dev = torch.device("cuda")
+    xg, W1g, W3g, W2g = xp.cuda(), W1.cuda(), W3.cuda(), W2.cuda()
+    offg = torch.from_numpy(off).cuda()
+    ws = torch.zeros(M.ffn_workspace_size(rows_max, f, "bf16"), dtype=torch.uint8, device=dev)
+    full = torch.zeros((rows_max, d), dtype=torch.bfloat16, device=dev)
+    M.moe_expert_ffn(cfg, xg, offg, S, rows_max, f, W1g, W3g, W2g, full, ws)
+    for max_sms in (1, 2, 7, 18, 148, 1000):
+        op = torch.zeros_like(full)
+        M.moe_expert_ffn_on_sms(cfg, xg, offg, S, rows_max, f, W1g, W3g, W2g, op, max_sms, ws)
+        torch.cuda.synchronize()
+        assert M.moe_get_device_status(ws) == M.MOE_OK
+        if max_sms >= 2:  # the same GEMM form: the same bits
+            assert torch.equal(op, full), max_sms
+        got = op.float().cpu().numpy()
+        for s in range(S):
+            a, b = int(off[s]), int(off[s + 1])
+            if a < b:
+                ref = O.swiglu(G.np32(xp[a:b]), G.np32(W1[s]), G.np32(W3[s]), G.np32(W2[s]), "bf16")
+                G.assert_output_close(got[a:b], ref, "bf16", f"segment {s}, {max_sms} SMs")
+    # experts 2..4 as one device on 18 SMs
+    lo, hi = 2, 5
+    op = torch.zeros_like(full)
+    M.moe_expert_ffn_on_sms(cfg, xg, offg.data_ptr() + 4 * lo, hi - lo, rows_max, f,
+                            W1g[lo].data_ptr(), W3g[lo].data_ptr(), W2g[lo].data_ptr(), op, 18, ws)
+    torch.cuda.synchronize()
+    a, b = int(off[lo]), int(off[hi])
+    assert torch.equal(op[a:b], full[a:b])
+    assert not op[:a].any() and not op[b:].any()
+
+
 @pytest.mark.parametrize("sizes,d,f", [([100, 0, 37, 64], 128, 256), ([5], 64, 200)])
 def test_expert_ffn_f32_against_oracle(sizes, d, f):
     S = len(sizes)
