@@ -219,6 +219,24 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def max_over_ranks(ms: float, dev) -> float:
+    """The slowest rank's time: every rank calls this with its own; without
+    an initialised process group it returns `ms` unchanged."""
+    import torch.distributed as td
+    if not (td.is_available() and td.is_initialized()):
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    td.all_reduce(t, op=td.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world: int, units_per_rank: int, steps: int, ms: float) -> float:
+    """Whole-job throughput under weak scaling: every rank processes
+    `units_per_rank` units per step, and the job takes the slowest rank's
+    time `ms` for `steps` steps."""
+    return world * units_per_rank * steps / (ms / 1e3)
+
+
 def gemm_traffic(w):
     """DRAM bytes per launch of the grouped GEMM pair on this workload from
     the committed ncu capture, or None when the kernel source differs from
@@ -332,12 +350,9 @@ def run_ours(args, rank, world, local_rank):
     total_ms = sum(step_ms) if flush is not None else evs[0][0].elapsed_time(evs[-1][-1])
     g1_ms = statistics.mean(row[g1_i].elapsed_time(row[g1_i + 1]) for row in evs)
     g2_ms = statistics.mean(row[g1_i + 1].elapsed_time(row[g1_i + 2]) for row in evs)
-    if dist:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        td.all_reduce(t, op=td.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dev)
     ms_per_step = total_ms / args.steps
-    value = world * w.T * args.steps / (total_ms / 1e3)
+    value = job_rate(world, w.T, args.steps, total_ms)
 
     # ---- per-kernel breakdown: a few more steps with an event at every
     # kernel boundary (this serialises the launches) ----
@@ -407,13 +422,10 @@ def run_ours(args, rank, world, local_rank):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        td.all_reduce(t, op=td.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dev)
     if not torch.equal(y_host[(args.steps - 1) & 1], y.cpu()):
         raise RuntimeError("end-to-end output differs from the device-resident run")
-    e2e_value = world * w.T * args.steps / (e2e_ms / 1e3)
+    e2e_value = job_rate(world, w.T, args.steps, e2e_ms)
     sx = 2 if w.dtype == "bf16" else 4
 
     if M.moe_get_device_status(ws) != M.MOE_OK:
