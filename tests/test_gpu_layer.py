@@ -100,6 +100,7 @@ def test_gamma_inf_equals_token_choice_bitwise():
     ("mixtral_bf16", 32),
     ("finegrained_bf16", 64),
     ("finegrained_bf16_expanded", 64),
+    ("finegrained_bf16_device", 64),
 ])
 def test_benchmark_workloads_full_size(name, sample):
     w = W.ALL[name]
