@@ -50,6 +50,7 @@ class Workload:
     renorm: bool = False
     f_shared: int = 0
     dtype: str = "bf16"          # "bf16" or "f32": activations, weights, output
+    weights: str = "same"        # "same" (the dtype) or "e4m3": routed experts in FP8
     zipf_s: Optional[float] = None
     seed: int = 0
 
@@ -76,6 +77,8 @@ class Workload:
             s += f" shared f={self.f_shared}"
         if self.zipf_s is not None:
             s += f" zipf_s={self.zipf_s}"
+        if self.weights == "e4m3":
+            s += " expert weights e4m3 (per-column scales)"
         return s
 
 
@@ -88,6 +91,8 @@ MIXTRAL_BF16 = Workload("mixtral_bf16", T=4096, d=4096, N=8, f=14336, k=2,
 FINE_BF16 = Workload("finegrained_bf16", T=8192, d=2048, N=64, f=1408, k=6,
                      mode=CAPACITY_DROP, gamma=1.25, f_shared=2816, zipf_s=1.0)
 DECODE_BF16 = Workload("decode_bf16", T=32, d=4096, N=8, f=14336, k=2)
+# the decode step with its routed experts' weights stored in FP8
+DECODE_W8 = DECODE_BF16.replace(name="decode_bf16_w8", weights="e4m3")
 
 
 def mixtral(gamma: float) -> Workload:
@@ -110,7 +115,7 @@ def fine_device() -> Workload:
 
 
 ALL = {w.name: w for w in (TINY_F32, EC_BF16, MIXTRAL_BF16, mixtral(1.0), mixtral(1.5),
-                           FINE_BF16, fine_expanded(), fine_device(), DECODE_BF16)}
+                           FINE_BF16, fine_expanded(), fine_device(), DECODE_BF16, DECODE_W8)}
 
 
 def zipf_log_probs(N: int, s: float) -> np.ndarray:
@@ -142,6 +147,9 @@ def make_inputs(w: Workload, with_experts: bool = True) -> Dict[str, torch.Tenso
     out["W1"] = _draw(g, (w.N, w.d, w.f), w.d ** -0.5).to(dt)
     out["W3"] = _draw(g, (w.N, w.d, w.f), w.d ** -0.5).to(dt)
     out["W2"] = _draw(g, (w.N, w.f, w.d), w.f ** -0.5).to(dt)
+    if w.weights == "e4m3":
+        for name in ("W1", "W3", "W2"):
+            out[name + "q"], out[name + "s"] = quantize_e4m3(out[name])
     if w.f_shared:
         fs = w.f_shared
         out["Ws1"] = _draw(g, (w.d, fs), w.d ** -0.5).to(dt)
@@ -150,6 +158,21 @@ def make_inputs(w: Workload, with_experts: bool = True) -> Dict[str, torch.Tenso
     else:
         out["Ws1"] = out["Ws3"] = out["Ws2"] = None
     return out
+
+
+E4M3_MAX = 448.0
+
+
+def quantize_e4m3(W: torch.Tensor):
+    """Weights [..., K, n] -> (bytes [..., K, n] uint8, scale [..., n] fp32):
+    per output column, scale = max_k |W| / 448 (1 for an all-zero column) and
+    each weight is W / scale rounded to the nearest e4m3 value (ties to even,
+    the magnitude clamped to 448), so that W ~ value(byte) * scale."""
+    Wf = W.float()
+    amax = Wf.abs().amax(dim=-2)
+    scale = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax))
+    q = (Wf / scale.unsqueeze(-2)).clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn)
+    return q.view(torch.uint8).contiguous(), scale.contiguous()
 
 
 def random_logits(T: int, N: int, seed: int, scale: float = 1.0,

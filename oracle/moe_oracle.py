@@ -491,6 +491,28 @@ def layer_forward(x, W_r, bias, W1, W3, W2, *, mode: str, k: int, gamma: float =
 
 
 # --------------------------------------------------------------------------
+# FP8 expert weights
+# --------------------------------------------------------------------------
+
+
+def e4m3_value(b) -> np.ndarray:
+    """Values of e4m3 bytes (1 sign bit, 4 exponent bits with bias 7, 3
+    mantissa bits; exponent 0 holds the subnormals m * 2^-9; the byte pattern
+    with all exponent and mantissa bits set is NaN; there is no infinity)."""
+    b = np.asarray(b, dtype=np.int64)
+    s, e, m = (b >> 7) & 1, (b >> 3) & 15, b & 7
+    val = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    val = np.where((e == 15) & (m == 7), np.nan, val)
+    return np.where(s == 1, -val, val)
+
+
+def dequantize_e4m3(q, scale) -> np.ndarray:
+    """Expert weights stored as e4m3 bytes q [..., K, n] with one fp32 scale
+    per output column, scale [..., n]: W = value(q) * scale, exact in fp64."""
+    return e4m3_value(q) * np.asarray(scale, np.float64)[..., None, :]
+
+
+# --------------------------------------------------------------------------
 # Load statistics
 # --------------------------------------------------------------------------
 

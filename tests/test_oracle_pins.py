@@ -199,6 +199,37 @@ def test_gamma_inf_equals_token_choice_and_zero_drops_all():
 
 
 
+# ---------------------------------------------------------- FP8 expert weights
+
+def test_e4m3_values_match_torch_and_hand_values():
+    b = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(b).view(torch.float8_e4m3fn).double().numpy()
+    got = O.e4m3_value(b)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+    assert O.e4m3_value([0x38, 0x7E, 0x01, 0x08, 0x80, 0xB8])[[0, 1, 2, 3, 5]].tolist() == \
+        [1.0, 448.0, 2.0 ** -9, 2.0 ** -6, -1.0]
+    assert np.signbit(O.e4m3_value([0x80]))[0]
+
+
+def test_e4m3_quantizer_error_bound_and_dequantization():
+    g = torch.Generator().manual_seed(4)
+    Wt = (torch.randn(3, 64, 40, generator=g) * 0.05).to(torch.bfloat16)
+    Wt[1, :, 7] = 0                                     # an all-zero column
+    q, s = W.quantize_e4m3(Wt)
+    assert q.dtype == torch.uint8 and s.shape == (3, 40)
+    deq = O.dequantize_e4m3(q.numpy(), s.numpy())
+    Wd = Wt.double().numpy()
+    # each column's largest magnitude maps to 448 * scale, exact up to the scale's rounding
+    amax = np.abs(Wd).max(axis=1)
+    assert np.allclose(np.abs(deq).max(axis=1), amax, rtol=2 ** -20)
+    # round to nearest with 3 mantissa bits: relative error <= 2^-4 above the subnormal range
+    big = np.abs(Wd) >= 2.0 ** -6 * s.numpy()[:, None, :]
+    assert np.all(np.abs(deq - Wd)[big] <= 2.0 ** -4 * np.abs(Wd)[big] * (1 + 1e-6))
+    assert np.all(deq[1, :, 7] == 0)
+
+
 # ------------------------------------------------- device-level capacity (§2③)
 
 def test_device_capacity_values():
