@@ -120,6 +120,26 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm), "window": window}
 
 
+def layer_call(M, cfg, w, d, x, y, ws, stats=None, stream=None):
+    """One moe_layer_forward (moe_layer_forward_e4m3 for FP8 routed experts)."""
+    if w.weights == "e4m3":
+        ex = M.e4m3_experts(d["W1q"], d["W3q"], d["W2q"], d["W1s"], d["W3s"], d["W2s"])
+        M.moe_layer_forward_e4m3(cfg, x, d["W_r"], d["bias"], ex, d.get("Ws1"), d.get("Ws3"),
+                                 d.get("Ws2"), y, ws, stats=stats, stream=stream)
+    else:
+        M.moe_layer_forward(cfg, x, d["W_r"], d["bias"], d["W1"], d["W3"], d["W2"], d.get("Ws1"),
+                            d.get("Ws3"), d.get("Ws2"), y, ws, stats=stats, stream=stream)
+
+
+def routed_weight_bytes(w, kept) -> int:
+    """Bytes of the routed experts a step reads: the weights (and column
+    scales) of every expert that kept at least one row."""
+    per = 3 * w.d * w.f * (1 if w.weights == "e4m3" else (2 if w.dtype == "bf16" else 4))
+    if w.weights == "e4m3":
+        per += 4 * (2 * w.f + w.d)
+    return per * int((np.asarray(kept) > 0).sum())
+
+
 def ffn_flops(w, P: int) -> float:
     return 6.0 * w.d * w.f * P + (6.0 * w.d * w.f_shared * w.T if w.f_shared else 0.0)
 
@@ -158,8 +178,12 @@ class OracleSampler:
         self.w = w
         inp = W.make_inputs(w)
         f = lambda t: None if t is None else t.float().numpy()  # noqa: E731
-        self.args = (f(inp["x"]), f(inp["W_r"]), f(inp["bias"]), f(inp["W1"]), f(inp["W3"]),
-                     f(inp["W2"]))
+        if w.weights == "e4m3":  # the experts the library multiplies
+            Wx = [O.dequantize_e4m3(inp[n + "q"].numpy(), inp[n + "s"].numpy())
+                  for n in ("W1", "W3", "W2")]
+        else:
+            Wx = [f(inp[n]) for n in ("W1", "W3", "W2")]
+        self.args = (f(inp["x"]), f(inp["W_r"]), f(inp["bias"]), *Wx)
         self.shared = [f(inp.get(k)) for k in ("Ws1", "Ws3", "Ws2")]
         self.n_tokens = None
 
@@ -273,6 +297,8 @@ def run_ours(args, rank, world, local_rank):
         import torch.distributed as td
 
     inp = W.make_inputs(w.replace(seed=w.seed + rank) if args.distinct_batches else w)
+    if w.weights == "e4m3":  # the routed experts live on the device in e4m3 only
+        inp = {k: v for k, v in inp.items() if k not in ("W1", "W3", "W2")}
     d = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
     cfg = M.config_from_workload(w)
     sz = M.sizes(cfg)
@@ -283,7 +309,8 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.current_stream(dev)
     stages = M.moe_layer_stages(cfg)
     weight_bytes = sum(t.numel() * t.element_size() for k, t in d.items()
-                       if t is not None and k in ("W1", "W3", "W2", "Ws1", "Ws3", "Ws2"))
+                       if t is not None and k in ("W1", "W3", "W2", "Ws1", "Ws3", "Ws2",
+                                                  "W1q", "W3q", "W2q"))
     l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
     # Between steps the L2 is not flushed: every step streams all expert
     # weights it uses (far more than the L2) through it, so the next step's
@@ -293,9 +320,7 @@ def run_ours(args, rank, world, local_rank):
         flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
 
     def step():
-        M.moe_layer_forward(cfg, d["x"], d["W_r"], d["bias"], d["W1"], d["W3"], d["W2"],
-                            d.get("Ws1"), d.get("Ws3"), d.get("Ws2"), y, ws, stats=stats,
-                            stream=stream)
+        layer_call(M, cfg, w, d, d["x"], y, ws, stats=stats, stream=stream)
 
     for _ in range(args.warmup):
         if flush is not None:
@@ -306,6 +331,9 @@ def run_ours(args, rank, world, local_rank):
         raise RuntimeError("device status error after warm-up")
     st = stats.cpu().numpy()
     P = int(st[0])
+    vw = M.moe_workspace_views(cfg, ws)
+    k0 = vw.kept - ws.data_ptr()  # per-expert kept rows, inside the workspace
+    kept_h = ws[k0:k0 + 4 * w.N].view(torch.int32).cpu().numpy()
 
     # ---- timed region: K layer steps. The library records events on the
     # launching stream at the step's start and end and around the expert GEMMs
@@ -398,9 +426,7 @@ def run_ours(args, rank, world, local_rank):
             stream.wait_event(up_done[b])
             if i >= 2:
                 stream.wait_event(down_done[b])  # step i-2's y_dev[b] is on the host
-            M.moe_layer_forward(cfg, x_dev[b], d["W_r"], d["bias"], d["W1"], d["W3"], d["W2"],
-                                d.get("Ws1"), d.get("Ws3"), d.get("Ws2"), y_dev[b], ws,
-                                stats=stats, stream=stream)
+            layer_call(M, cfg, w, d, x_dev[b], y_dev[b], ws, stats=stats, stream=stream)
             layer_done[b].record(stream)
             with torch.cuda.stream(s_down):
                 s_down.wait_event(layer_done[b])
@@ -447,6 +473,20 @@ def run_ours(args, rank, world, local_rank):
     g1, g2 = g1_ms, g2_ms
     routed_flops = 6.0 * w.d * w.f * P
     ffn_tflops = routed_flops / ((g1 + g2) * 1e-3) / 1e12
+    # the expert GEMMs are weight-bound when their flops per weight byte fall
+    # below the machine balance (decode batches)
+    sx_ = 2 if w.dtype == "bf16" else 4
+    gemm_bytes = routed_weight_bytes(w, kept_h) + 2 * P * (w.d + w.f) * sx_
+    hbm_bound = routed_flops / gemm_bytes < peak_tf * 1e12 / (hbm * 1e9)
+    if hbm_bound:
+        gbs = gemm_bytes / ((g1 + g2) * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                "algorithmic_bytes": gemm_bytes, "peak_source": f"{peak_src} HBM copy"}
+    else:
+        roof = {"bound": "tensor", "achieved": ffn_tflops, "peak": peak_tf, "unit": "TFLOP/s",
+                "frac": ffn_tflops / peak_tf, "peak_source": f"{peak_src} bf16 burst",
+                "frac_of_sustained": ffn_tflops / float(peaks.get("bf16_tflops_sustained",
+                                                                  peak_tf))}
     kernels["expert_gemm1_swiglu"] = {"ms": g1, "flops": 4.0 * w.d * w.f * P,
                                       "TFLOP/s": 4.0 * w.d * w.f * P / (g1 * 1e-3) / 1e12}
     kernels["expert_gemm2"] = {"ms": g2, "flops": 2.0 * w.d * w.f * P,
@@ -479,15 +519,13 @@ def run_ours(args, rank, world, local_rank):
                                "L2 every step)"),
                    "parallelism": f"replicas x{world}"},
         "tflops": ffn_flops(w, P) * args.steps * world / (total_ms / 1e3) / 1e12,
-        "roofline": {"kernel": "grouped_gemm_tc_kernel (expert GEMM1+SwiGLU and GEMM2, "
-                               "one launch each per step; times from the timed steps)",
-                     "bound": "tensor", "achieved": ffn_tflops, "peak": peak_tf,
-                     "unit": "TFLOP/s", "frac": ffn_tflops / peak_tf,
-                     "traffic": gemm_traffic(w),
-                     "traffic_unit": "DRAM bytes per step (both GEMM launches), one ncu capture",
-                     "peak_source": f"{peak_src} bf16 burst",
-                     "frac_of_sustained": ffn_tflops / float(peaks.get("bf16_tflops_sustained",
-                                                                       peak_tf))},
+        "roofline": dict({"kernel": ("grouped_gemm_w8_kernel" if w.weights == "e4m3" else
+                                     "grouped_gemm_tc_kernel") +
+                          " (expert GEMM1+SwiGLU and GEMM2, one launch each per step; times "
+                          "from the timed steps)",
+                          "traffic": gemm_traffic(w),
+                          "traffic_unit": "DRAM bytes per step (both GEMM launches), one ncu "
+                                          "capture"}, **roof),
         "kernels": kernels,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": w.T * w.d * sx,
                 "d2h_bytes_per_step": w.T * w.d * sx,

@@ -285,6 +285,46 @@ int moe_expert_ffn_noalloc(const moe_config* cfg, const void* xp, const int32_t*
                            void* stream);
 
 /*
+ * Routed experts stored in FP8 (e4m3: 1 sign, 4 exponent bits with bias 7, 3
+ * mantissa bits), one fp32 scale per output column: W1[e][k][n] =
+ * value(W1q[e][k][n]) * s1[e][n], likewise W3 with s3 and W2 with s2. Halves
+ * the bytes a weight-bound (decode) step streams; activations stay bf16 and
+ * accumulation fp32. ("From personas to MoE 02", section "dense was honestly
+ * heavy": quantising the weights, NVFP4 for instance, lightens the weight
+ * side; the e4m3 format with column scales is this library's choice.)
+ */
+typedef struct moe_e4m3_experts {
+  const uint8_t* W1;   /* [N, d, f] e4m3 bytes */
+  const uint8_t* W3;   /* [N, d, f] */
+  const uint8_t* W2;   /* [N, f, d] */
+  const float*   s1;   /* [N, f] */
+  const float*   s3;   /* [N, f] */
+  const float*   s2;   /* [N, d] */
+} moe_e4m3_experts;
+
+/*
+ * moe_expert_ffn with e4m3 experts (struct above; its pointers are device
+ * pointers, the struct itself is read on the host). bf16 only, d and f
+ * multiples of 128; MOE_ERR_UNSUPPORTED for fp32 configs. The e4m3 bytes are
+ * widened to bf16 in shared memory (exactly) and the column scales multiply
+ * the fp32 accumulators. ws as for moe_expert_ffn.
+ */
+int moe_expert_ffn_e4m3(const moe_config* cfg, const void* xp, const int32_t* offsets,
+                        int32_t n_segments, int64_t rows_max, int32_t f,
+                        const moe_e4m3_experts* experts, void* op, void* ws, size_t ws_bytes,
+                        void* stream);
+
+/*
+ * moe_layer_forward with e4m3 routed experts; the router, the shared expert
+ * (Ws1, Ws3, Ws2, bf16) and everything else as in moe_layer_forward.
+ */
+int moe_layer_forward_e4m3(const moe_config* cfg, const void* x, const void* W_router,
+                           const float* bias, const moe_e4m3_experts* experts, const void* Ws1,
+                           const void* Ws3, const void* Ws2, const int32_t* home_group,
+                           float* logits, void* y, double* stats, void* ws, size_t ws_bytes,
+                           void* stream);
+
+/*
  * moe_expert_ffn confined to a slice of the GPU: its two persistent GEMMs
  * launch on at most max_sms streaming multiprocessors (bf16 only; f32 returns
  * MOE_ERR_UNSUPPORTED). Same arguments and result as moe_expert_ffn.

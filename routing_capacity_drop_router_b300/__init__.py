@@ -64,6 +64,10 @@ class moe_sizes_t(ctypes.Structure):
                 ("ffn_workspace", ctypes.c_size_t)]
 
 
+class moe_e4m3_experts(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("W1", "W3", "W2", "s1", "s3", "s2")]
+
+
 class moe_views_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "status", "logits", "scores", "cand_idx", "cand_gate", "slot", "keep", "demand", "kept",
@@ -90,6 +94,12 @@ SIGNATURES = {
     "moe_expert_ffn_on_sms": (ctypes.c_int, [_CFG, _VP, _VP, ctypes.c_int32, ctypes.c_int64,
                                              ctypes.c_int32, _VP, _VP, _VP, _VP, ctypes.c_int32,
                                              _VP, ctypes.c_size_t, _VP]),
+    "moe_expert_ffn_e4m3": (ctypes.c_int, [_CFG, _VP, _VP, ctypes.c_int32, ctypes.c_int64,
+                                           ctypes.c_int32, ctypes.c_void_p, _VP, _VP,
+                                           ctypes.c_size_t, _VP]),
+    "moe_layer_forward_e4m3": (ctypes.c_int, [_CFG, _VP, _VP, _VP, ctypes.c_void_p, _VP, _VP,
+                                              _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_size_t,
+                                              _VP]),
     "moe_grouped_gemm": (ctypes.c_int, [ctypes.c_int32, _VP, _VP, ctypes.c_int32, ctypes.c_int64,
                                         ctypes.c_int32, ctypes.c_int32, _VP, _VP, _VP,
                                         ctypes.c_size_t, _VP]),
@@ -221,6 +231,19 @@ def moe_expert_ffn(cfg, xp, offsets, n_segments, rows_max, f, W1, W3, W2, op, ws
                                 _stream(stream)), "moe_expert_ffn")
 
 
+def e4m3_experts(W1q, W3q, W2q, s1, s3, s2) -> moe_e4m3_experts:
+    """The pointer struct of e4m3 routed experts (tensors must stay alive)."""
+    return moe_e4m3_experts(*(_p(t) for t in (W1q, W3q, W2q, s1, s3, s2)))
+
+
+def moe_expert_ffn_e4m3(cfg, xp, offsets, n_segments, rows_max, f, experts, op, ws,
+                        stream=None) -> None:
+    _check(lib().moe_expert_ffn_e4m3(ctypes.byref(cfg), _p(xp), _p(offsets), n_segments, rows_max,
+                                     f, ctypes.byref(experts), _p(op), _p(ws),
+                                     ws.numel() * ws.element_size(), _stream(stream)),
+           "moe_expert_ffn_e4m3")
+
+
 def moe_expert_ffn_on_sms(cfg, xp, offsets, n_segments, rows_max, f, W1, W3, W2, op, max_sms, ws,
                           stream=None) -> None:
     """moe_expert_ffn on at most ``max_sms`` SMs (bf16). ``offsets``, ``W1``,
@@ -280,6 +303,16 @@ def moe_layer_forward(cfg, x, W_router, bias, W1, W3, W2, Ws1, Ws3, Ws2, y, ws, 
                                    _p(logits), _p(y), _p(stats), _p(ws),
                                    ws.numel() * ws.element_size(), _stream(stream)),
            "moe_layer_forward")
+
+
+def moe_layer_forward_e4m3(cfg, x, W_router, bias, experts, Ws1, Ws3, Ws2, y, ws, *,
+                           home_group=None, logits=None, stats=None, stream=None) -> None:
+    """moe_layer_forward with e4m3 routed experts (``experts`` from e4m3_experts)."""
+    _check(lib().moe_layer_forward_e4m3(ctypes.byref(cfg), _p(x), _p(W_router), _p(bias),
+                                        ctypes.byref(experts), _p(Ws1), _p(Ws3), _p(Ws2),
+                                        _p(home_group), _p(logits), _p(y), _p(stats), _p(ws),
+                                        ws.numel() * ws.element_size(), _stream(stream)),
+           "moe_layer_forward_e4m3")
 
 
 def moe_workspace_views(cfg, ws) -> moe_views_t:

@@ -107,6 +107,14 @@ cudaError_t launch_dispatch(int dtype, const void* x, const int32_t* cand_idx,
                             int32_t* expert_offsets, int32_t* row_token, float* row_gate,
                             int32_t* tok_rows, void* xp, cudaStream_t s);
 
+// Grouped GEMM with e4m3 weights and per-column fp32 scales (sc1 [S, n_out],
+// sc3 likewise for SwiGLU): out = silu(A (B1*sc1)) * (A (B3*sc3)) or A (B1*sc1);
+// A bf16, out bf16.
+cudaError_t launch_grouped_gemm_tc_w8(const void* A, const int32_t* offsets, int S,
+                                      int64_t rows_max, int K, int n_out, const void* B1,
+                                      const float* sc1, const void* B3, const float* sc3,
+                                      void* out, bool swiglu, int32_t* status, cudaStream_t s);
+
 // Grouped GEMMs. SwiGLU variant: out = silu(A B1) * (A B3); plain: out = A B1.
 cudaError_t launch_grouped_gemm_simt_f32(const float* A, const int32_t* offsets, int S,
                                          int64_t rows_max, int K, int n_out, const float* B1,
@@ -134,5 +142,8 @@ bool make_tmap_2d_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t 
                        uint32_t box_cols, uint32_t box_rows);
 bool make_tmap_3d_bf16(CUtensorMap* m, const void* ptr, uint64_t S, uint64_t K, uint64_t n,
                        uint32_t box_n, uint32_t box_k);
+// [S, K, n] bytes (e4m3 weights), 128-byte swizzle.
+bool make_tmap_3d_u8(CUtensorMap* m, const void* ptr, uint64_t S, uint64_t K, uint64_t n,
+                     uint32_t box_n, uint32_t box_k);
 
 }  // namespace moe

@@ -280,6 +280,28 @@ int run_ffn(int dtype, const void* xp, const int32_t* offsets, int S, int64_t ro
   return MOE_OK;
 }
 
+// Expert FFN with e4m3 weights and per-column scales (bf16 activations).
+int run_ffn_e4m3(const void* xp, const int32_t* offsets, int S, int64_t rows_max, int d, int f,
+                 const moe_e4m3_experts& w, void* hp, void* op, int32_t* status, cudaStream_t s,
+                 Tracer* tr = nullptr) {
+  cudaError_t e = launch_grouped_gemm_tc_w8(xp, offsets, S, rows_max, d, f, w.W1, w.s1, w.W3,
+                                            w.s3, hp, true, status, s);
+  if (e != cudaSuccess || (tr && !tr->mark())) return MOE_ERR_LAUNCH;
+  e = launch_grouped_gemm_tc_w8(hp, offsets, S, rows_max, f, d, w.W2, w.s2, nullptr, nullptr, op,
+                                false, status, s);
+  if (e != cudaSuccess || (tr && !tr->mark())) return MOE_ERR_LAUNCH;
+  return MOE_OK;
+}
+
+int check_e4m3(const moe_config& c, int f, const moe_e4m3_experts* w) {
+  if (c.dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (!w) return MOE_ERR_NULL;
+  if (c.d % 128 || f % 128) return MOE_ERR_SHAPE;
+  if (!w->W1 || !w->W3 || !w->W2 || !w->s1 || !w->s3 || !w->s2) return MOE_ERR_NULL;
+  if (!aligned16(w->W1) || !aligned16(w->W3) || !aligned16(w->W2)) return MOE_ERR_ALIGN;
+  return MOE_OK;
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -470,16 +492,29 @@ int moe_load_stats(const moe_config* cfg, const int32_t* demand, const int32_t* 
                                         cfg->N, stats, s));
 }
 
-int moe_layer_forward(const moe_config* cfg, const void* x, const void* W_router,
-                      const float* bias, const void* W1, const void* W3, const void* W2,
-                      const void* Ws1, const void* Ws3, const void* Ws2,
-                      const int32_t* home_group, float* logits, void* y, double* stats, void* ws,
-                      size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace moe {
+namespace {
+
+// moe_layer_forward with bf16/fp32 experts (W1, W3, W2) or, when w8 is set,
+// e4m3 experts.
+int layer_forward(const moe_config* cfg, const void* x, const void* W_router, const float* bias,
+                  const void* W1, const void* W3, const void* W2, const moe_e4m3_experts* w8,
+                  const void* Ws1, const void* Ws3, const void* Ws2, const int32_t* home_group,
+                  float* logits, void* y, double* stats, void* ws, size_t ws_bytes,
+                  void* stream) {
   Derived d;
   int st = validate(cfg, &d);
   if (st != MOE_OK) return st;
   const moe_config& c = *cfg;
   const bool given = (c.flags & MOE_LOGITS_GIVEN) != 0;
+  if (w8) {
+    if ((st = check_e4m3(c, c.f, w8)) != MOE_OK) return st;
+    W1 = w8->W1;
+    W3 = w8->W3;
+    W2 = w8->W2;
+  }
   if (!have(x, c.T) || !W1 || !W3 || !W2 || !have(y, c.T) || !ws) return MOE_ERR_NULL;
   if (given ? !have(logits, c.T) : !W_router) return MOE_ERR_NULL;
   if (c.f_shared > 0 && (!Ws1 || !Ws3 || !Ws2)) return MOE_ERR_NULL;
@@ -530,8 +565,9 @@ int moe_layer_forward(const moe_config* cfg, const void* x, const void* W_router
                       d.ec ? 1 : 0, d.rows_max, offsets, row_token, row_gate, tok_rows, xp,
                       s) != cudaSuccess || !tr.mark(1))
     return MOE_ERR_LAUNCH;
-  st = run_ffn(c.dtype, xp, offsets, c.N, d.rows_max, c.d, c.f, W1, W3, W2, hp, op, status, s,
-               &tr);
+  st = w8 ? run_ffn_e4m3(xp, offsets, c.N, d.rows_max, c.d, c.f, *w8, hp, op, status, s, &tr)
+          : run_ffn(c.dtype, xp, offsets, c.N, d.rows_max, c.d, c.f, W1, W3, W2, hp, op, status, s,
+                    &tr);
   if (st != MOE_OK) return st;
   if (c.f_shared > 0) {
     if (c.T > 0) {
@@ -550,6 +586,47 @@ int moe_layer_forward(const moe_config* cfg, const void* x, const void* W_router
       !tr.mark(1))
     return MOE_ERR_LAUNCH;
   return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" {
+
+int moe_layer_forward(const moe_config* cfg, const void* x, const void* W_router,
+                      const float* bias, const void* W1, const void* W3, const void* W2,
+                      const void* Ws1, const void* Ws3, const void* Ws2,
+                      const int32_t* home_group, float* logits, void* y, double* stats, void* ws,
+                      size_t ws_bytes, void* stream) {
+  return layer_forward(cfg, x, W_router, bias, W1, W3, W2, nullptr, Ws1, Ws3, Ws2, home_group,
+                       logits, y, stats, ws, ws_bytes, stream);
+}
+
+int moe_layer_forward_e4m3(const moe_config* cfg, const void* x, const void* W_router,
+                           const float* bias, const moe_e4m3_experts* experts, const void* Ws1,
+                           const void* Ws3, const void* Ws2, const int32_t* home_group,
+                           float* logits, void* y, double* stats, void* ws, size_t ws_bytes,
+                           void* stream) {
+  if (!experts) return MOE_ERR_NULL;
+  return layer_forward(cfg, x, W_router, bias, nullptr, nullptr, nullptr, experts, Ws1, Ws3, Ws2,
+                       home_group, logits, y, stats, ws, ws_bytes, stream);
+}
+
+int moe_expert_ffn_e4m3(const moe_config* cfg, const void* xp, const int32_t* offsets,
+                        int32_t n_segments, int64_t rows_max, int32_t f,
+                        const moe_e4m3_experts* experts, void* op, void* ws, size_t ws_bytes,
+                        void* stream) {
+  if (!cfg) return MOE_ERR_NULL;
+  if (cfg->d <= 0 || f <= 0 || n_segments < 0 || rows_max < 0) return MOE_ERR_SHAPE;
+  int st = check_e4m3(*cfg, f, experts);
+  if (st != MOE_OK) return st;
+  if (n_segments > kMaxN) return MOE_ERR_UNSUPPORTED;
+  if (!xp || !offsets || !op || !ws) return MOE_ERR_NULL;
+  if (!aligned16(xp) || !aligned16(op) || !aligned16(ws)) return MOE_ERR_ALIGN;
+  if (ws_bytes < moe_ffn_workspace_size(rows_max, f, MOE_BF16)) return MOE_ERR_WORKSPACE;
+  void* hp = static_cast<unsigned char*>(ws) + kCtrlBytes;
+  return run_ffn_e4m3(xp, offsets, n_segments, rows_max, cfg->d, f, *experts, hp, op,
+                      static_cast<int32_t*>(ws), as_stream(stream));
 }
 
 int moe_layer_stages(const moe_config* cfg, const char** names, int max_names) {

@@ -57,4 +57,17 @@ bool make_tmap_3d_bf16(CUtensorMap* m, const void* ptr, uint64_t S, uint64_t K, 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_tmap_3d_u8(CUtensorMap* m, const void* ptr, uint64_t S, uint64_t K, uint64_t n,
+                     uint32_t box_n, uint32_t box_k) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {n, K, S};
+  const cuuint64_t strides[2] = {n, n * K};
+  const cuuint32_t box[3] = {box_n, box_k, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace moe

@@ -122,10 +122,17 @@ def layer_gpu(w: W.Workload, inp: Dict[str, torch.Tensor], logits: Optional[np.n
     stats = torch.zeros(M.MOE_STATS_LEN, dtype=torch.float64, device=dev)
     Lg = torch.from_numpy(np.ascontiguousarray(logits)).to(dev) if logits is not None else \
         torch.empty((w.T, w.N), dtype=torch.float32, device=dev)
-    M.moe_layer_forward(cfg, cuda(inp["x"]), cuda(inp["W_r"]), cuda(inp["bias"]), cuda(inp["W1"]),
-                        cuda(inp["W3"]), cuda(inp["W2"]), cuda(inp.get("Ws1")),
-                        cuda(inp.get("Ws3")), cuda(inp.get("Ws2")), y, ws,
-                        home_group=cuda(home_group), logits=Lg, stats=stats)
+    if w.weights == "e4m3":
+        q = {k: cuda(inp[k]) for k in ("W1q", "W3q", "W2q", "W1s", "W3s", "W2s")}
+        ex = M.e4m3_experts(q["W1q"], q["W3q"], q["W2q"], q["W1s"], q["W3s"], q["W2s"])
+        M.moe_layer_forward_e4m3(cfg, cuda(inp["x"]), cuda(inp["W_r"]), cuda(inp["bias"]), ex,
+                                 cuda(inp.get("Ws1")), cuda(inp.get("Ws3")), cuda(inp.get("Ws2")),
+                                 y, ws, home_group=cuda(home_group), logits=Lg, stats=stats)
+    else:
+        M.moe_layer_forward(cfg, cuda(inp["x"]), cuda(inp["W_r"]), cuda(inp["bias"]),
+                            cuda(inp["W1"]), cuda(inp["W3"]), cuda(inp["W2"]),
+                            cuda(inp.get("Ws1")), cuda(inp.get("Ws3")), cuda(inp.get("Ws2")), y, ws,
+                            home_group=cuda(home_group), logits=Lg, stats=stats)
     torch.cuda.synchronize()
     assert M.moe_get_device_status(ws) == M.MOE_OK
     out = dict(y=np32(y), logits=Lg.cpu().numpy(), stats=stats.cpu().numpy())
@@ -140,8 +147,13 @@ def layer_gpu(w: W.Workload, inp: Dict[str, torch.Tensor], logits: Optional[np.n
 
 def oracle_layer(w: W.Workload, inp: Dict[str, torch.Tensor], logits: Optional[np.ndarray] = None,
                  tokens=None, home_group=None):
-    return O.layer_forward(np32(inp["x"]), np32(inp["W_r"]), np32(inp["bias"]), np32(inp["W1"]),
-                           np32(inp["W3"]), np32(inp["W2"]), mode=w.mode, k=w.k, gamma=w.gamma,
+    if w.weights == "e4m3":  # the experts the GPU multiplies: e4m3 values times column scales
+        W1, W3, W2 = (O.dequantize_e4m3(inp[n + "q"].numpy(), inp[n + "s"].numpy())
+                      for n in ("W1", "W3", "W2"))
+    else:
+        W1, W3, W2 = np32(inp["W1"]), np32(inp["W3"]), np32(inp["W2"])
+    return O.layer_forward(np32(inp["x"]), np32(inp["W_r"]), np32(inp["bias"]), W1,
+                           W3, W2, mode=w.mode, k=w.k, gamma=w.gamma,
                            m=w.m, group_size=w.group_size, renorm=w.renorm, dtype=w.dtype,
                            Ws1=np32(inp.get("Ws1")), Ws3=np32(inp.get("Ws3")),
                            Ws2=np32(inp.get("Ws2")), logits=logits, tokens=tokens,

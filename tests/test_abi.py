@@ -36,6 +36,7 @@ def test_struct_layout_matches_header():
     assert M.moe_config.gamma.offset == 24
     assert ctypes.sizeof(M.moe_sizes_t) == 32
     assert ctypes.sizeof(M.moe_views_t) == 16 * 8
+    assert ctypes.sizeof(M.moe_e4m3_experts) == 6 * 8
 
 
 @pytest.mark.parametrize("w", list(W.ALL.values()), ids=list(W.ALL))
@@ -166,6 +167,23 @@ def test_expert_ffn_on_sms_host_checks():
     assert lib.moe_expert_ffn_on_sms(ctypes.byref(bf), *args, 4, fake, need - 1, None) == \
         M.MOE_ERR_WORKSPACE
     assert lib.moe_expert_ffn_on_sms(None, *args, 4, fake, need, None) == M.MOE_ERR_NULL
+
+
+def test_e4m3_experts_host_checks():
+    lib = M.lib()
+    fake = ctypes.c_void_p(1 << 20)
+    ex = M.moe_e4m3_experts(*([1 << 20] * 6))
+    need = M.ffn_workspace_size(8, 128, "bf16")
+    args = lambda cfg, f, e: (ctypes.byref(cfg), fake, fake, 2, 8, f, e, fake, fake, need, None)  # noqa: E731
+    bf = M.make_config(T=8, d=128, N=2, f=128, k=1, dtype="bf16")
+    f32 = M.make_config(T=8, d=128, N=2, f=128, k=1, dtype="f32")
+    assert lib.moe_expert_ffn_e4m3(*args(f32, 128, ctypes.byref(ex))) == M.MOE_ERR_UNSUPPORTED
+    assert lib.moe_expert_ffn_e4m3(*args(bf, 192, ctypes.byref(ex))) == M.MOE_ERR_SHAPE
+    assert lib.moe_expert_ffn_e4m3(*args(bf, 128, None)) == M.MOE_ERR_NULL
+    bad = M.moe_e4m3_experts(*([1 << 20] * 5 + [None]))
+    assert lib.moe_expert_ffn_e4m3(*args(bf, 128, ctypes.byref(bad))) == M.MOE_ERR_NULL
+    assert lib.moe_layer_forward_e4m3(ctypes.byref(bf), *([None] * 3), None, *([None] * 8), 0,
+                                      None) == M.MOE_ERR_NULL
 
 
 def test_status_strings():

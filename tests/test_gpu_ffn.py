@@ -5,6 +5,7 @@ import numpy as np
 import pytest
 import torch
 
+import moe_workloads as W
 import oracle as O
 from tests import gpu_util as G
 
@@ -136,6 +137,43 @@ def test_expert_ffn_on_a_slice_of_the_gpu():
     a, b = int(off[lo]), int(off[hi])
     assert torch.equal(op[a:b], full[a:b])
     assert not op[:a].any() and not op[b:].any()
+
+
+@pytest.mark.parametrize("sizes,d,f", [
+    ([130, 0, 170, 1, 249], 256, 384),
+    ([8, 8, 7, 9, 8, 8, 8, 8], 512, 1408),     # decode-like: a handful of rows per expert
+    ([300, 400], 128, 256),
+])
+def test_expert_ffn_e4m3_against_oracle(sizes, d, f):
+    """e4m3 experts with per-column scales: the GPU result against the oracle
+    run on the dequantized weights (values times scales, exact)."""
+    S = len(sizes)
+    off = _segments(sizes)
+    P = int(off[-1])
+    rows_max = P + 5
+    xp = _rand((rows_max, d), 21)
+    Wb = {n: _rand(shape, seed, scale) for n, shape, seed, scale in (
+        ("W1", (S, d, f), 22, d ** -0.5), ("W3", (S, d, f), 23, d ** -0.5),
+        ("W2", (S, f, d), 24, f ** -0.5))}
+    q = {n: W.quantize_e4m3(Wb[n]) for n in Wb}
+    deq = {n: O.dequantize_e4m3(q[n][0].numpy(), q[n][1].numpy()) for n in q}
+    cfg = M.make_config(T=1, d=d, N=S, f=f, k=1, dtype="bf16")
+    dev = torch.device("cuda")
+    qd = {n: (q[n][0].cuda(), q[n][1].cuda()) for n in q}
+    ex = M.e4m3_experts(qd["W1"][0], qd["W3"][0], qd["W2"][0], qd["W1"][1], qd["W3"][1],
+                        qd["W2"][1])
+    op = torch.zeros((rows_max, d), dtype=torch.bfloat16, device=dev)
+    ws = torch.zeros(M.ffn_workspace_size(rows_max, f, "bf16"), dtype=torch.uint8, device=dev)
+    M.moe_expert_ffn_e4m3(cfg, xp.cuda(), torch.from_numpy(off).cuda(), S, rows_max, f, ex, op, ws)
+    torch.cuda.synchronize()
+    assert M.moe_get_device_status(ws) == M.MOE_OK
+    got = op.float().cpu().numpy()
+    for s in range(S):
+        a, b = int(off[s]), int(off[s + 1])
+        if a < b:
+            ref = O.swiglu(G.np32(xp[a:b]), deq["W1"][s], deq["W3"][s], deq["W2"][s], "bf16")
+            G.assert_output_close(got[a:b], ref, "bf16", f"segment {s}")
+    assert not op[P:].any()
 
 
 @pytest.mark.parametrize("sizes,d,f", [([100, 0, 37, 64], 128, 256), ([5], 64, 200)])

@@ -28,6 +28,8 @@ SMALL = [
                gamma=1.0),
     W.Workload("small_device_shared", T=500, d=128, N=16, f=128, k=3,
                mode=W.CAPACITY_DROP_DEVICE, gamma=1.0, group_size=4, f_shared=192, zipf_s=1.0),
+    W.Workload("small_drop_e4m3_shared", T=600, d=256, N=8, f=384, k=2, mode=W.CAPACITY_DROP,
+               gamma=1.0, renorm=True, zipf_s=1.2, f_shared=128, weights="e4m3"),
 ]
 
 
@@ -101,6 +103,7 @@ def test_gamma_inf_equals_token_choice_bitwise():
     ("finegrained_bf16", 64),
     ("finegrained_bf16_expanded", 64),
     ("finegrained_bf16_device", 64),
+    ("decode_bf16_w8", None),
 ])
 def test_benchmark_workloads_full_size(name, sample):
     w = W.ALL[name]
