@@ -280,10 +280,10 @@ def gemm_traffic(w):
 # keyed by the sha256 prefix of the kernel source it was taken on.
 GEMM_TRAFFIC = {
     # profiles/grouped_gemm_tc_pairs_mixtral_gamma1_bf16.md: GEMM1+SwiGLU
-    # 1.973634 GB read + 0.141470 GB written, GEMM2 1.185924 GB + 0.040475 GB
-    "mixtral_bf16_gamma1": {"kernel_sha": "441cef60e131d3bc",
-                            "bytes_per_launch_pair": 1.973634e9 + 0.141470e9 +
-                            1.185924e9 + 0.040475e9},
+    # 1.954983 GB read + 0.141425 GB written, GEMM2 1.185948 GB + 0.040500 GB
+    "mixtral_bf16_gamma1": {"kernel_sha": "7b6a8ade120d9c69",
+                            "bytes_per_launch_pair": 1.954983e9 + 0.141425e9 +
+                            1.185948e9 + 0.040500e9},
 }
 
 
@@ -545,16 +545,21 @@ def run_ours(args, rank, world, local_rank):
 def run_stage(args):
     """--kernel STAGE: loop one stage of the layer on the workload (T
     overridable with --T) and print its device time and algorithmic GB/s.
-    Holds only the routing-side tensors on the device, so a single kernel can
-    be profiled with ncu on inputs larger than L2."""
+    Holds only the routing-side tensors on the device (plus the routed
+    experts for --kernel ffn, the expert FFN of the routed rows: both grouped
+    GEMMs), so a single kernel can be profiled with ncu on inputs larger than
+    L2."""
     import routing_capacity_drop_router_b300 as M
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
     w = W.ALL[args.workload]
     if args.T:
         w = w.replace(T=args.T)
-    inp = W.make_inputs(w, with_experts=False)
-    d = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
+    inp = W.make_inputs(w, with_experts=args.kernel == "ffn")
+    if w.weights == "e4m3":
+        inp = {k: v for k, v in inp.items() if k not in ("W1", "W3", "W2")}
+    d = {k: (v.to(dev) if v is not None and k not in ("Ws1", "Ws3", "Ws2") else None)
+         for k, v in inp.items()}
     cfg = M.config_from_workload(w)
     sz = M.sizes(cfg)
     R, kc = int(sz.rows_max), sz.kc
@@ -587,6 +592,14 @@ def run_stage(args):
                                            row_token, row_gate, tok_rows, xp),
         "combine": lambda: M.moe_combine(cfg, op, row_gate, tok_rows, None, y),
     }
+    if args.kernel == "ffn":
+        fws = torch.zeros(M.ffn_workspace_size(R, w.f, w.dtype), dtype=torch.uint8, device=dev)
+        if w.weights == "e4m3":
+            ex = M.e4m3_experts(d["W1q"], d["W3q"], d["W2q"], d["W1s"], d["W3s"], d["W2s"])
+            fns["ffn"] = lambda: M.moe_expert_ffn_e4m3(cfg, xp, offs, w.N, R, w.f, ex, op, fws)
+        else:
+            fns["ffn"] = lambda: M.moe_expert_ffn(cfg, xp, offs, w.N, R, w.f, d["W1"], d["W3"],
+                                                  d["W2"], op, fws)
     for name in ("route", "select", "dispatch"):
         fns[name]()
     torch.cuda.synchronize()
@@ -607,6 +620,9 @@ def run_stage(args):
     torch.cuda.synchronize()
     ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
     nbytes = stage_bytes(w, P).get(args.kernel)
+    if args.kernel == "ffn":  # weights of the experts hit, rows in and out of both GEMMs
+        nbytes = routed_weight_bytes(w, kept.cpu().numpy()) + \
+            2 * P * (w.d + w.f) * (2 if w.dtype == "bf16" else 4)
     peaks, src = load_peaks()
     out = {"kernel": args.kernel, "workload": w.describe(), "kept_pairs": P, "ms": ms}
     if nbytes:
@@ -708,7 +724,7 @@ def main():
                     help="--impl reference: seconds for warm-up + timed samples together")
     ap.add_argument("--distinct-batches", action="store_true",
                     help="each rank draws its own x (seed + rank)")
-    ap.add_argument("--kernel", choices=["route", "select", "dispatch", "combine"],
+    ap.add_argument("--kernel", choices=["route", "select", "dispatch", "combine", "ffn"],
                     help="time one stage alone instead of the layer")
     ap.add_argument("--T", type=int, default=0, help="token count override for --kernel")
     ap.add_argument("--ep-sim", action="store_true",
