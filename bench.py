@@ -144,12 +144,13 @@ def ffn_flops(w, P: int) -> float:
     return 6.0 * w.d * w.f * P + (6.0 * w.d * w.f_shared * w.T if w.f_shared else 0.0)
 
 
-def stage_bytes(w, P: int):
+def stage_bytes(w, P: int, fused_gather: bool = False):
     sx = 2 if w.dtype == "bf16" else 4
     kc = w.N if w.mode == W.EXPERT_CHOICE else w.k + w.m
     return {
         "route": w.T * w.d * sx + w.d * w.N * sx + w.T * w.N * 4 * 2 + w.T * kc * 8,
-        "dispatch": w.T * w.d * sx + P * w.d * sx + 16 * P,
+        # with the gather fused into GEMM1 dispatch moves only the row tables
+        "dispatch": (0 if fused_gather else w.T * w.d * sx + P * w.d * sx) + 16 * P,
         "combine": P * w.d * sx + w.T * w.d * sx + 8 * P + (w.T * w.d * sx if w.f_shared else 0),
     }
 
@@ -280,10 +281,10 @@ def gemm_traffic(w):
 # keyed by the sha256 prefix of the kernel source it was taken on.
 GEMM_TRAFFIC = {
     # profiles/grouped_gemm_tc_pairs_mixtral_gamma1_bf16.md: GEMM1+SwiGLU
-    # 1.954983 GB read + 0.141425 GB written, GEMM2 1.185948 GB + 0.040500 GB
-    "mixtral_bf16_gamma1": {"kernel_sha": "7b6a8ade120d9c69",
-                            "bytes_per_launch_pair": 1.954983e9 + 0.141425e9 +
-                            1.185948e9 + 0.040500e9},
+    # 1.967098 GB read + 0.141841 GB written, GEMM2 1.185967 GB + 0.040459 GB
+    "mixtral_bf16_gamma1": {"kernel_sha": "bc4d48697a603fd5",
+                            "bytes_per_launch_pair": 1.967098e9 + 0.141841e9 +
+                            1.185967e9 + 0.040459e9},
 }
 
 
@@ -300,7 +301,7 @@ def run_ours(args, rank, world, local_rank):
     if w.weights == "e4m3":  # the routed experts live on the device in e4m3 only
         inp = {k: v for k, v in inp.items() if k not in ("W1", "W3", "W2")}
     d = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
-    cfg = M.config_from_workload(w)
+    cfg = M.config_from_workload(w, fuse_gather=args.gather == "fused")
     sz = M.sizes(cfg)
     ws = torch.zeros(sz.workspace, dtype=torch.uint8, device=dev)
     dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
@@ -465,7 +466,8 @@ def run_ours(args, rank, world, local_rank):
     peaks, peak_src = load_peaks()
     peak_tf = float(peaks["bf16_tflops"])
     hbm = float(peaks["hbm_gbs"])
-    sbytes = stage_bytes(w, P)
+    sbytes = stage_bytes(w, P, fused_gather=bool(cfg.flags & M.MOE_FUSE_GATHER) and
+                         w.dtype == "bf16" and w.weights == "same")
     kernels = {}
     route_ms = sum(stage_ms.get(n, 0.0) for n in ("router", "router_logits", "route_tokens"))
     for name, ms in (("route", route_ms), ("dispatch", stage_ms["dispatch"]),
@@ -523,6 +525,9 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": w.describe(), "T": w.T, "d": w.d, "N": w.N, "f": w.f, "k": w.k,
                    "mode": w.mode, "gamma": None if math.isinf(w.gamma) else w.gamma,
                    "kept_pairs": P,
+                   "gather": ("fused into expert GEMM1 (MOE_FUSE_GATHER)"
+                              if args.gather == "fused" and w.dtype == "bf16" and
+                              w.weights == "same" else "dispatch copies the token rows"),
                    "l2": ("flushed (256 MiB write) before every timed step" if flush is not None
                           else f"not flushed: inputs larger than L2 ({weight_bytes / 1e9:.2f} GB "
                                f"of expert weights stream through the {l2_bytes / 2**20:.0f} MiB "
@@ -607,6 +612,9 @@ def run_stage(args):
         if w.weights == "e4m3":
             ex = M.e4m3_experts(d["W1q"], d["W3q"], d["W2q"], d["W1s"], d["W3s"], d["W2s"])
             fns["ffn"] = lambda: M.moe_expert_ffn_e4m3(cfg, xp, offs, w.N, R, w.f, ex, op, fws)
+        elif args.gather == "fused":
+            fns["ffn"] = lambda: M.moe_expert_ffn_gather(cfg, d["x"], row_token, offs, w.N, R, w.f,
+                                                         d["W1"], d["W3"], d["W2"], op, fws)
         else:
             fns["ffn"] = lambda: M.moe_expert_ffn(cfg, xp, offs, w.N, R, w.f, d["W1"], d["W3"],
                                                   d["W2"], op, fws)
@@ -737,6 +745,9 @@ def main():
     ap.add_argument("--kernel", choices=["route", "select", "dispatch", "combine", "ffn"],
                     help="time one stage alone instead of the layer")
     ap.add_argument("--T", type=int, default=0, help="token count override for --kernel")
+    ap.add_argument("--gather", choices=["copy", "fused"], default="copy",
+                    help="bf16 experts: dispatch copies the token rows (copy) or expert GEMM1 "
+                         "gathers them itself (fused, MOE_FUSE_GATHER)")
     ap.add_argument("--ep-sim", action="store_true",
                     help="simulate expert parallelism: time each device group's experts on "
                          "its share of the SMs and report the straggler")

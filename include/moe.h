@@ -76,6 +76,9 @@ extern "C" {
 
 /* flags */
 #define MOE_LOGITS_GIVEN 1  /* router logits are an input; x and W_router are not read for routing */
+#define MOE_FUSE_GATHER  2  /* moe_layer_forward, bf16 experts: the first expert GEMM reads each
+                               token row of x through row_token (moe_expert_ffn_gather) and
+                               dispatch writes no xp copy; ignored for fp32 or e4m3 experts */
 
 /* Limits: 1 <= N <= 256, 1 <= k <= N, k + m <= 32, expert choice N <= 256,
  * T <= 24576 (per-expert candidate lists are held in shared memory),
@@ -97,7 +100,7 @@ typedef struct moe_config {
   int32_t renorm;     /* 1: gates divided by their sum over the token's candidates */
   int32_t f_shared;   /* hidden width of the always-on shared expert (0 = none) */
   int32_t dtype;      /* MOE_BF16 or MOE_F32 */
-  int32_t flags;      /* MOE_LOGITS_GIVEN */
+  int32_t flags;      /* MOE_LOGITS_GIVEN | MOE_FUSE_GATHER */
 } moe_config;
 
 /* Derived sizes of a config (host values). */
@@ -252,6 +255,33 @@ int moe_expert_ffn(const moe_config* cfg, const void* xp, const int32_t* offsets
                    int32_t n_segments, int64_t rows_max, int32_t f,
                    const void* W1, const void* W3, const void* W2, void* op,
                    void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * moe_expert_ffn with the dispatch gather fused into the first GEMM: row r of
+ * segment s is computed from x[row_token[r]] instead of xp[r], so the
+ * expert-contiguous copy of the token rows is never written or read. Moving
+ * token rows is one of the data movements the pages name as the cost of MoE
+ * inference ("From personas to MoE 02", section "ugh, bandwidth"); the result
+ * equals moe_expert_ffn on xp[r] = x[row_token[r]] bit for bit.
+ *
+ *   x            [T, d] bf16 (T = cfg->T), 16-byte aligned, non-NULL
+ *   row_token    [rows_max] int32: the token of each row (as moe_dispatch
+ *                writes it); read for rows below offsets[n_segments]
+ *   other arguments as in moe_expert_ffn (bf16 only: MOE_ERR_UNSUPPORTED for
+ *   fp32). A row_token entry outside [0, T) makes that row read zeros and
+ *   records MOE_ERR_DEVICE_BOUNDS in the status word.
+ * The first GEMM copies the rows with 16-byte asynchronous copies into the
+ * same swizzled shared-memory tiles the TMA path fills, one CTA per 128-row
+ * tile unless MOE_GEMM_CTA_PAIRS asks for pairs; the second GEMM is
+ * unchanged. On a B300 these copies feed the tensor cores at about half the
+ * rate of the TMA tile loads, so the first GEMM takes about twice as long as
+ * on the dispatched copy, which costs far more than the copy saves:
+ * MOE_FUSE_GATHER is off unless asked for.
+ */
+int moe_expert_ffn_gather(const moe_config* cfg, const void* x, const int32_t* row_token,
+                          const int32_t* offsets, int32_t n_segments, int64_t rows_max, int32_t f,
+                          const void* W1, const void* W3, const void* W2, void* op, void* ws,
+                          size_t ws_bytes, void* stream);
 
 /*
  * moe_expert_ffn for callers that cannot allocate device memory. The source
@@ -452,7 +482,7 @@ typedef struct moe_views_t {
   int32_t* row_token;      /* [rows_max] */
   float*   row_gate;       /* [rows_max] */
   int32_t* tok_rows;       /* [T, kc] */
-  void*    xp;             /* [rows_max, d] */
+  void*    xp;             /* [rows_max, d] (not written with MOE_FUSE_GATHER) */
   void*    op;             /* [rows_max, d] */
   void*    shared_out;     /* [T, d] or NULL */
 } moe_views_t;

@@ -34,6 +34,7 @@ MOE_CAPACITY_DROP_DEVICE = 3
 MOE_F32 = 0
 MOE_BF16 = 1
 MOE_LOGITS_GIVEN = 1
+MOE_FUSE_GATHER = 2
 MOE_STATS_LEN = 8
 MOE_CTRL_BYTES = 1024
 MOE_NOALLOC_SCRATCH_BYTES = 64 << 20
@@ -91,6 +92,9 @@ SIGNATURES = {
                                       _VP]),
     "moe_expert_ffn_noalloc": (ctypes.c_int, [_CFG, _VP, _VP, ctypes.c_int32, ctypes.c_int64,
                                               ctypes.c_int32, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "moe_expert_ffn_gather": (ctypes.c_int, [_CFG, _VP, _VP, _VP, ctypes.c_int32, ctypes.c_int64,
+                                             ctypes.c_int32, _VP, _VP, _VP, _VP, _VP,
+                                             ctypes.c_size_t, _VP]),
     "moe_expert_ffn_on_sms": (ctypes.c_int, [_CFG, _VP, _VP, ctypes.c_int32, ctypes.c_int64,
                                              ctypes.c_int32, _VP, _VP, _VP, _VP, ctypes.c_int32,
                                              _VP, ctypes.c_size_t, _VP]),
@@ -144,19 +148,21 @@ def status_string(status: int) -> str:
 
 def make_config(*, T: int, d: int, N: int, f: int, k: int, mode="token_choice",
                 gamma: float = math.inf, m: int = 0, group_size: int = 8, renorm: bool = False,
-                f_shared: int = 0, dtype="bf16", logits_given: bool = False) -> moe_config:
+                f_shared: int = 0, dtype="bf16", logits_given: bool = False,
+                fuse_gather: bool = False) -> moe_config:
     return moe_config(T=T, d=d, N=N, f=f, k=k, mode=MODES.get(mode, mode), gamma=float(gamma),
                       m=m, group_size=group_size, renorm=int(bool(renorm)), f_shared=f_shared,
                       dtype=DTYPES.get(dtype, dtype),
-                      flags=MOE_LOGITS_GIVEN if logits_given else 0)
+                      flags=(MOE_LOGITS_GIVEN if logits_given else 0) |
+                      (MOE_FUSE_GATHER if fuse_gather else 0))
 
 
-def config_from_workload(w, logits_given: bool = False) -> moe_config:
+def config_from_workload(w, logits_given: bool = False, fuse_gather: bool = False) -> moe_config:
     """moe_config from any object with the workload fields (T, d, N, f, k,
     mode, gamma, m, group_size, renorm, f_shared, dtype)."""
     return make_config(T=w.T, d=w.d, N=w.N, f=w.f, k=w.k, mode=w.mode, gamma=w.gamma, m=w.m,
                        group_size=w.group_size, renorm=w.renorm, f_shared=w.f_shared,
-                       dtype=w.dtype, logits_given=logits_given)
+                       dtype=w.dtype, logits_given=logits_given, fuse_gather=fuse_gather)
 
 
 def _p(t) -> Optional[int]:
@@ -242,6 +248,15 @@ def moe_expert_ffn_e4m3(cfg, xp, offsets, n_segments, rows_max, f, experts, op, 
                                      f, ctypes.byref(experts), _p(op), _p(ws),
                                      ws.numel() * ws.element_size(), _stream(stream)),
            "moe_expert_ffn_e4m3")
+
+
+def moe_expert_ffn_gather(cfg, x, row_token, offsets, n_segments, rows_max, f, W1, W3, W2, op, ws,
+                          stream=None) -> None:
+    """moe_expert_ffn whose first GEMM reads row r from x[row_token[r]] (bf16)."""
+    _check(lib().moe_expert_ffn_gather(ctypes.byref(cfg), _p(x), _p(row_token), _p(offsets),
+                                       n_segments, rows_max, f, _p(W1), _p(W3), _p(W2), _p(op),
+                                       _p(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "moe_expert_ffn_gather")
 
 
 def moe_expert_ffn_on_sms(cfg, xp, offsets, n_segments, rows_max, f, W1, W3, W2, op, max_sms, ws,

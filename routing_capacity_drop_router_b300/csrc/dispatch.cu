@@ -9,7 +9,9 @@
 // memory (N <= 256), then one warp per token:
 //   row(t, j) = offsets[e] + slot[t, j] for every kept slot j;
 //   tok_rows[t] = those rows sorted ascending (= ascending expert);
-//   x[t] is read once, 16 bytes per lane, and written to each of its rows.
+//   x[t] is read once, 16 bytes per lane, and written to each of its rows
+//   (skipped when xp is null: the expert GEMM then gathers the rows itself
+//   through row_token).
 #include <climits>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -116,7 +118,7 @@ __global__ void __launch_bounds__(kDispThreads) dispatch_kernel(
     __syncwarp();
     int32_t* tr = tok_rows + static_cast<size_t>(t) * kc;
     for (int j = lane; j < kc; j += 32) tr[j] = (j < nrows) ? rows[j] : -1;
-    if (nrows == 0) {
+    if (nrows == 0 || xp == nullptr) {
       __syncwarp();
       continue;
     }

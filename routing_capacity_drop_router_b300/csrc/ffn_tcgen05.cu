@@ -26,6 +26,14 @@
 //              is K-major, B is read as stored ([K, n] row-major = MN-major),
 //              so weights need no repack. In a pair both producers count
 //              their bytes on CTA 0's full barrier.
+//              Row-gather form (GATHER): A row r is row row_src[r] of the
+//              token matrix x, so the dispatched copy of x is never written.
+//              All 32 lanes copy the A tile with 16-byte cp.async into the
+//              same swizzled layout TMA would produce (lane: chunk lane % 8 of
+//              rows 4i + lane / 8); a k-block's rows are announced on the full
+//              barrier (one arrival per CTA, after the copies land and a proxy
+//              fence) while up to stages - 1 later k-blocks are in flight;
+//              lane 0 still loads B by TMA.
 //   warp 1   : allocates 512 TMEM columns (two 256-column accumulators);
 //              lane 0 of CTA 0 issues tcgen05.mma and tcgen05.commit, whose
 //              arrivals are multicast to both CTAs' barriers.
@@ -67,6 +75,7 @@ constexpr int kEpiWarps = 4;
 constexpr int kMaxSegments = 256;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 constexpr int kErrDeviceTimeout = -7;  // MOE_ERR_DEVICE_TIMEOUT
+constexpr int kErrDeviceBounds = -8;   // MOE_ERR_DEVICE_BOUNDS
 
 // Geometry of the pair (PAIR) and single-CTA forms.
 template <bool PAIR>
@@ -77,6 +86,8 @@ struct Geo {
   static constexpr int kTileRows = PAIR ? 2 * kBM : kBM;
   // bytes the MMA issuer's full barrier waits for per k-block (both CTAs)
   static constexpr uint32_t kTxBytes = (PAIR ? 2u : 1u) * static_cast<uint32_t>(kStageBytes);
+  // the same with A gathered by cp.async (B bytes only)
+  static constexpr uint32_t kTxBytesB = (PAIR ? 2u : 1u) * static_cast<uint32_t>(kBoxes * kBoxBytes);
   // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A bf16 (7-9 =
   // 1), B bf16 (10-12 = 1), A K-major (bit 15 = 0), B MN-major (bit 16 = 1),
   // N >> 3 in bits 17-22, M >> 4 in bits 24-28 (M = 256 for a pair).
@@ -136,12 +147,13 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t base) {
                  : "memory");
 }
 
-template <bool SWIGLU, bool PAIR>
+template <bool SWIGLU, bool PAIR, bool GATHER>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
     const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB1,
     const __grid_constant__ CUtensorMap tmB3, const int32_t* __restrict__ offsets, int S, int K,
     int n_out, int rows_max, __nv_bfloat16* __restrict__ out, int32_t* __restrict__ status,
-    int withhold_kb) {
+    int withhold_kb, const __nv_bfloat16* __restrict__ xg, const int32_t* __restrict__ row_src,
+    int x_rows) {
   using G = Geo<PAIR>;
   constexpr int kStages = G::kStages;
   extern __shared__ unsigned char smem_raw[];
@@ -162,7 +174,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
   // ---- set-up: barriers, tile table, TMEM ----
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&ctrl->full[s]), 1);
+      // GATHER: the expect_tx arrival plus one per CTA once its rows landed
+      mbar_init(smem_u32(&ctrl->full[s]), GATHER ? (PAIR ? 3 : 2) : 1);
       mbar_init(smem_u32(&ctrl->empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -235,14 +248,108 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
   };
 
   const uint32_t stage0 = base;
-  if (warp == 0 && lane == 0) {
-    // ---------------- TMA producer ----------------
+  // B tiles of one k-block: CTA 0 of a pair W1 (or B) columns col0.., CTA 1
+  // W3 columns col0.. (or B columns col0 + 128..); one CTA: all of them
+  auto load_b = [&](uint32_t sb, uint32_t fb, int seg, int col0, int kb) {
+    if (PAIR) {
+      const CUtensorMap* mb = (SWIGLU && rank == 1) ? &tmB3 : &tmB1;
+      const int c = SWIGLU ? col0 : col0 + static_cast<int>(rank) * 128;
+      tma_load_3d_pair(sb, mb, c, kb * kBK, seg, fb);
+      tma_load_3d_pair(sb + kBoxBytes, mb, c + 64, kb * kBK, seg, fb);
+    } else if (SWIGLU) {
+      tma_load_3d(sb + 0 * kBoxBytes, &tmB1, col0, kb * kBK, seg, fb);
+      tma_load_3d(sb + 1 * kBoxBytes, &tmB1, col0 + 64, kb * kBK, seg, fb);
+      tma_load_3d(sb + 2 * kBoxBytes, &tmB3, col0, kb * kBK, seg, fb);
+      tma_load_3d(sb + 3 * kBoxBytes, &tmB3, col0 + 64, kb * kBK, seg, fb);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        tma_load_3d(sb + j * kBoxBytes, &tmB1, col0 + 64 * j, kb * kBK, seg, fb);
+    }
+  };
+  if (warp == 0 && (GATHER || lane == 0)) {
+    // ---------------- producer ----------------
     int stage = 0;
     uint32_t phase = 0;
     int issued[kStages];
     uint32_t issued_phase[kStages];
     for (int s = 0; s < kStages; ++s) issued[s] = 0, issued_phase[s] = 0;
     bool ok = true;
+    if constexpr (GATHER) {
+      constexpr int kDepth = kStages - 1;  // k-blocks whose rows may still be in flight
+      constexpr int kRowsPerLane = kBM / 4;
+      const int rsub = lane >> 3, ch = lane & 7;
+      const int lim = min(ctrl->seg_row[S], rows_max);  // rows that have a token
+      int pend = 0, pend_stage = 0;  // k-blocks copied but not yet announced; the oldest
+      auto announce = [&]() {  // the oldest pending k-block's rows have landed
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          const uint32_t fb = smem_u32(&ctrl->full[pend_stage]);
+          if (PAIR) mbar_arrive_cluster(map_to_rank(fb, 0));
+          else mbar_arrive(fb);
+        }
+        pend_stage = pend_stage + 1 == kStages ? 0 : pend_stage + 1;
+        --pend;
+      };
+      for (int tile = unit; ok && tile < total; tile += n_units) {
+        int seg, row0, row_end, col0;
+        decode(tile, seg, row0, row_end, col0);
+        const int arow = row0 + static_cast<int>(rank) * kBM;
+        int tok[kRowsPerLane];  // source row of x, -1: zero row
+        bool bad = false;
+#pragma unroll
+        for (int i = 0; i < kRowsPerLane; ++i) {
+          const int r = arow + 4 * i + rsub;
+          int t = -1;
+          if (r < lim) {
+            t = row_src[r];
+            if (t < 0 || t >= x_rows) {
+              bad = true;
+              t = -1;
+            }
+          }
+          tok[i] = t;
+        }
+        if (bad) record_status(status, kErrDeviceBounds);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          int w = 1;
+          if (lane == 0)
+            w = mbar_wait(smem_u32(&ctrl->empty[stage]), phase ^ 1u, abort_flag, kWaitLimitNs);
+          if (!__shfl_sync(0xffffffffu, w, 0)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sa = stage0 + stage * G::kStageBytes;
+          if (lane == 0) {
+            const uint32_t fb_local = smem_u32(&ctrl->full[stage]);
+            if (rank == 0) mbar_expect_tx(fb_local, G::kTxBytesB);
+            issued[stage] = 1;
+            issued_phase[stage] = phase;
+            load_b(sa + kABytes, PAIR ? map_to_rank(fb_local, 0) : fb_local, seg, col0, kb);
+          }
+          const __nv_bfloat16* xk = xg + kb * kBK + ch * 8;
+#pragma unroll
+          for (int i = 0; i < kRowsPerLane; ++i) {
+            const int r = 4 * i + rsub;
+            const int t = tok[i];
+            cp_async16(sa + r * 128 + ((ch ^ (r & 7)) << 4),
+                       xk + static_cast<size_t>(t < 0 ? 0 : t) * K, t < 0 ? 0u : 16u);
+          }
+          cp_async_commit();
+          if (++pend == kDepth) {
+            cp_async_wait<kDepth - 1>();
+            announce();
+          }
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      cp_async_wait_all();  // every copy lands before its k-block is announced
+      while (pend > 0) announce();
+    } else {
     for (int tile = unit; ok && tile < total; tile += n_units) {
       int seg, row0, row_end, col0;
       decode(tile, seg, row0, row_end, col0);
@@ -262,28 +369,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
           // (failure-detection self-test: the withheld k-block is announced
           // but never loaded, so the MMA issuer's bounded wait expires)
           const uint32_t sa = stage0 + stage * G::kStageBytes;
-          const uint32_t sb = sa + kABytes;
-          if (PAIR) {
-            tma_load_2d_pair(sa, &tmA, kb * kBK, arow, fb);
-            // CTA 0: W1 (or B) columns col0.., CTA 1: W3 columns col0.. (or
-            // B columns col0 + 128..)
-            const CUtensorMap* mb = (SWIGLU && rank == 1) ? &tmB3 : &tmB1;
-            const int c = SWIGLU ? col0 : col0 + static_cast<int>(rank) * 128;
-            tma_load_3d_pair(sb, mb, c, kb * kBK, seg, fb);
-            tma_load_3d_pair(sb + kBoxBytes, mb, c + 64, kb * kBK, seg, fb);
-          } else {
-            tma_load_2d(sa, &tmA, kb * kBK, arow, fb);
-            if (SWIGLU) {
-              tma_load_3d(sb + 0 * kBoxBytes, &tmB1, col0, kb * kBK, seg, fb);
-              tma_load_3d(sb + 1 * kBoxBytes, &tmB1, col0 + 64, kb * kBK, seg, fb);
-              tma_load_3d(sb + 2 * kBoxBytes, &tmB3, col0, kb * kBK, seg, fb);
-              tma_load_3d(sb + 3 * kBoxBytes, &tmB3, col0 + 64, kb * kBK, seg, fb);
-            } else {
-#pragma unroll
-              for (int j = 0; j < 4; ++j)
-                tma_load_3d(sb + j * kBoxBytes, &tmB1, col0 + 64 * j, kb * kBK, seg, fb);
-            }
-          }
+          if (PAIR) tma_load_2d_pair(sa, &tmA, kb * kBK, arow, fb);
+          else tma_load_2d(sa, &tmA, kb * kBK, arow, fb);
+          load_b(sa + kABytes, fb, seg, col0, kb);
         }
         if (++stage == kStages) {
           stage = 0;
@@ -291,7 +379,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
         }
       }
     }
-    if (!ok) {  // copies in flight land before the CTA (or its pair) can exit (bounded)
+    }
+    if (!ok && lane == 0) {  // copies in flight land before the CTA (or its pair) can exit (bounded)
       if (rank == 0) {
         for (int s = 0; s < kStages; ++s) {
           if (!issued[s]) continue;
@@ -323,7 +412,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * kBN);
       for (int kb = 0; kb < num_kb; ++kb) {
-        if (!mbar_wait(smem_u32(&ctrl->full[stage]), phase, abort_flag, kWaitLimitNs)) {
+        // (row gather in a pair: CTA 1's rows are released at cluster scope)
+        const bool got =
+            (GATHER && PAIR)
+                ? mbar_wait_cluster(smem_u32(&ctrl->full[stage]), phase, abort_flag, kWaitLimitNs)
+                : mbar_wait(smem_u32(&ctrl->full[stage]), phase, abort_flag, kWaitLimitNs);
+        if (!got) {
           ok = false;
           break;
         }
@@ -436,8 +530,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
   }
 }
 
-// Clusters of 2 that can be resident at once (0: pairs unavailable).
-template <bool SWIGLU>
+// Clusters of 2 of the kernel that will be launched (its shared-memory
+// attribute already set) that can be resident at once (0: pairs unavailable).
+template <bool SWIGLU, bool GATHER>
 int pair_slots(int dev) {
   static int cached[64] = {};
   static bool done[64] = {};
@@ -455,7 +550,8 @@ int pair_slots(int dev) {
   cfg.dynamicSmemBytes = smem_bytes<true>();
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_tc_kernel<SWIGLU, true>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_tc_kernel<SWIGLU, true, GATHER>, &cfg) !=
+      cudaSuccess) {
     (void)cudaGetLastError();
     n = 0;
   }
@@ -464,35 +560,38 @@ int pair_slots(int dev) {
   return n;
 }
 
-template <bool SWIGLU, bool PAIR>
+template <bool SWIGLU, bool PAIR, bool GATHER>
 cudaError_t set_smem_attr(int dev) {
   static bool attr_set[64] = {};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (attr_set[dev]) return cudaSuccess;
-  const cudaError_t err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<SWIGLU, PAIR>,
+  const cudaError_t err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<SWIGLU, PAIR, GATHER>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                smem_bytes<PAIR>());
   if (err == cudaSuccess) attr_set[dev] = true;
   return err;
 }
 
-template <bool SWIGLU>
+template <bool SWIGLU, bool GATHER>
 cudaError_t launch_gemm(const CUtensorMap& mA, const CUtensorMap& mB1, const CUtensorMap& mB3,
                         const int32_t* offsets, int S, int64_t rows_max, int K, int n_out,
                         __nv_bfloat16* o, int32_t* status, cudaStream_t s, int withhold_kb,
-                        int max_sms) {
+                        int max_sms, const __nv_bfloat16* xg, const int32_t* row_src,
+                        int x_rows) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  if ((err = set_smem_attr<SWIGLU, true>(dev)) != cudaSuccess) return err;
-  if ((err = set_smem_attr<SWIGLU, false>(dev)) != cudaSuccess) return err;
+  if ((err = set_smem_attr<SWIGLU, true, GATHER>(dev)) != cudaSuccess) return err;
+  if ((err = set_smem_attr<SWIGLU, false, GATHER>(dev)) != cudaSuccess) return err;
   // Pairs pay off once segments average a 256-row tile; below that (decode
-  // batches) half of every pair tile would be padding.
+  // batches) half of every pair tile would be padding. The row-gather form
+  // runs one CTA per tile: its pairs wait on two CTAs' copies per k-block and
+  // measured about twice as slow.
   const char* env = getenv("MOE_GEMM_CTA_PAIRS");
-  const bool want_pairs = env ? env[0] != '0' : rows_max >= 2LL * kBM * S;
+  const bool want_pairs = env ? env[0] != '0' : (!GATHER && rows_max >= 2LL * kBM * S);
   int sms = device_sm_count();
   if (max_sms > 0 && max_sms < sms) sms = max_sms;  // confined to a slice of the GPU
-  int slots = want_pairs ? pair_slots<SWIGLU>(dev) : 0;
+  int slots = want_pairs ? pair_slots<SWIGLU, GATHER>(dev) : 0;
   if (slots > sms / 2) slots = sms / 2;
   const bool pair = slots > 0;
   const int tile_rows = pair ? 2 * kBM : kBM;
@@ -519,10 +618,12 @@ cudaError_t launch_gemm(const CUtensorMap& mA, const CUtensorMap& mB1, const CUt
   cfg.attrs = attr;
   cfg.numAttrs = pair ? 2 : 1;
   if (pair)
-    return cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<SWIGLU, true>, mA, mB1, mB3, offsets, S,
-                              K, n_out, rmax, o, status, withhold_kb);
-  return cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<SWIGLU, false>, mA, mB1, mB3, offsets, S,
-                            K, n_out, rmax, o, status, withhold_kb);
+    return cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<SWIGLU, true, GATHER>, mA, mB1, mB3,
+                              offsets, S, K, n_out, rmax, o, status, withhold_kb, xg, row_src,
+                              x_rows);
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<SWIGLU, false, GATHER>, mA, mB1, mB3,
+                            offsets, S, K, n_out, rmax, o, status, withhold_kb, xg, row_src,
+                            x_rows);
 }
 
 }  // namespace
@@ -531,24 +632,33 @@ cudaError_t launch_grouped_gemm_tc_bf16(const void* A, const int32_t* offsets, i
                                         int64_t rows_max, int K, int n_out, const void* B1,
                                         const void* B3, void* out, bool swiglu,
                                         int32_t* status, cudaStream_t s, int withhold_kb,
-                                        int max_sms) {
+                                        int max_sms, const int32_t* row_src, int a_rows) {
   if (S == 0 || rows_max == 0) return cudaSuccess;
   if (S > kMaxSegments) return cudaErrorInvalidValue;
+  if (row_src && (!swiglu || a_rows < 0 || K % kBK)) return cudaErrorInvalidValue;
   CUtensorMap mA, mB1, mB3;
-  if (!make_tmap_2d_bf16(&mA, A, static_cast<uint64_t>(rows_max), static_cast<uint64_t>(K), 64, kBM))
-    return cudaErrorInvalidValue;
   if (!make_tmap_3d_bf16(&mB1, B1, S, K, n_out, 64, kBK)) return cudaErrorInvalidValue;
+  if (row_src) {
+    mA = mB1;  // not read: A rows are gathered
+  } else if (!make_tmap_2d_bf16(&mA, A, static_cast<uint64_t>(rows_max), static_cast<uint64_t>(K),
+                                64, kBM)) {
+    return cudaErrorInvalidValue;
+  }
   if (swiglu) {
     if (!make_tmap_3d_bf16(&mB3, B3, S, K, n_out, 64, kBK)) return cudaErrorInvalidValue;
   } else {
     mB3 = mB1;
   }
   __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
+  const __nv_bfloat16* xg = static_cast<const __nv_bfloat16*>(A);
+  if (swiglu && row_src)
+    return launch_gemm<true, true>(mA, mB1, mB3, offsets, S, rows_max, K, n_out, o, status, s, -1,
+                                   max_sms, xg, row_src, a_rows);
   if (swiglu)
-    return launch_gemm<true>(mA, mB1, mB3, offsets, S, rows_max, K, n_out, o, status, s, withhold_kb,
-                             max_sms);
-  return launch_gemm<false>(mA, mB1, mB3, offsets, S, rows_max, K, n_out, o, status, s, withhold_kb,
-                            max_sms);
+    return launch_gemm<true, false>(mA, mB1, mB3, offsets, S, rows_max, K, n_out, o, status, s,
+                                    withhold_kb, max_sms, nullptr, nullptr, 0);
+  return launch_gemm<false, false>(mA, mB1, mB3, offsets, S, rows_max, K, n_out, o, status, s,
+                                   withhold_kb, max_sms, nullptr, nullptr, 0);
 }
 
 }  // namespace moe

@@ -122,12 +122,16 @@ cudaError_t launch_grouped_gemm_simt_f32(const float* A, const int32_t* offsets,
                                          cudaStream_t s);
 // withhold_kb >= 0 (self-test only): the first tile announces but never
 // loads its k-block withhold_kb, so a bounded wait expires. max_sms > 0 caps
-// the persistent grid at that many SMs.
+// the persistent grid at that many SMs. row_src (SwiGLU only): A is the
+// [a_rows, K] token matrix and row r of the product reads A[row_src[r]]
+// (rows at or past offsets[S] read zeros; an index outside [0, a_rows) reads
+// zeros and records MOE_ERR_DEVICE_BOUNDS).
 cudaError_t launch_grouped_gemm_tc_bf16(const void* A, const int32_t* offsets, int S,
                                         int64_t rows_max, int K, int n_out, const void* B1,
                                         const void* B3, void* out, bool swiglu,
                                         int32_t* status, cudaStream_t s, int withhold_kb = -1,
-                                        int max_sms = 0);
+                                        int max_sms = 0, const int32_t* row_src = nullptr,
+                                        int a_rows = 0);
 
 // y[t] = sum_r gate_r op[r] (+ shared[t]).
 cudaError_t launch_combine(int dtype, const void* op, const float* row_gate,

@@ -256,14 +256,18 @@ P* at(void* ws, size_t off) {
 
 
 // FFN over expert-contiguous rows; hp is scratch of rows_max * f elements;
-// status is the workspace's status word.
+// status is the workspace's status word. With row_src (bf16 only) xp is the
+// [a_rows, d] token matrix and GEMM1 reads row r of the segments from
+// xp[row_src[r]].
 int run_ffn(int dtype, const void* xp, const int32_t* offsets, int S, int64_t rows_max, int d,
             int f, const void* W1, const void* W3, const void* W2, void* hp, void* op,
-            int32_t* status, cudaStream_t s, Tracer* tr = nullptr, int max_sms = 0) {
+            int32_t* status, cudaStream_t s, Tracer* tr = nullptr, int max_sms = 0,
+            const int32_t* row_src = nullptr, int a_rows = 0) {
   cudaError_t e;
+  if (row_src && dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
   if (dtype == MOE_BF16) {
     e = launch_grouped_gemm_tc_bf16(xp, offsets, S, rows_max, d, f, W1, W3, hp, true, status, s, -1,
-                                    max_sms);
+                                    max_sms, row_src, a_rows);
     if (e != cudaSuccess || (tr && !tr->mark())) return MOE_ERR_LAUNCH;
     e = launch_grouped_gemm_tc_bf16(hp, offsets, S, rows_max, f, d, W2, nullptr, op, false, status,
                                     s, -1, max_sms);
@@ -408,6 +412,26 @@ int moe_expert_ffn(const moe_config* cfg, const void* xp, const int32_t* offsets
                  static_cast<int32_t*>(ws), as_stream(stream));
 }
 
+int moe_expert_ffn_gather(const moe_config* cfg, const void* x, const int32_t* row_token,
+                          const int32_t* offsets, int32_t n_segments, int64_t rows_max, int32_t f,
+                          const void* W1, const void* W3, const void* W2, void* op, void* ws,
+                          size_t ws_bytes, void* stream) {
+  if (!cfg) return MOE_ERR_NULL;
+  if (cfg->dtype != MOE_BF16) return cfg->dtype == MOE_F32 ? MOE_ERR_UNSUPPORTED : MOE_ERR_SHAPE;
+  if (cfg->T < 0 || cfg->d <= 0 || f <= 0 || n_segments < 0 || rows_max < 0) return MOE_ERR_SHAPE;
+  if (cfg->d % 64 || f % 64) return MOE_ERR_SHAPE;
+  if (n_segments > kMaxN) return MOE_ERR_UNSUPPORTED;
+  if (!offsets || !W1 || !W3 || !W2 || !op || !ws) return MOE_ERR_NULL;
+  if (!x || (rows_max > 0 && !row_token)) return MOE_ERR_NULL;
+  if (!aligned16(x) || !aligned16(W1) || !aligned16(W3) || !aligned16(W2) || !aligned16(op) ||
+      !aligned16(ws))
+    return MOE_ERR_ALIGN;
+  if (ws_bytes < moe_ffn_workspace_size(rows_max, f, cfg->dtype)) return MOE_ERR_WORKSPACE;
+  void* hp = static_cast<unsigned char*>(ws) + kCtrlBytes;
+  return run_ffn(cfg->dtype, x, offsets, n_segments, rows_max, cfg->d, f, W1, W3, W2, hp, op,
+                 static_cast<int32_t*>(ws), as_stream(stream), nullptr, 0, row_token, cfg->T);
+}
+
 int moe_expert_ffn_on_sms(const moe_config* cfg, const void* xp, const int32_t* offsets,
                           int32_t n_segments, int64_t rows_max, int32_t f, const void* W1,
                           const void* W3, const void* W2, void* op, int32_t max_sms, void* ws,
@@ -509,6 +533,8 @@ int layer_forward(const moe_config* cfg, const void* x, const void* W_router, co
   if (st != MOE_OK) return st;
   const moe_config& c = *cfg;
   const bool given = (c.flags & MOE_LOGITS_GIVEN) != 0;
+  // bf16 experts: GEMM1 gathers the token rows itself, dispatch copies none
+  const bool fuse = (c.flags & MOE_FUSE_GATHER) != 0 && c.dtype == MOE_BF16 && !w8;
   if (w8) {
     if ((st = check_e4m3(c, c.f, w8)) != MOE_OK) return st;
     W1 = w8->W1;
@@ -562,12 +588,17 @@ int layer_forward(const moe_config* cfg, const void* x, const void* W_router, co
       !tr.mark(1))
     return MOE_ERR_LAUNCH;
   if (launch_dispatch(c.dtype, x, cand_idx, cand_gate, slot, kept, c.T, c.d, c.N, d.kc,
-                      d.ec ? 1 : 0, d.rows_max, offsets, row_token, row_gate, tok_rows, xp,
-                      s) != cudaSuccess || !tr.mark(1))
+                      d.ec ? 1 : 0, d.rows_max, offsets, row_token, row_gate, tok_rows,
+                      fuse ? nullptr : xp, s) != cudaSuccess || !tr.mark(1))
     return MOE_ERR_LAUNCH;
-  st = w8 ? run_ffn_e4m3(xp, offsets, c.N, d.rows_max, c.d, c.f, *w8, hp, op, status, s, &tr)
-          : run_ffn(c.dtype, xp, offsets, c.N, d.rows_max, c.d, c.f, W1, W3, W2, hp, op, status, s,
-                    &tr);
+  if (w8)
+    st = run_ffn_e4m3(xp, offsets, c.N, d.rows_max, c.d, c.f, *w8, hp, op, status, s, &tr);
+  else if (fuse)
+    st = run_ffn(c.dtype, x, offsets, c.N, d.rows_max, c.d, c.f, W1, W3, W2, hp, op, status, s,
+                 &tr, 0, row_token, c.T);
+  else
+    st = run_ffn(c.dtype, xp, offsets, c.N, d.rows_max, c.d, c.f, W1, W3, W2, hp, op, status, s,
+                 &tr);
   if (st != MOE_OK) return st;
   if (c.f_shared > 0) {
     if (c.T > 0) {

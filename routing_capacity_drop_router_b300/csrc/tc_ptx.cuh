@@ -201,6 +201,25 @@ __device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
                : "memory");
 }
 
+// ---- 16-byte asynchronous copies global -> shared (row gathers) ----
+// src_bytes 16 copies, 0 writes 16 zero bytes and reads nothing. The copy is
+// cached in L2 only.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// Wait until at most N of this thread's committed groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format: start
 // address >> 4 in bits 0-13, leading byte offset >> 4 in 16-29, stride byte
 // offset >> 4 in 32-45, descriptor version 1 in 46-47, swizzle mode 2 =

@@ -112,9 +112,10 @@ def compare_routing(w: W.Workload, g: Dict[str, np.ndarray], L: np.ndarray, home
 
 
 def layer_gpu(w: W.Workload, inp: Dict[str, torch.Tensor], logits: Optional[np.ndarray] = None,
-              home_group=None, want_views: bool = False):
-    """moe_layer_forward on the GPU. ``logits`` given -> MOE_LOGITS_GIVEN."""
-    cfg = M.config_from_workload(w, logits_given=logits is not None)
+              home_group=None, want_views: bool = False, fuse_gather: bool = False):
+    """moe_layer_forward on the GPU. ``logits`` given -> MOE_LOGITS_GIVEN;
+    ``fuse_gather`` -> MOE_FUSE_GATHER."""
+    cfg = M.config_from_workload(w, logits_given=logits is not None, fuse_gather=fuse_gather)
     dev = torch.device("cuda")
     ws = torch.zeros(M.workspace_size(cfg), dtype=torch.uint8, device=dev)  # status word = 0
     dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32

@@ -169,6 +169,36 @@ def test_expert_ffn_on_sms_host_checks():
     assert lib.moe_expert_ffn_on_sms(None, *args, 4, fake, need, None) == M.MOE_ERR_NULL
 
 
+def test_expert_ffn_gather_host_checks():
+    """moe_expert_ffn_gather rejects every bad argument before any launch."""
+    lib = M.lib()
+    fake = ctypes.c_void_p(1 << 20)
+    bf = M.make_config(T=8, d=64, N=2, f=64, k=1, dtype="bf16")
+    f32 = M.make_config(T=8, d=64, N=2, f=64, k=1, dtype="f32")
+    odd = M.make_config(T=8, d=96, N=2, f=64, k=1, dtype="bf16")
+    need = M.ffn_workspace_size(8, 64, "bf16")
+
+    def call(cfg, x=fake, row_token=fake, ws=fake, ws_bytes=need, f=64, W2=fake):
+        return lib.moe_expert_ffn_gather(cfg, x, row_token, fake, 2, 8, f, fake, fake, W2, fake,
+                                         ws, ws_bytes, None)
+
+    assert call(ctypes.byref(f32)) == M.MOE_ERR_UNSUPPORTED
+    assert call(ctypes.byref(odd)) == M.MOE_ERR_SHAPE
+    assert call(ctypes.byref(bf), f=100) == M.MOE_ERR_SHAPE
+    assert call(None) == M.MOE_ERR_NULL
+    assert call(ctypes.byref(bf), x=None) == M.MOE_ERR_NULL
+    assert call(ctypes.byref(bf), row_token=None) == M.MOE_ERR_NULL
+    assert call(ctypes.byref(bf), W2=None) == M.MOE_ERR_NULL
+    assert call(ctypes.byref(bf), x=ctypes.c_void_p((1 << 20) + 8)) == M.MOE_ERR_ALIGN
+    assert call(ctypes.byref(bf), ws_bytes=need - 1) == M.MOE_ERR_WORKSPACE
+
+
+def test_fuse_gather_flag_in_config():
+    cfg = M.make_config(T=8, d=64, N=2, f=64, k=1, fuse_gather=True, logits_given=True)
+    assert cfg.flags == M.MOE_FUSE_GATHER | M.MOE_LOGITS_GIVEN
+    assert M.sizes(cfg).workspace == M.sizes(M.make_config(T=8, d=64, N=2, f=64, k=1)).workspace
+
+
 def test_e4m3_experts_host_checks():
     lib = M.lib()
     fake = ctypes.c_void_p(1 << 20)

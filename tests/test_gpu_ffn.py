@@ -95,6 +95,89 @@ def test_expert_ffn_bf16_against_oracle(sizes, d, f, gemm_form):
         G.assert_output_close(got[a:b], ref, "bf16", f"segment {s}")
 
 
+@pytest.mark.parametrize("sizes,d,f,T", [
+    ([130, 0, 170, 1, 249], 256, 384, 300),
+    ([3, 500, 64, 0, 0, 257], 512, 256, 700),   # several 256-row tiles, empty segments
+    ([77, 300, 5], 2048, 512, 200),             # long K: the row ring wraps many times
+    ([1000], 128, 128, 1000),                   # one k-block per tile
+])
+def test_expert_ffn_gather_equals_copy(sizes, d, f, T, gemm_form):
+    """moe_expert_ffn_gather on (x, row_token) computes the same bits as
+    moe_expert_ffn on the copied rows xp[r] = x[row_token[r]] (tokens repeat,
+    as under top-k), and matches the oracle; rows past the segments stay
+    untouched."""
+    S = len(sizes)
+    off = _segments(sizes)
+    P = int(off[-1])
+    rows_max = P + 37
+    x = _rand((T, d), 21)
+    row_token = np.random.default_rng(22).integers(0, T, size=rows_max).astype(np.int32)
+    W1 = _rand((S, d, f), 23, d ** -0.5)
+    W3 = _rand((S, d, f), 24, d ** -0.5)
+    W2 = _rand((S, f, d), 25, f ** -0.5)
+    dev = torch.device("cuda")
+    xg, rt = x.cuda(), torch.from_numpy(row_token).cuda()
+    xp = xg[rt.long()].contiguous()
+    offg = torch.from_numpy(off).cuda()
+    W1g, W3g, W2g = W1.cuda(), W3.cuda(), W2.cuda()
+    ws = torch.zeros(M.ffn_workspace_size(rows_max, f, "bf16"), dtype=torch.uint8, device=dev)
+    cfg = M.make_config(T=T, d=d, N=S, f=f, k=1, dtype="bf16")
+    copy = torch.full((rows_max, d), 7.0, dtype=torch.bfloat16, device=dev)
+    M.moe_expert_ffn(cfg, xp, offg, S, rows_max, f, W1g, W3g, W2g, copy, ws)
+    fused = torch.full((rows_max, d), 7.0, dtype=torch.bfloat16, device=dev)
+    M.moe_expert_ffn_gather(cfg, xg, rt, offg, S, rows_max, f, W1g, W3g, W2g, fused, ws)
+    torch.cuda.synchronize()
+    assert M.moe_get_device_status(ws) == M.MOE_OK
+    assert torch.equal(fused[:P], copy[:P])
+    assert torch.all(fused[P:] == 7.0), "rows past the last segment were written"
+    got = fused.float().cpu().numpy()
+    xs = x[torch.from_numpy(row_token).long()]
+    for s in range(S):
+        a, b = int(off[s]), int(off[s + 1])
+        if a < b:
+            ref = O.swiglu(G.np32(xs[a:b]), G.np32(W1[s]), G.np32(W3[s]), G.np32(W2[s]), "bf16")
+            G.assert_output_close(got[a:b], ref, "bf16", f"segment {s}")
+
+
+def test_expert_ffn_gather_out_of_range_token_reads_zeros(gemm_form):
+    """A row_token entry outside [0, T) is caught by the kernel's own bounds
+    check: that row reads zeros (its output is exactly 0) and the status word
+    records MOE_ERR_DEVICE_BOUNDS; every other row is unaffected."""
+    sizes, d, f, T = [200, 90, 300], 256, 256, 400
+    S = len(sizes)
+    off = _segments(sizes)
+    P = int(off[-1])
+    rows_max = P
+    x = _rand((T, d), 31)
+    row_token = np.random.default_rng(32).integers(0, T, size=rows_max).astype(np.int32)
+    bad = [5, 260, P - 1]
+    row_token[bad] = [T, -3, 1 << 30]
+    W1 = _rand((S, d, f), 33, d ** -0.5).cuda()
+    W3 = _rand((S, d, f), 34, d ** -0.5).cuda()
+    W2 = _rand((S, f, d), 35, f ** -0.5).cuda()
+    dev = torch.device("cuda")
+    xg = x.cuda()
+    rt = torch.from_numpy(row_token).cuda()
+    xp = xg[rt.clamp(0, T - 1).long()].contiguous()
+    xp[bad] = 0
+    offg = torch.from_numpy(off).cuda()
+    cfg = M.make_config(T=T, d=d, N=S, f=f, k=1, dtype="bf16")
+    ws = torch.zeros(M.ffn_workspace_size(rows_max, f, "bf16"), dtype=torch.uint8, device=dev)
+    copy = torch.empty((rows_max, d), dtype=torch.bfloat16, device=dev)
+    M.moe_expert_ffn(cfg, xp, offg, S, rows_max, f, W1, W3, W2, copy, ws)
+    torch.cuda.synchronize()
+    assert M.moe_get_device_status(ws) == M.MOE_OK
+    fused = torch.empty_like(copy)
+    M.moe_expert_ffn_gather(cfg, xg, rt, offg, S, rows_max, f, W1, W3, W2, fused, ws)
+    torch.cuda.synchronize()
+    assert M.moe_get_device_status(ws) == M.MOE_ERR_DEVICE_BOUNDS
+    assert not fused[bad].any()
+    assert torch.equal(fused, copy)
+    M.moe_clear_device_status(ws)
+    torch.cuda.synchronize()
+    assert M.moe_get_device_status(ws) == M.MOE_OK
+
+
 def test_expert_ffn_on_a_slice_of_the_gpu():
     """moe_expert_ffn_on_sms: the same rows as moe_expert_ffn on any number of
     SMs, and a device group's call (offsets and weights pointing at its first

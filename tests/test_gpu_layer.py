@@ -77,6 +77,41 @@ def test_tiny_fp32_workload_full():
     _check_own_logits(w, inp, L, ref)
 
 
+FUSABLE = [w for w in SMALL if w.dtype == "bf16" and w.weights == "same"]
+
+
+@pytest.mark.parametrize("w", FUSABLE, ids=[w.name for w in FUSABLE])
+def test_small_layer_fused_gather(w):
+    """MOE_FUSE_GATHER: GEMM1 reads the token rows through row_token; the
+    layer output is the same bits as with the dispatched copy, and within
+    tolerance of the oracle."""
+    inp = W.make_inputs(w)
+    L = O.router_logits(G.np32(inp["x"]), G.np32(inp["W_r"]), G.np32(inp["bias"]))
+    ref = G.oracle_layer(w, inp, logits=L)
+    copy = G.layer_gpu(w, inp, logits=L)
+    fused = G.layer_gpu(w, inp, logits=L, fuse_gather=True, want_views=True)
+    assert np.array_equal(fused["y"], copy["y"])
+    assert np.array_equal(fused["kept"], ref["kept"])
+    G.assert_output_close(fused["y"][ref["tokens"]], ref["y"], w.dtype)
+
+
+@pytest.mark.parametrize("name", ["mixtral_bf16_gamma1", "expert_choice_bf16",
+                                  "finegrained_bf16_expanded"])
+def test_fused_gather_full_size(name):
+    """The benchmark workloads at full size with MOE_FUSE_GATHER: the same
+    output bits as the copy path, and a token sample within tolerance of the
+    oracle."""
+    w = W.ALL[name]
+    inp = W.make_inputs(w)
+    L = O.router_logits(G.np32(inp["x"]), G.np32(inp["W_r"]), G.np32(inp["bias"]))
+    copy = G.layer_gpu(w, inp, logits=L)
+    fused = G.layer_gpu(w, inp, logits=L, fuse_gather=True)
+    assert np.array_equal(fused["y"], copy["y"])
+    tokens = np.sort(np.random.default_rng(1).choice(w.T, size=16, replace=False))
+    ref = G.oracle_layer(w, inp, logits=L, tokens=tokens)
+    G.assert_output_close(fused["y"][ref["tokens"]], ref["y"], w.dtype)
+
+
 def test_capacity_zero_outputs_zero():
     w = W.Workload("zero_cap", T=200, d=128, N=8, f=128, k=2, mode=W.CAPACITY_DROP, gamma=0.0)
     inp = W.make_inputs(w)
