@@ -112,6 +112,39 @@ def test_fused_gather_full_size(name):
     G.assert_output_close(fused["y"][ref["tokens"]], ref["y"], w.dtype)
 
 
+DEGENERATE = [
+    W.Workload("one_token_top1", T=1, d=128, N=8, f=128, k=1),
+    W.Workload("one_token_no_room", T=1, d=128, N=8, f=128, k=2, mode=W.CAPACITY_DROP,
+               gamma=1.0),  # C = floor(1.0 * 2 * 1 / 8) = 0: the token is dropped everywhere
+    W.Workload("every_expert", T=300, d=128, N=8, f=128, k=8, renorm=True),  # dense mixture
+    W.Workload("every_expert_choice", T=64, d=128, N=8, f=128, k=8,
+               mode=W.EXPERT_CHOICE),  # c = T: each expert takes every token
+]
+
+
+@pytest.mark.parametrize("fuse", [False, True], ids=["copy", "fused_gather"])
+@pytest.mark.parametrize("w", DEGENERATE, ids=[w.name for w in DEGENERATE])
+def test_degenerate_layers(w, fuse):
+    """The method's degenerate cases through the whole layer: one token, no
+    room at all, every expert per token (token and expert choice)."""
+    inp = W.make_inputs(w)
+    L = O.router_logits(G.np32(inp["x"]), G.np32(inp["W_r"]), G.np32(inp["bias"]))
+    ref = G.oracle_layer(w, inp, logits=L)
+    got = G.layer_gpu(w, inp, logits=L, want_views=True, fuse_gather=fuse)
+    assert np.array_equal(got["kept"], ref["kept"])
+    G.assert_output_close(got["y"], ref["y"], w.dtype)
+
+
+def test_empty_layer():
+    """T = 0 through the whole layer: nothing routed, nothing written, no error."""
+    w = W.Workload("empty_layer", T=0, d=128, N=8, f=128, k=2, mode=W.CAPACITY_DROP, gamma=1.0)
+    inp = W.make_inputs(w)
+    got = G.layer_gpu(w, inp, want_views=True)
+    assert got["y"].shape == (0, w.d)
+    assert (got["kept"] == 0).all()
+    assert got["stats"][0] == 0
+
+
 def test_capacity_zero_outputs_zero():
     w = W.Workload("zero_cap", T=200, d=128, N=8, f=128, k=2, mode=W.CAPACITY_DROP, gamma=0.0)
     inp = W.make_inputs(w)
