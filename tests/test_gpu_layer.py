@@ -119,14 +119,19 @@ DEGENERATE = [
     W.Workload("every_expert", T=300, d=128, N=8, f=128, k=8, renorm=True),  # dense mixture
     W.Workload("every_expert_choice", T=64, d=128, N=8, f=128, k=8,
                mode=W.EXPERT_CHOICE),  # c = T: each expert takes every token
+    # the limits: 256 experts (one GEMM segment each), 32 candidate slots per token
+    W.Workload("max_experts", T=300, d=64, N=256, f=64, k=8, mode=W.CAPACITY_DROP, gamma=1.0),
+    W.Workload("max_slots", T=200, d=64, N=64, f=64, k=24, m=8, group_size=16,
+               mode=W.CAPACITY_DROP, gamma=1.25),
 ]
 
 
 @pytest.mark.parametrize("fuse", [False, True], ids=["copy", "fused_gather"])
 @pytest.mark.parametrize("w", DEGENERATE, ids=[w.name for w in DEGENERATE])
 def test_degenerate_layers(w, fuse):
-    """The method's degenerate cases through the whole layer: one token, no
-    room at all, every expert per token (token and expert choice)."""
+    """The method's degenerate cases through the whole layer (one token, no
+    room at all, every expert per token under token and expert choice) and
+    its limits (256 experts, 32 candidate slots)."""
     inp = W.make_inputs(w)
     L = O.router_logits(G.np32(inp["x"]), G.np32(inp["W_r"]), G.np32(inp["bias"]))
     ref = G.oracle_layer(w, inp, logits=L)
