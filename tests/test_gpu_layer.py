@@ -123,6 +123,10 @@ DEGENERATE = [
     W.Workload("max_experts", T=300, d=64, N=256, f=64, k=8, mode=W.CAPACITY_DROP, gamma=1.0),
     W.Workload("max_slots", T=200, d=64, N=64, f=64, k=24, m=8, group_size=16,
                mode=W.CAPACITY_DROP, gamma=1.25),
+    # the fp32 path (FMA GEMMs; the fused-gather flag does not apply to it)
+    W.Workload("one_token_f32", T=1, d=64, N=8, f=96, k=2, dtype="f32"),
+    W.Workload("max_experts_f32", T=300, d=64, N=256, f=64, k=8, mode=W.CAPACITY_DROP,
+               gamma=1.0, dtype="f32"),
 ]
 
 
