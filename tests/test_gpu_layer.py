@@ -144,6 +144,39 @@ def test_degenerate_layers(w, fuse):
     G.assert_output_close(got["y"], ref["y"], w.dtype)
 
 
+@pytest.mark.parametrize("w", [
+    W.Workload("repeat_drop_expanded_shared", T=3000, d=256, N=64, f=128, k=6, m=2,
+               group_size=8, mode=W.CAPACITY_DROP, gamma=1.25, f_shared=128, zipf_s=1.0),
+    W.Workload("repeat_device", T=3000, d=256, N=64, f=128, k=6, group_size=8,
+               mode=W.CAPACITY_DROP_DEVICE, gamma=1.0, zipf_s=1.0),
+    W.Workload("repeat_ec", T=2048, d=256, N=16, f=128, k=2, mode=W.EXPERT_CHOICE),
+], ids=lambda w: w.name)
+def test_repeated_calls_on_one_workspace_are_bitwise_identical(w):
+    """Five back-to-back layer calls (own router logits) on one workspace that
+    is never re-zeroed: every call leaves the control block as it found it and
+    nothing depends on the order of atomics, so logits, y and the statistics
+    repeat bit for bit."""
+    inp = W.make_inputs(w)
+    cfg = G.M.config_from_workload(w)
+    dev = torch.device("cuda")
+    ws = torch.zeros(G.M.workspace_size(cfg), dtype=torch.uint8, device=dev)
+    d = {k: G.cuda(inp.get(k)) for k in ("x", "W_r", "bias", "W1", "W3", "W2", "Ws1", "Ws3", "Ws2")}
+    outs = []
+    for _ in range(5):
+        y = torch.empty((w.T, w.d), dtype=torch.bfloat16, device=dev)
+        L = torch.empty((w.T, w.N), dtype=torch.float32, device=dev)
+        st = torch.zeros(G.M.MOE_STATS_LEN, dtype=torch.float64, device=dev)
+        G.M.moe_layer_forward(cfg, d["x"], d["W_r"], d["bias"], d["W1"], d["W3"], d["W2"],
+                              d["Ws1"], d["Ws3"], d["Ws2"], y, ws, logits=L, stats=st)
+        outs.append((y, L, st))
+    torch.cuda.synchronize()
+    assert G.M.moe_get_device_status(ws) == G.M.MOE_OK
+    y0, L0, s0 = outs[0]
+    for y, L, st in outs[1:]:
+        assert torch.equal(L, L0) and torch.equal(y, y0) and torch.equal(st, s0)
+    assert s0[0].item() > 0
+
+
 def test_empty_layer():
     """T = 0 through the whole layer: nothing routed, nothing written, no error."""
     w = W.Workload("empty_layer", T=0, d=128, N=8, f=128, k=2, mode=W.CAPACITY_DROP, gamma=1.0)
