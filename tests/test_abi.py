@@ -232,6 +232,8 @@ def test_layer_stage_list_follows_the_config():
     names = M.moe_layer_stages(_cfg(dtype="f32"))
     assert names[:2] == ["router_logits", "route_tokens"]
     assert M.lib().moe_layer_stages(ctypes.byref(_cfg(N=0)), None, 0) == M.MOE_ERR_SHAPE
+    # the fused gather launches the same six kernels (dispatch keeps the row tables)
+    assert M.moe_layer_stages(_cfg(fuse_gather=True)) == M.moe_layer_stages(_cfg())
 
 
 def test_trace_event_arguments_checked_on_the_host():
