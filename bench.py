@@ -554,7 +554,8 @@ def run_ours(args, rank, world, local_rank):
         "launch": "programmatic dependent launch; events only around the expert GEMMs",
         "clocks": clk,
         "cpu_baseline": cpu,
-        "stats": {"max_over_mean": float(st[4]), "drop_fraction": float(st[5]),
+        "stats": {"kept_pairs": float(st[0]), "max_over_mean": float(st[4]),
+                  "drop_fraction": float(st[5]), "balance": float(st[6]),
                   "balance_times_N": float(st[7])},
     }
     print(json.dumps(line), flush=True)
