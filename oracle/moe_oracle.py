@@ -75,9 +75,12 @@ F32 = np.float32
 def round_bf16(v) -> np.ndarray:
     """Round to the nearest bf16 value (ties to even), returned as fp32.
 
-    Works on the fp64 bit pattern so a fp64 value is rounded once, not twice.
-    Exact for every value whose magnitude is at least 2**-126 (bf16 normals);
-    smaller magnitudes are flushed to zero.
+    Works on the fp64 value so it is rounded once, not twice. bf16 has the
+    exponent range of fp32 and 8 significant bits: a normal magnitude (at
+    least 2**-126) keeps the top 8 bits of its significand; below 2**-126 the
+    bf16 values are the subnormals m * 2**-133 (m = 0..127), so the value is
+    rounded to the nearest multiple of 2**-133, ties to even m (m = 128 is
+    the smallest normal, 2**-126).
     """
     a = np.asarray(v, dtype=np.float64)
     bits = a.view(np.uint64)
@@ -85,7 +88,9 @@ def round_bf16(v) -> np.ndarray:
     lsb = (bits >> np.uint64(45)) & np.uint64(1)
     rounded = (bits + np.uint64((1 << 44) - 1) + lsb) & ~np.uint64((1 << 45) - 1)
     out = rounded.view(np.float64)
-    out = np.where(np.abs(a) < 2.0 ** -126, 0.0, out)
+    # a * 2**133 is exact in fp64 and np.rint rounds half to even
+    sub = np.rint(a * 2.0 ** 133) * 2.0 ** -133
+    out = np.where(np.abs(a) < 2.0 ** -126, sub, out)
     return out.astype(np.float32)
 
 

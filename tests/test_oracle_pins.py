@@ -70,6 +70,28 @@ def test_round_bf16_matches_torch_and_rounds_once():
     assert O.round_bf16(np.array([1.0 + 2.0 ** -8]))[0] == F32(1.0)
 
 
+def test_round_bf16_subnormals_round_to_nearest_even():
+    # bf16 subnormals are m * 2**-133, m = 1..127; the rounding keeps them
+    # (round to nearest, ties to even m) instead of flushing to zero
+    q = 2.0 ** -133
+    cases = [(0.5 * q, 0.0), (0.75 * q, q), (1.5 * q, 2 * q), (2.5 * q, 2 * q), (3.5 * q, 4 * q),
+             (-1.25 * q, -q), (127.5 * q, 128 * q), (2.0 ** -126 - 2.0 ** -140, 2.0 ** -126),
+             (2.0 ** -126, 2.0 ** -126), (1e-45, 0.0)]
+    got = O.round_bf16(np.array([a for a, _ in cases]))
+    assert got.tolist() == [F32(b) for _, b in cases]
+    # a single rounding from fp64: just above a subnormal midpoint goes up
+    assert O.round_bf16(np.array([0.5 * q + 2.0 ** -170]))[0] == F32(q)
+    # against torch's fp32 -> bf16 conversion over the whole subnormal range
+    # and across the boundary 2**-126
+    rng = np.random.default_rng(31)
+    v = np.concatenate([rng.uniform(-2.0 ** -126, 2.0 ** -126, 50000),
+                        rng.uniform(2.0 ** -127, 2.0 ** -125, 20000),
+                        np.arange(-300, 300) * 2.0 ** -135]).astype(F32)
+    ref = torch.from_numpy(v).to(torch.bfloat16).float().numpy()
+    assert np.array_equal(O.round_bf16(v), ref)
+    assert np.count_nonzero(ref[np.abs(v) < 2.0 ** -126]) > 40000
+
+
 # ------------------------------------------------------------ softmax / logits
 
 def test_router_logits_closed_form():
