@@ -40,6 +40,7 @@ def _check_layer(w, inp, tokens=None):
     got = G.layer_gpu(w, inp, logits=L, want_views=True)
     assert np.array_equal(got["kept"], ref["kept"])
     assert np.array_equal(got["keep"].astype(bool), ref["keep"])
+    assert np.array_equal(got["coverage"], ref["coverage"])
     rows = ref["tokens"]
     G.assert_output_close(got["y"][rows], ref["y"], w.dtype)
     s = O.load_stats(ref["demand"], ref["kept"], ref["p"])
@@ -107,7 +108,8 @@ def test_fused_gather_full_size(name):
     copy = G.layer_gpu(w, inp, logits=L)
     fused = G.layer_gpu(w, inp, logits=L, fuse_gather=True)
     assert np.array_equal(fused["y"], copy["y"])
-    tokens = np.sort(np.random.default_rng(1).choice(w.T, size=16, replace=False))
+    tokens = np.union1d(np.random.default_rng(1).choice(w.T, size=16, replace=False),
+                        G.tile_edge_tokens(w, L))
     ref = G.oracle_layer(w, inp, logits=L, tokens=tokens)
     G.assert_output_close(fused["y"][ref["tokens"]], ref["y"], w.dtype)
 
@@ -216,12 +218,17 @@ def test_gamma_inf_equals_token_choice_bitwise():
     ("decode_bf16_w8", None),
 ])
 def test_benchmark_workloads_full_size(name, sample):
+    """Full size. Sampled workloads check a random token sample plus every
+    token at the first or last row of a 128-row tile of an expert segment, so
+    that every tile of both GEMMs is checked at the full d and f depth."""
     w = W.ALL[name]
     inp = W.make_inputs(w)
     tokens = None
     if sample is not None:
         rng = np.random.default_rng(0)
-        tokens = np.sort(rng.choice(w.T, size=sample, replace=False))
+        L0 = O.router_logits(G.np32(inp["x"]), G.np32(inp["W_r"]), G.np32(inp["bias"]))
+        tokens = np.union1d(rng.choice(w.T, size=sample, replace=False),
+                            G.tile_edge_tokens(w, L0))
     L, ref, _ = _check_layer(w, inp, tokens=tokens)
     _check_own_logits(w, inp, L, ref, tokens=tokens)
 
