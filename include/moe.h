@@ -218,13 +218,19 @@ int moe_capacity_drop(const moe_config* cfg, const int32_t* cand_idx, const floa
  *   row_gate       [rows_max] fp32 out: gate of each row
  *   tok_rows       [T, kc] int32 out: rows of each token in ascending expert
  *                  order (= ascending row), padded with -1
+ *   coverage       [T] int32 out, nullable: the number of kept pairs of each
+ *                  token. Under expert choice this is how many experts took
+ *                  the token: some tokens are taken by several experts and
+ *                  some by none ("MoE vs MoT", section "Mixture of Tokens");
+ *                  it sums to N * c. Under token choice and drop it is the
+ *                  token's surviving candidates.
  *   xp             [rows_max, d] dtype out: xp[r] = x[row_token[r]]
  * Rows inside an expert are in ascending token order. Rows >= P are not written.
  */
 int moe_dispatch(const moe_config* cfg, const void* x, const int32_t* cand_idx,
                  const float* cand_gate, const int32_t* slot, const int32_t* kept,
                  int32_t* expert_offsets, int32_t* row_token, float* row_gate,
-                 int32_t* tok_rows, void* xp, void* stream);
+                 int32_t* tok_rows, int32_t* coverage, void* xp, void* stream);
 
 /*
  * Grouped SwiGLU experts over expert-contiguous rows ("MoE vs MoT", section
@@ -485,6 +491,7 @@ typedef struct moe_views_t {
   void*    xp;             /* [rows_max, d] (not written with MOE_FUSE_GATHER) */
   void*    op;             /* [rows_max, d] */
   void*    shared_out;     /* [T, d] or NULL */
+  int32_t* coverage;       /* [T] kept pairs per token (moe_dispatch's coverage) */
 } moe_views_t;
 
 /* Carve `ws` into the views above. Host only; no CUDA call. */

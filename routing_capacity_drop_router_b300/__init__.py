@@ -72,7 +72,8 @@ class moe_e4m3_experts(ctypes.Structure):
 class moe_views_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "status", "logits", "scores", "cand_idx", "cand_gate", "slot", "keep", "demand", "kept",
-        "expert_offsets", "row_token", "row_gate", "tok_rows", "xp", "op", "shared_out")]
+        "expert_offsets", "row_token", "row_gate", "tok_rows", "xp", "op", "shared_out",
+        "coverage")]
 
 
 # name -> (restype, argtypes)
@@ -86,7 +87,8 @@ SIGNATURES = {
     "moe_route": (ctypes.c_int, [_CFG, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                  ctypes.c_size_t, _VP]),
     "moe_capacity_drop": (ctypes.c_int, [_CFG, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
-    "moe_dispatch": (ctypes.c_int, [_CFG, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "moe_dispatch": (ctypes.c_int, [_CFG, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                    _VP]),
     "moe_expert_ffn": (ctypes.c_int, [_CFG, _VP, _VP, ctypes.c_int32, ctypes.c_int64,
                                       ctypes.c_int32, _VP, _VP, _VP, _VP, _VP, ctypes.c_size_t,
                                       _VP]),
@@ -224,10 +226,11 @@ def moe_capacity_drop(cfg, cand_idx, cand_gate, slot, keep, demand, kept, stream
 
 
 def moe_dispatch(cfg, x, cand_idx, cand_gate, slot, kept, expert_offsets, row_token, row_gate,
-                 tok_rows, xp, stream=None) -> None:
+                 tok_rows, xp, coverage=None, stream=None) -> None:
     _check(lib().moe_dispatch(ctypes.byref(cfg), _p(x), _p(cand_idx), _p(cand_gate), _p(slot),
                               _p(kept), _p(expert_offsets), _p(row_token), _p(row_gate),
-                              _p(tok_rows), _p(xp), _stream(stream)), "moe_dispatch")
+                              _p(tok_rows), _p(coverage), _p(xp), _stream(stream)),
+           "moe_dispatch")
 
 
 def moe_expert_ffn(cfg, xp, offsets, n_segments, rows_max, f, W1, W3, W2, op, ws,

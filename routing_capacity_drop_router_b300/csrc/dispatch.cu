@@ -9,6 +9,7 @@
 // memory (N <= 256), then one warp per token:
 //   row(t, j) = offsets[e] + slot[t, j] for every kept slot j;
 //   tok_rows[t] = those rows sorted ascending (= ascending expert);
+//   coverage[t] = how many rows token t has (the experts that took it);
 //   x[t] is read once, 16 bytes per lane, and written to each of its rows
 //   (skipped when xp is null: the expert GEMM then gathers the rows itself
 //   through row_token).
@@ -60,7 +61,8 @@ __global__ void __launch_bounds__(kDispThreads) dispatch_kernel(
     const int32_t* __restrict__ kept, int T, int d, int N, int kc, int expert_choice,
     int rows_max,
     int32_t* __restrict__ expert_offsets, int32_t* __restrict__ row_token,
-    float* __restrict__ row_gate, int32_t* __restrict__ tok_rows, E* __restrict__ xp) {
+    float* __restrict__ row_gate, int32_t* __restrict__ tok_rows,
+    int32_t* __restrict__ coverage, E* __restrict__ xp) {
   __shared__ int s_off[257];
   __shared__ int s_rows[kDispWarps][kMaxRowsPerToken];
   pdl_launch_dependents();
@@ -118,6 +120,7 @@ __global__ void __launch_bounds__(kDispThreads) dispatch_kernel(
     __syncwarp();
     int32_t* tr = tok_rows + static_cast<size_t>(t) * kc;
     for (int j = lane; j < kc; j += 32) tr[j] = (j < nrows) ? rows[j] : -1;
+    if (coverage && lane == 0) coverage[t] = nrows;
     if (nrows == 0 || xp == nullptr) {
       __syncwarp();
       continue;
@@ -150,7 +153,7 @@ cudaError_t launch_dispatch(int dtype, const void* x, const int32_t* cand_idx,
                             const float* cand_gate, const int32_t* slot, const int32_t* kept,
                             int T, int d, int N, int kc, int expert_choice, int64_t rows_max,
                             int32_t* expert_offsets, int32_t* row_token, float* row_gate,
-                            int32_t* tok_rows, void* xp, cudaStream_t s) {
+                            int32_t* tok_rows, int32_t* coverage, void* xp, cudaStream_t s) {
   const int rmax = rows_max > 0x7fffffff ? 0x7fffffff : static_cast<int>(rows_max);
   int blocks = (T + kDispWarps - 1) / kDispWarps;
   const int cap = device_sm_count() * 8;
@@ -160,12 +163,12 @@ cudaError_t launch_dispatch(int dtype, const void* x, const int32_t* cand_idx,
     return launch_pdl(dispatch_kernel<__nv_bfloat16>, blocks, kDispThreads, 0, s,
                       static_cast<const __nv_bfloat16*>(x), cand_idx, cand_gate, slot, kept, T, d,
                       N, kc, expert_choice, rmax, expert_offsets, row_token, row_gate, tok_rows,
-                      static_cast<__nv_bfloat16*>(xp));
+                      coverage, static_cast<__nv_bfloat16*>(xp));
   }
   return launch_pdl(dispatch_kernel<float>, blocks, kDispThreads, 0, s,
                     static_cast<const float*>(x), cand_idx, cand_gate, slot, kept, T, d, N, kc,
                     expert_choice, rmax, expert_offsets, row_token, row_gate, tok_rows,
-                    static_cast<float*>(xp));
+                    coverage, static_cast<float*>(xp));
 }
 
 }  // namespace moe

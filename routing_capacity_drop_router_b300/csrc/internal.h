@@ -100,12 +100,13 @@ cudaError_t launch_select(const int32_t* cand_idx, const float* cand_gate, int T
                           uint32_t* counter, cudaStream_t s);
 int select_max_tokens();
 
-// Offsets, row maps, token rows and the gather of x into xp.
+// Offsets, row maps, token rows, per-token coverage (nullable) and the
+// gather of x into xp.
 cudaError_t launch_dispatch(int dtype, const void* x, const int32_t* cand_idx,
                             const float* cand_gate, const int32_t* slot, const int32_t* kept,
                             int T, int d, int N, int kc, int expert_choice, int64_t rows_max,
                             int32_t* expert_offsets, int32_t* row_token, float* row_gate,
-                            int32_t* tok_rows, void* xp, cudaStream_t s);
+                            int32_t* tok_rows, int32_t* coverage, void* xp, cudaStream_t s);
 
 // Grouped GEMM with e4m3 weights and per-column fp32 scales (sc1 [S, n_out],
 // sc3 likewise for SwiGLU): out = silu(A (B1*sc1)) * (A (B3*sc3)) or A (B1*sc1);

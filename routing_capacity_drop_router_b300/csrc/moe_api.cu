@@ -213,7 +213,8 @@ int run_router(const moe_config& c, bool ec, const void* x, const void* W_r, con
 
 struct Layout {
   size_t ctrl, logits, scores, cand_idx, cand_gate, slot, keep, demand, kept, offsets,
-      shared_offsets, row_token, row_gate, tok_rows, xp, hp, op, shared_out, colsum, total;
+      shared_offsets, row_token, row_gate, tok_rows, coverage, xp, hp, op, shared_out, colsum,
+      total;
 };
 
 Layout layout(const moe_config& c, const Derived& d) {
@@ -239,6 +240,7 @@ Layout layout(const moe_config& c, const Derived& d) {
   L.row_token = take(R * 4);
   L.row_gate = take(R * 4);
   L.tok_rows = take(T * kc * 4);
+  L.coverage = take(T * 4);
   L.xp = take(R * dd * d.sx);
   const size_t hp_rows = std::max(R * static_cast<size_t>(c.f), T * static_cast<size_t>(c.f_shared));
   L.hp = take(hp_rows * d.sx);
@@ -378,7 +380,7 @@ int moe_capacity_drop(const moe_config* cfg, const int32_t* cand_idx, const floa
 int moe_dispatch(const moe_config* cfg, const void* x, const int32_t* cand_idx,
                  const float* cand_gate, const int32_t* slot, const int32_t* kept,
                  int32_t* expert_offsets, int32_t* row_token, float* row_gate, int32_t* tok_rows,
-                 void* xp, void* stream) {
+                 int32_t* coverage, void* xp, void* stream) {
   Derived d;
   int st = validate(cfg, &d);
   if (st != MOE_OK) return st;
@@ -390,7 +392,7 @@ int moe_dispatch(const moe_config* cfg, const void* x, const int32_t* cand_idx,
   if (!aligned16(x) || !aligned16(xp)) return MOE_ERR_ALIGN;
   return status_from(launch_dispatch(cfg->dtype, x, cand_idx, cand_gate, slot, kept, cfg->T,
                                      cfg->d, cfg->N, d.kc, d.ec ? 1 : 0, d.rows_max, expert_offsets, row_token,
-                                     row_gate, tok_rows, xp, as_stream(stream)));
+                                     row_gate, tok_rows, coverage, xp, as_stream(stream)));
 }
 
 int moe_expert_ffn(const moe_config* cfg, const void* xp, const int32_t* offsets,
@@ -589,7 +591,8 @@ int layer_forward(const moe_config* cfg, const void* x, const void* W_router, co
     return MOE_ERR_LAUNCH;
   if (launch_dispatch(c.dtype, x, cand_idx, cand_gate, slot, kept, c.T, c.d, c.N, d.kc,
                       d.ec ? 1 : 0, d.rows_max, offsets, row_token, row_gate, tok_rows,
-                      fuse ? nullptr : xp, s) != cudaSuccess || !tr.mark(1))
+                      at<int32_t>(ws, L.coverage), fuse ? nullptr : xp, s) != cudaSuccess ||
+      !tr.mark(1))
     return MOE_ERR_LAUNCH;
   if (w8)
     st = run_ffn_e4m3(xp, offsets, c.N, d.rows_max, c.d, c.f, *w8, hp, op, status, s, &tr);
@@ -697,6 +700,7 @@ int moe_workspace_views(const moe_config* cfg, void* ws, moe_views_t* out) {
   out->xp = at<void>(ws, L.xp);
   out->op = at<void>(ws, L.op);
   out->shared_out = cfg->f_shared > 0 ? at<void>(ws, L.shared_out) : nullptr;
+  out->coverage = at<int32_t>(ws, L.coverage);
   return MOE_OK;
 }
 

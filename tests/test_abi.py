@@ -35,7 +35,7 @@ def test_struct_layout_matches_header():
     assert ctypes.sizeof(M.moe_config) == 56
     assert M.moe_config.gamma.offset == 24
     assert ctypes.sizeof(M.moe_sizes_t) == 32
-    assert ctypes.sizeof(M.moe_views_t) == 16 * 8
+    assert ctypes.sizeof(M.moe_views_t) == 17 * 8
     assert ctypes.sizeof(M.moe_e4m3_experts) == 6 * 8
 
 
@@ -117,7 +117,7 @@ def test_null_pointers_rejected_before_any_launch():
     r = ctypes.byref(cfg)
     assert lib.moe_route(r, *([None] * 9), 0, None) == M.MOE_ERR_NULL
     assert lib.moe_capacity_drop(r, None, None, None, None, None, None, None) == M.MOE_ERR_NULL
-    assert lib.moe_dispatch(r, *([None] * 10), None) == M.MOE_ERR_NULL
+    assert lib.moe_dispatch(r, *([None] * 11), None) == M.MOE_ERR_NULL
     assert lib.moe_combine(r, None, None, None, None, None, None) == M.MOE_ERR_NULL
     assert lib.moe_layer_forward(r, *([None] * 14), 0, None) == M.MOE_ERR_NULL
     assert lib.moe_expert_ffn(r, None, None, 8, 64, 128, None, None, None, None, None, 0,
