@@ -305,12 +305,18 @@ int moe_expert_ffn_gather(const moe_config* cfg, const void* x, const int32_t* r
  *   rows_max * f * sizeof(dtype) must not exceed MOE_NOALLOC_SCRATCH_BYTES - 256,
  *            otherwise MOE_ERR_WORKSPACE is returned and nothing is enqueued
  *            (e.g. bf16 with f = 14336 fits up to 2340 rows).
- *   device_status [1] int32 nullable, device: cleared to 0 by the call, then
- *            receives MOE_ERR_DEVICE_TIMEOUT if a bounded wait expires; NULL
- *            uses a word inside the library's array.
+ *   device_status [1] int32 nullable, device: receives MOE_ERR_DEVICE_TIMEOUT
+ *            if a bounded wait expires. The call does not clear it: the
+ *            caller sets it to 0 before first use (it may share the word with
+ *            earlier stages; the first error recorded wins). With NULL the
+ *            call records into a word inside the library's array that no entry
+ *            point reads back, so device-side errors are then lost: pass a
+ *            word whenever a timeout must be observed.
  * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture. Every call on a device shares the one array:
+ * (cudaGetSymbolAddress) with that device current, and looks it up again
+ * after the device's context changes (cudaDeviceReset); make the first call
+ * in each context before any stream capture. Every call on a device shares
+ * the one array:
  * calls whose work overlaps on the GPU (different streams, or host threads
  * without ordering) race on it and must be serialised by the caller.
  */
