@@ -278,10 +278,10 @@ def gemm_traffic(w):
 
 
 # dram__bytes_read.sum + dram__bytes_write.sum of expert_gemm1_swiglu +
-# expert_gemm2 from one ncu capture per workload (profiles/ has the summary),
+# expert_gemm2 from one ncu capture per workload,
 # keyed by the sha256 prefix of the kernel source it was taken on.
 GEMM_TRAFFIC = {
-    # profiles/grouped_gemm_tc_pairs_mixtral_gamma1_bf16.md: GEMM1+SwiGLU
+    # the CTA-pair grouped GEMM on the Mixtral-shaped layer at gamma 1: GEMM1+SwiGLU
     # 1.967098 GB read + 0.141841 GB written, GEMM2 1.185967 GB + 0.040459 GB
     "mixtral_bf16_gamma1": {"kernel_sha": "bc4d48697a603fd5",
                             "bytes_per_launch_pair": 1.967098e9 + 0.141841e9 +
@@ -289,20 +289,51 @@ GEMM_TRAFFIC = {
 }
 
 
-def run_ours(args, rank, world, local_rank):
-    import routing_capacity_drop_router_b300 as M
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    w = W.ALL[args.workload]
-    dist = world > 1
-    if dist:
-        import torch.distributed as td
-
-    inp = W.make_inputs(w.replace(seed=w.seed + rank) if args.distinct_batches else w)
+def device_inputs(w, dev, rank=0, distinct=False):
+    """The workload's seeded inputs on the device (e4m3 experts: only the
+    bytes and scales), plus the host copy of x for the end-to-end leg."""
+    inp = W.make_inputs(w.replace(seed=w.seed + rank) if distinct else w)
     if w.weights == "e4m3":  # the routed experts live on the device in e4m3 only
         inp = {k: v for k, v in inp.items() if k not in ("W1", "W3", "W2")}
     d = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
-    cfg = M.config_from_workload(w, fuse_gather=args.gather == "fused")
+    return d, inp["x"]
+
+
+def roofline_of(w, P, kept_h, g1, g2, peaks, peak_src):
+    """Roofline of the expert GEMMs (GEMM1+SwiGLU and GEMM2 event times, ms):
+    tensor-bound at the kept pairs' 6*d*f flops, or HBM-bound on the bytes of
+    the experts hit plus the rows in and out when the flops per byte fall
+    below the machine balance (decode batches)."""
+    peak_tf = float(peaks["bf16_tflops"])
+    hbm = float(peaks["hbm_gbs"])
+    routed_flops = 6.0 * w.d * w.f * P
+    sx = 2 if w.dtype == "bf16" else 4
+    gemm_bytes = routed_weight_bytes(w, kept_h) + 2 * P * (w.d + w.f) * sx
+    sec = (g1 + g2) * 1e-3
+    tflops = routed_flops / sec / 1e12
+    gbs = gemm_bytes / sec / 1e9
+    ridge = peak_tf * 1e12 / (hbm * 1e9)
+    if routed_flops / gemm_bytes < ridge:
+        return {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                "algorithmic_bytes": gemm_bytes, "peak_source": f"{peak_src} HBM copy",
+                "tflops": tflops}
+    return {"bound": "tensor", "achieved": tflops, "peak": peak_tf, "unit": "TFLOP/s",
+            "frac": tflops / peak_tf, "peak_source": f"{peak_src} bf16 burst",
+            "frac_of_sustained": tflops / float(peaks.get("bf16_tflops_sustained", peak_tf)),
+            "flops_per_byte": routed_flops / gemm_bytes, "machine_balance": ridge,
+            "hbm_view": {"achieved": gbs, "unit": "GB/s", "frac": gbs / hbm,
+                         "algorithmic_bytes": gemm_bytes}}
+
+
+def measure_layer(M, w, d, args, dev, world, rank, fuse_gather=False):
+    """Warm-up, then args.steps timed moe_layer_forward steps (events only at
+    the step boundaries and around the expert GEMMs, clocks sampled inside
+    the timed region, max over ranks), then a pass with an event at every
+    kernel boundary for the per-stage times. Returns the measurements and the
+    state the end-to-end leg reuses."""
+    import torch.distributed as td
+    dist = world > 1
+    cfg = M.config_from_workload(w, fuse_gather=fuse_gather)
     sz = M.sizes(cfg)
     ws = torch.zeros(sz.workspace, dtype=torch.uint8, device=dev)
     dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
@@ -314,9 +345,9 @@ def run_ours(args, rank, world, local_rank):
                        if t is not None and k in ("W1", "W3", "W2", "Ws1", "Ws3", "Ws2",
                                                   "W1q", "W3q", "W2q"))
     l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
-    # Between steps the L2 is not flushed: every step streams all expert
-    # weights it uses (far more than the L2) through it, so the next step's
-    # activations start cold. Smaller workloads flush explicitly.
+    # Between steps the L2 is not flushed when every step streams expert
+    # weights far larger than the L2 through it (the next step's activations
+    # start cold); smaller workloads flush explicitly.
     flush = None
     if weight_bytes < 4 * l2_bytes:
         flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
@@ -330,12 +361,12 @@ def run_ours(args, rank, world, local_rank):
         step()
     torch.cuda.synchronize()
     if M.moe_get_device_status(ws) != M.MOE_OK:
-        raise RuntimeError("device status error after warm-up")
+        raise RuntimeError(f"{w.name}: device status error after warm-up")
     st = stats.cpu().numpy()
     P = int(st[0])
     vw = M.moe_workspace_views(cfg, ws)
-    k0 = vw.kept - ws.data_ptr()  # per-expert kept rows, inside the workspace
-    kept_h = ws[k0:k0 + 4 * w.N].view(torch.int32).cpu().numpy()
+    kept_h = M.view_tensor(vw.kept, (w.N,), torch.int32, dev).cpu().numpy()
+    coverage = M.view_tensor(vw.coverage, (w.T,), torch.int32, dev).cpu().numpy()
 
     # ---- timed region: K layer steps. The library records events on the
     # launching stream at the step's start and end and around the expert GEMMs
@@ -384,8 +415,6 @@ def run_ours(args, rank, world, local_rank):
     pre_ms = statistics.mean(row[0].elapsed_time(row[g1_i]) for row in evs)
     post_ms = statistics.mean(row[g1_i + 2].elapsed_time(row[-1]) for row in evs)
     total_ms = max_over_ranks(total_ms, dev)
-    ms_per_step = total_ms / args.steps
-    value = job_rate(world, w.T, args.steps, total_ms)
 
     # ---- per-kernel breakdown: a few more steps with an event at every
     # kernel boundary (this serialises the launches) ----
@@ -404,13 +433,112 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     stage_ms = {name: statistics.mean(row[i].elapsed_time(row[i + 1]) for row in tr)
                 for i, name in enumerate(stages)}
+    if M.moe_get_device_status(ws) != M.MOE_OK:
+        raise RuntimeError(f"{w.name}: device status error in the timed region")
+    return dict(cfg=cfg, ws=ws, y=y, stats=stats, st=st, P=P, kept_h=kept_h, coverage=coverage,
+                stages=stages, stream=stream, flush=flush, weight_bytes=weight_bytes,
+                l2_bytes=l2_bytes, total_ms=total_ms, g1=g1_ms, g2=g2_ms, pre=pre_ms,
+                post=post_ms, stage_ms=stage_ms, clocks=clk)
+
+
+def kernel_table(w, r, peaks, fused_gather=False):
+    """Per-kernel figures: the HBM-bound stages' algorithmic GB/s, the
+    selection's time, the expert GEMMs' flops rate and the stage times."""
+    hbm = float(peaks["hbm_gbs"])
+    P, stage_ms = r["P"], r["stage_ms"]
+    sbytes = stage_bytes(w, P, fused_gather=fused_gather)
+    kernels = {}
+    route_ms = sum(stage_ms.get(n, 0.0) for n in ("router", "router_logits", "route_tokens"))
+    for name, ms in (("route", route_ms), ("dispatch", stage_ms["dispatch"]),
+                     ("combine", stage_ms["combine"])):
+        gbs = sbytes[name] / (ms * 1e-3) / 1e9
+        kernels[name] = {"ms": ms, "bytes": sbytes[name], "GB/s": gbs, "frac_hbm": gbs / hbm}
+    kernels["select"] = {"ms": stage_ms["select"]}
+    g1, g2 = r["g1"], r["g2"]
+    kernels["expert_gemm1_swiglu"] = {"ms": g1, "flops": 4.0 * w.d * w.f * P,
+                                      "TFLOP/s": 4.0 * w.d * w.f * P / (g1 * 1e-3) / 1e12}
+    kernels["expert_gemm2"] = {"ms": g2, "flops": 2.0 * w.d * w.f * P,
+                               "TFLOP/s": 2.0 * w.d * w.f * P / (g2 * 1e-3) / 1e12}
+    if w.f_shared and "shared_gemm1_swiglu" in stage_ms:
+        sg = stage_ms["shared_gemm1_swiglu"] + stage_ms["shared_gemm2"]
+        kernels["shared_expert"] = {"ms": sg, "flops": 6.0 * w.d * w.f_shared * w.T,
+                                    "TFLOP/s": 6.0 * w.d * w.f_shared * w.T / (sg * 1e-3) / 1e12}
+    kernels["stage_ms_serialised"] = stage_ms
+    kernels["timed_steps_ms"] = {"before_expert_gemms": r["pre"], "expert_gemms": g1 + g2,
+                                 "after_expert_gemms": r["post"]}
+    return kernels
+
+
+def coverage_summary(cov):
+    """How many experts took each token (expert choice: some tokens are taken
+    by several experts, some by none)."""
+    cov = np.asarray(cov)
+    if cov.size == 0:
+        return None
+    return {"min": int(cov.min()), "max": int(cov.max()), "mean": float(cov.mean()),
+            "zero_coverage_tokens": int((cov == 0).sum()),
+            "histogram": {str(int(v)): int(c) for v, c in zip(*np.unique(cov, return_counts=True))}}
+
+
+# Further workloads measured after the headline one, each in the same way and
+# reported in the line's "configs" object: the Mixtral-shaped layer without a
+# capacity limit and at capacity factor 1.5, the fine-grained layer with its
+# shared expert, the expert-choice layer and the decode batch.
+EXTRA_CONFIGS = ("mixtral_bf16", "mixtral_bf16_gamma1.5", "finegrained_bf16",
+                 "expert_choice_bf16", "decode_bf16")
+
+
+def config_entry(w, r, args, world, peaks, peak_src):
+    """One workload's entry of the "configs" object."""
+    roof = roofline_of(w, r["P"], r["kept_h"], r["g1"], r["g2"], peaks, peak_src)
+    kern = kernel_table(w, r, peaks)
+    st = r["st"]
+    out = {
+        "workload": w.describe(), "steps": args.steps, "warmup": args.warmup,
+        "tokens_per_s": job_rate(world, w.T, args.steps, r["total_ms"]),
+        "ms_per_step": r["total_ms"] / args.steps, "kept_pairs": r["P"],
+        "gemm1_us": 1e3 * r["g1"], "gemm2_us": 1e3 * r["g2"],
+        "roofline": roof,
+        "hbm_stages": {k: {"GB/s": kern[k]["GB/s"], "frac_hbm": kern[k]["frac_hbm"],
+                           "ms": kern[k]["ms"]} for k in ("route", "dispatch", "combine")},
+        "select_ms": kern["select"]["ms"],
+        "timed_steps_ms": kern["timed_steps_ms"],
+        "stats": {"max_over_mean": float(st[4]), "drop_fraction": float(st[5]),
+                  "balance_times_N": float(st[7])},
+        "clocks": r["clocks"],
+        "l2": "flushed before every timed step" if r["flush"] is not None else "not flushed",
+    }
+    if "shared_expert" in kern:
+        out["shared_expert_us"] = 1e3 * kern["shared_expert"]["ms"]
+    if w.mode == W.EXPERT_CHOICE:
+        out["coverage"] = coverage_summary(r["coverage"])
+    return out
+
+
+def run_ours(args, rank, world, local_rank):
+    import routing_capacity_drop_router_b300 as M
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = W.ALL[args.workload]
+    dist = world > 1
+    if dist:
+        import torch.distributed as td
+
+    d, x_cpu = device_inputs(w, dev, rank, args.distinct_batches)
+    fused = args.gather == "fused"
+    r = measure_layer(M, w, d, args, dev, world, rank, fuse_gather=fused)
+    cfg, ws, y, stats, stream = r["cfg"], r["ws"], r["y"], r["stats"], r["stream"]
+    total_ms, st, P = r["total_ms"], r["st"], r["P"]
+    ms_per_step = total_ms / args.steps
+    value = job_rate(world, w.T, args.steps, total_ms)
+    dt = y.dtype
 
     # ---- end to end through host buffers: every step copies its x from
     # pinned host memory, runs the layer and copies y back to pinned host
     # memory. Three streams pipeline the steps as a server would: step i+1's
     # upload and step i-1's download overlap step i's layer (double-buffered
     # device x and y; events order the reuse of each buffer) ----
-    x_host = inp["x"].pin_memory()
+    x_host = x_cpu.pin_memory()
     y_host = [torch.empty((w.T, w.d), dtype=dt).pin_memory() for _ in range(2)]
     x_dev = [torch.empty_like(d["x"]) for _ in range(2)]
     y_dev = [torch.empty_like(y) for _ in range(2)]
@@ -458,57 +586,46 @@ def run_ours(args, rank, world, local_rank):
         raise RuntimeError("end-to-end output differs from the device-resident run")
     e2e_value = job_rate(world, w.T, args.steps, e2e_ms)
     sx = 2 if w.dtype == "bf16" else 4
-
     if M.moe_get_device_status(ws) != M.MOE_OK:
-        raise RuntimeError("device status error in the timed region")
-    if rank != 0:
-        return
+        raise RuntimeError("device status error in the end-to-end steps")
 
     peaks, peak_src = load_peaks()
-    peak_tf = float(peaks["bf16_tflops"])
-    hbm = float(peaks["hbm_gbs"])
-    sbytes = stage_bytes(w, P, fused_gather=bool(cfg.flags & M.MOE_FUSE_GATHER) and
-                         w.dtype == "bf16" and w.weights == "same")
-    kernels = {}
-    route_ms = sum(stage_ms.get(n, 0.0) for n in ("router", "router_logits", "route_tokens"))
-    for name, ms in (("route", route_ms), ("dispatch", stage_ms["dispatch"]),
-                     ("combine", stage_ms["combine"])):
-        gbs = sbytes[name] / (ms * 1e-3) / 1e9
-        kernels[name] = {"ms": ms, "bytes": sbytes[name], "GB/s": gbs, "frac_hbm": gbs / hbm}
-    kernels["select"] = {"ms": stage_ms["select"]}
-    g1, g2 = g1_ms, g2_ms
-    routed_flops = 6.0 * w.d * w.f * P
-    ffn_tflops = routed_flops / ((g1 + g2) * 1e-3) / 1e12
-    # the expert GEMMs are weight-bound when their flops per weight byte fall
-    # below the machine balance (decode batches)
-    sx_ = 2 if w.dtype == "bf16" else 4
-    gemm_bytes = routed_weight_bytes(w, kept_h) + 2 * P * (w.d + w.f) * sx_
-    ridge = peak_tf * 1e12 / (hbm * 1e9)
-    hbm_bound = routed_flops / gemm_bytes < ridge
-    if hbm_bound:
-        gbs = gemm_bytes / ((g1 + g2) * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
-                "algorithmic_bytes": gemm_bytes, "peak_source": f"{peak_src} HBM copy"}
-    else:
-        gbs = gemm_bytes / ((g1 + g2) * 1e-3) / 1e9
-        roof = {"bound": "tensor", "achieved": ffn_tflops, "peak": peak_tf, "unit": "TFLOP/s",
-                "frac": ffn_tflops / peak_tf, "peak_source": f"{peak_src} bf16 burst",
-                "frac_of_sustained": ffn_tflops / float(peaks.get("bf16_tflops_sustained",
-                                                                  peak_tf)),
-                "flops_per_byte": routed_flops / gemm_bytes, "machine_balance": ridge,
-                "hbm_view": {"achieved": gbs, "unit": "GB/s", "frac": gbs / hbm,
-                             "algorithmic_bytes": gemm_bytes}}
-    kernels["expert_gemm1_swiglu"] = {"ms": g1, "flops": 4.0 * w.d * w.f * P,
-                                      "TFLOP/s": 4.0 * w.d * w.f * P / (g1 * 1e-3) / 1e12}
-    kernels["expert_gemm2"] = {"ms": g2, "flops": 2.0 * w.d * w.f * P,
-                               "TFLOP/s": 2.0 * w.d * w.f * P / (g2 * 1e-3) / 1e12}
-    if w.f_shared:
-        sg = stage_ms["shared_gemm1_swiglu"] + stage_ms["shared_gemm2"]
-        kernels["shared_expert"] = {"ms": sg, "flops": 6.0 * w.d * w.f_shared * w.T,
-                                    "TFLOP/s": 6.0 * w.d * w.f_shared * w.T / (sg * 1e-3) / 1e12}
-    kernels["stage_ms_serialised"] = stage_ms
-    kernels["timed_steps_ms"] = {"before_expert_gemms": pre_ms, "expert_gemms": g1 + g2,
-                                 "after_expert_gemms": post_ms}
+    fused_stage = fused and w.dtype == "bf16" and w.weights == "same"
+    roof = roofline_of(w, P, r["kept_h"], r["g1"], r["g2"], peaks, peak_src)
+    kernels = kernel_table(w, r, peaks, fused_gather=fused_stage)
+
+    # ---- the other workloads, each measured the same way (one GPU only:
+    # the replica runs under torchrun time the headline workload alone) ----
+    configs = None
+    if world == 1 and not args.no_configs:
+        del x_host, y_host, x_dev, y_dev
+        configs = {}
+        cache = {w.name: d} if w.T == W.MIXTRAL_BF16.T and w.d == W.MIXTRAL_BF16.d and \
+            w.N == W.MIXTRAL_BF16.N and w.f == W.MIXTRAL_BF16.f and w.weights == "same" and \
+            w.seed == W.MIXTRAL_BF16.seed and not args.distinct_batches else {}
+        for name in EXTRA_CONFIGS:
+            if name == w.name:
+                continue
+            wx = W.ALL[name]
+            same_draws = [k for k, v in cache.items()
+                          if (W.ALL[k].T, W.ALL[k].d, W.ALL[k].N, W.ALL[k].f, W.ALL[k].f_shared,
+                              W.ALL[k].zipf_s, W.ALL[k].dtype, W.ALL[k].weights) ==
+                          (wx.T, wx.d, wx.N, wx.f, wx.f_shared, wx.zipf_s, wx.dtype, wx.weights)]
+            if same_draws:  # the same draws (only the routing mode differs)
+                dx = cache[same_draws[0]]
+            else:
+                cache.clear()
+                torch.cuda.empty_cache()
+                dx, _ = device_inputs(wx, dev)
+                cache[name] = dx
+            rx = measure_layer(M, wx, dx, args, dev, world, rank)
+            configs[name] = config_entry(wx, rx, args, world, peaks, peak_src)
+            del rx
+        cache.clear()
+        torch.cuda.empty_cache()
+
+    if rank != 0:
+        return
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
@@ -520,6 +637,7 @@ def run_ours(args, rank, world, local_rank):
         cpu = {"value": n / t_cpu, "unit": "tokens/s", "cores": _blas_threads(),
                "kind": "oracle", "sample": smp.describe(n, t_cpu)}
 
+    flush, weight_bytes, l2_bytes = r["flush"], r["weight_bytes"], r["l2_bytes"]
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -529,8 +647,7 @@ def run_ours(args, rank, world, local_rank):
                    "mode": w.mode, "gamma": None if math.isinf(w.gamma) else w.gamma,
                    "kept_pairs": P,
                    "gather": ("fused into expert GEMM1 (MOE_FUSE_GATHER)"
-                              if args.gather == "fused" and w.dtype == "bf16" and
-                              w.weights == "same" else "dispatch copies the token rows"),
+                              if fused_stage else "dispatch copies the token rows"),
                    "l2": ("flushed (256 MiB write) before every timed step" if flush is not None
                           else f"not flushed: inputs larger than L2 ({weight_bytes / 1e9:.2f} GB "
                                f"of expert weights stream through the {l2_bytes / 2**20:.0f} MiB "
@@ -550,14 +667,18 @@ def run_ours(args, rank, world, local_rank):
                 "pipeline": "pinned host x -> device, layer, device y -> pinned host every "
                             "step; step i+1's upload and step i-1's download overlap step "
                             "i's layer (3 streams)"},
-        "gpu_launches": len(stages) * args.steps,
+        "gpu_launches": len(r["stages"]) * args.steps,
         "launch": "programmatic dependent launch; events only around the expert GEMMs",
-        "clocks": clk,
+        "clocks": r["clocks"],
         "cpu_baseline": cpu,
         "stats": {"kept_pairs": float(st[0]), "max_over_mean": float(st[4]),
                   "drop_fraction": float(st[5]), "balance": float(st[6]),
                   "balance_times_N": float(st[7])},
     }
+    if w.mode == W.EXPERT_CHOICE:
+        line["coverage"] = coverage_summary(r["coverage"])
+    if configs is not None:
+        line["configs"] = configs
     print(json.dumps(line), flush=True)
 
 
@@ -740,6 +861,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.ALL))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="time the headline workload only (skip the line's \"configs\" object)")
     ap.add_argument("--cpu-sample-s", type=float, default=15.0,
                     help="seconds of oracle work in the cpu_baseline sample")
     ap.add_argument("--reference-budget-s", type=float, default=150.0,

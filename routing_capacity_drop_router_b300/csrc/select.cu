@@ -532,8 +532,12 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
       const uint32_t old = atomicAdd(counter, 1u);
       s_last = old == gridDim.x - 1;
       if (s_last) {
-        *counter = 0u;
+        // acquire side: the fence after observing the final count orders this
+        // block's reads of every other block's demand/kept after their
+        // release (fence, then arrival); the block barrier below carries the
+        // order to the block's other threads
         __threadfence();
+        *counter = 0u;
       }
     }
     __syncthreads();
