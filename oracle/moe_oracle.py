@@ -51,6 +51,11 @@ Readings taken where the pages are silent (each repeated where it is used):
   R8 storage points: bf16 layers keep x, weights, the SwiGLU hidden h, each
      expert output and y in bf16; fp32 layers keep them in fp32; every sum and
      product is taken in fp64 here and rounded only at those points.
+  R14 FP8 experts: the routed experts' weights are e4m3 bytes with one fp32
+     scale per output column (input preparation); both operands of each
+     expert product are e4m3, the activation rows (the token rows before W1
+     and W3, the stored hidden rows before W2) quantized per row with scale
+     max|row| / 448; products of e4m3 values, fp32 scales applied to the sums.
   R13 device-level capacity: a device is the group of `group_size` consecutive
      experts (as in R7); its capacity is the sum of its experts' capacities,
      floor(gamma * N_bar * group_size), capped at T * min(kc, group_size);
@@ -443,20 +448,29 @@ def silu(z) -> np.ndarray:
         return z / (1.0 + np.exp(-z))
 
 
-def swiglu(X, W1e, W3e, W2e, dtype: str) -> np.ndarray:
+def swiglu(X, W1e, W3e, W2e, dtype: str, act_e4m3: bool = False) -> np.ndarray:
     """E(X) = (silu(X W1) * (X W3)) W2 in fp64, rounding h and the result at
-    the layer's storage points (readings R1, R8)."""
+    the layer's storage points (readings R1, R8).
+
+    ``act_e4m3`` (reading R14, experts in FP8): the operand rows of both
+    products are quantized to e4m3 first, X before W1 and W3, the stored h
+    before W2 (quantize_rows_e4m3), and the products use their dequantized
+    values, exactly in fp64."""
     X = np.asarray(X, np.float64)
+    if act_e4m3:
+        X = dequantize_rows_e4m3(*quantize_rows_e4m3(X))
     a = X @ np.asarray(W1e, np.float64)
     g = X @ np.asarray(W3e, np.float64)
     h = store(silu(a) * g, dtype)
+    if act_e4m3:
+        h = dequantize_rows_e4m3(*quantize_rows_e4m3(h))
     return store(h @ np.asarray(W2e, np.float64), dtype)
 
 
 def layer_forward(x, W_r, bias, W1, W3, W2, *, mode: str, k: int, gamma: float = math.inf,
                   m: int = 0, group_size: int = 8, renorm: bool = False, dtype: str = "bf16",
                   Ws1=None, Ws3=None, Ws2=None, logits=None, home_group=None,
-                  tokens=None) -> Dict[str, np.ndarray]:
+                  tokens=None, act_e4m3: bool = False) -> Dict[str, np.ndarray]:
     """y_t = sum over kept pairs (t, e), in ascending e, of gate * E_e(x_t),
     plus the shared expert's output when one is given; a token with no kept
     pair and no shared expert outputs 0 ("Understanding Mixture of Experts",
@@ -466,7 +480,9 @@ def layer_forward(x, W_r, bias, W1, W3, W2, *, mode: str, k: int, gamma: float =
     ``logits`` replaces the router GEMM with given fp32 logits. ``tokens``
     computes the output rows of those tokens only (routing is always computed
     for the whole batch, since capacity and expert choice couple all tokens);
-    y then has one row per listed token.
+    y then has one row per listed token. ``act_e4m3``: the routed experts run
+    in FP8 (reading R14: their weights are given dequantized, their operand
+    rows are quantized to e4m3 per row); the shared expert is unchanged.
     """
     x = np.asarray(x, np.float64)
     T = x.shape[0]
@@ -484,7 +500,7 @@ def layer_forward(x, W_r, bias, W1, W3, W2, *, mode: str, k: int, gamma: float =
         if not sel:
             continue
         ts, js = ts[sel], js[sel]
-        o = swiglu(x[ts], W1[e], W3[e], W2[e], dtype)
+        o = swiglu(x[ts], W1[e], W3[e], W2[e], dtype, act_e4m3=act_e4m3)
         rows = np.array([pos[int(t)] for t in ts])
         acc[rows] += gate[ts, js].astype(np.float64)[:, None] * o
     if Ws1 is not None:
@@ -511,10 +527,57 @@ def e4m3_value(b) -> np.ndarray:
     return np.where(s == 1, -val, val)
 
 
-def dequantize_e4m3(q, scale) -> np.ndarray:
-    """Expert weights stored as e4m3 bytes q [..., K, n] with one fp32 scale
-    per output column, scale [..., n]: W = value(q) * scale, exact in fp64."""
-    return e4m3_value(q) * np.asarray(scale, np.float64)[..., None, :]
+def dequantize_e4m3(q, scale, kmajor: bool = False) -> np.ndarray:
+    """Expert weights stored as e4m3 bytes q [..., K, n] (or, with kmajor,
+    [..., n, K]: each output column's K bytes contiguous) with one fp32 scale
+    per output column, scale [..., n]: W[k, n] = value(q) * scale[n], exact in
+    fp64, returned as [..., K, n]."""
+    v = e4m3_value(q)
+    if kmajor:
+        v = np.swapaxes(v, -1, -2)
+    return v * np.asarray(scale, np.float64)[..., None, :]
+
+
+E4M3_MAX = 448.0  # largest finite e4m3 magnitude, 1.75 * 2^8
+
+
+def round_e4m3(v) -> np.ndarray:
+    """The e4m3 value nearest to each v (fp64), ties to the even code, finite
+    magnitudes beyond 448 saturated to 448; the sign is kept (also on zero).
+
+    e4m3 values: in the binade [2^e, 2^(e+1)), e >= -6, the step is 2^(e-3)
+    (3 mantissa bits); below 2^-6 the subnormals m * 2^-9. Rounding a/step to
+    the nearest integer, ties to even, is ties-to-even of the code's last
+    mantissa bit."""
+    v = np.asarray(v, np.float64)
+    a = np.abs(v)
+    _, ex = np.frexp(np.where(a > 0, a, 1.0))     # a = m * 2^ex, 0.5 <= m < 1
+    e = np.maximum(ex - 1, -6)
+    step = np.ldexp(1.0, e - 3)
+    r = np.rint(a / step) * step                  # a / step: exact (a power-of-two scaling)
+    r = np.minimum(r, E4M3_MAX)
+    return np.copysign(r, v)
+
+
+def quantize_rows_e4m3(X):
+    """One fp32 scale per row and e4m3 values (reading R14, activations of the
+    FP8 experts): amax = max |X[r, :]| (exact), scale = amax / 448 rounded to
+    fp32 (1 for an all-zero row), v = X / scale rounded to fp32 (correctly
+    rounded division), then the nearest e4m3 value of v (round_e4m3).
+
+    Returns (values [R, K] fp64, each an e4m3 value; scale [R] fp32)."""
+    Xf = np.asarray(X, np.float64).astype(np.float32)
+    if Xf.ndim != 2:
+        raise ValueError("rows of a matrix")
+    amax = np.max(np.abs(Xf), axis=1) if Xf.shape[1] else np.zeros(Xf.shape[0], F32)
+    scale = np.where(amax > 0, (amax / F32(E4M3_MAX)).astype(F32), F32(1.0)).astype(F32)
+    v = (Xf / scale[:, None]).astype(F32)
+    return round_e4m3(v.astype(np.float64)), scale
+
+
+def dequantize_rows_e4m3(values, scale) -> np.ndarray:
+    """Row r of the quantized matrix times its scale, exact in fp64."""
+    return np.asarray(values, np.float64) * np.asarray(scale, np.float64)[:, None]
 
 
 # --------------------------------------------------------------------------

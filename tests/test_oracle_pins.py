@@ -252,6 +252,106 @@ def test_e4m3_quantizer_error_bound_and_dequantization():
     assert np.all(deq[1, :, 7] == 0)
 
 
+def _e4m3_table():
+    """Every finite e4m3 value with its code (NaN codes left out)."""
+    codes = np.arange(256)
+    vals = O.e4m3_value(codes)
+    ok = ~np.isnan(vals)
+    return vals[ok], codes[ok]
+
+
+def test_round_e4m3_is_the_nearest_code_by_brute_force():
+    vals, codes = _e4m3_table()
+    rng = np.random.default_rng(41)
+    v = np.concatenate([rng.uniform(-470, 470, 3000), rng.uniform(-0.05, 0.05, 3000),
+                        rng.uniform(-2.0 ** -5, 2.0 ** -5, 2000),
+                        (vals[:, None] + vals[None, :]).ravel()[::7] / 2,   # midpoints: ties
+                        np.array([0.0, -0.0, 448.0, -448.0, 460.0, 1e6, -1e6])])
+    got = O.round_e4m3(v)
+    for x, g in zip(v, got):
+        if abs(x) > 448:
+            assert g == math.copysign(448.0, x)
+            continue
+        dist = np.abs(vals - x)
+        best = np.flatnonzero(dist == dist.min())
+        if len(best) > 1:  # a tie: the code whose last mantissa bit is 0
+            best = [b for b in best if codes[b] % 2 == 0 and np.signbit(vals[b]) == np.signbit(x)] \
+                or [b for b in best if codes[b] % 2 == 0]
+        assert g == vals[best[0]], (x, g, vals[best])
+
+
+def test_round_e4m3_matches_torch_float8():
+    rng = np.random.default_rng(42)
+    v = np.concatenate([rng.standard_normal(20000) * 50, rng.standard_normal(20000) * 2.0 ** -7,
+                        rng.uniform(-448, 448, 10000)]).astype(F32)
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).double().numpy()
+    got = O.round_e4m3(v.astype(np.float64))
+    fin = np.abs(v) <= 448
+    assert np.array_equal(got[fin], ref[fin])
+    assert np.all(np.abs(got[~fin]) == 448.0)
+
+
+def test_quantize_rows_e4m3_hand_values_and_bounds():
+    # a row whose largest magnitude is 448 * 2^-3: the scale is exactly 2^-3 and
+    # every e4m3-representable entry comes back unchanged
+    q = 2.0 ** -3
+    row = np.array([448 * q, -1.5 * q, 0.75 * q, 2.0 ** -9 * q, 0.0])
+    vals, scale = O.quantize_rows_e4m3(row[None, :])
+    assert scale.dtype == np.float32 and scale[0] == F32(q)
+    assert np.array_equal(O.dequantize_rows_e4m3(vals, scale)[0], row)
+    # an all-zero row keeps scale 1; the largest magnitude maps to +-448
+    vals, scale = O.quantize_rows_e4m3(np.array([[0.0, 0.0], [3.0, -7.0]]))
+    assert scale[0] == 1.0 and np.all(vals[0] == 0)
+    assert scale[1] == F32(F32(7.0) / F32(448.0)) and vals[1, 1] == -448.0
+    # rounding to 3 mantissa bits: relative error <= 2^-4 above the subnormal
+    # range of the scaled values, absolute <= 2^-10 * scale below it
+    rng = np.random.default_rng(43)
+    X = (rng.standard_normal((64, 300)) * rng.uniform(1e-3, 1e3, (64, 1))).astype(F32)
+    vals, scale = O.quantize_rows_e4m3(X)
+    deq = O.dequantize_rows_e4m3(vals, scale)
+    Xd = X.astype(np.float64)
+    s = scale.astype(np.float64)[:, None]
+    big = np.abs(Xd) >= 2.0 ** -6 * s
+    assert np.all(np.abs(deq - Xd)[big] <= 2.0 ** -4 * np.abs(Xd)[big] * (1 + 1e-6))
+    assert np.all(np.abs(deq - Xd)[~big] <= 2.0 ** -10 * np.broadcast_to(s, X.shape)[~big] * (1 + 1e-6))
+    assert np.all(np.max(np.abs(vals), axis=1) == 448.0)
+
+
+def test_e4m3_expert_is_the_plain_expert_on_e4m3_exact_operands():
+    # X rows hold one entry 448 (scale 1); W1 makes a = 448 * 1 so that
+    # silu(a) = a in fp64 (exp(-448) vanishes beside 1); W3 = c / 448^2 makes
+    # h = c, e4m3 values with max |c| = 448 per row, so both quantizations are
+    # exact and the FP8 expert equals the plain one bit for bit
+    vals, _ = _e4m3_table()
+    rng = np.random.default_rng(44)
+    d, f, n = 8, 16, 8
+    X = np.zeros((n, d))
+    X[np.arange(n), np.arange(n) % d] = 448.0
+    W1 = np.ones((d, f)) / 1.0
+    c = rng.choice(vals[np.abs(vals) <= 448], size=(d, f))
+    c[:, 0] = 448.0
+    W3 = c / 448.0 ** 2
+    W2 = rng.standard_normal((f, 4))
+    plain = O.swiglu(X, W1, W3, W2, "f64")
+    fp8 = O.swiglu(X, W1, W3, W2, "f64", act_e4m3=True)
+    assert np.array_equal(plain, fp8)
+    # on general operands the two differ, by the e4m3 rounding of the operands
+    Xg = rng.standard_normal((n, d))
+    a = O.swiglu(Xg, W1 * 0.3, W3 * 900, W2, "f64")
+    b = O.swiglu(Xg, W1 * 0.3, W3 * 900, W2, "f64", act_e4m3=True)
+    assert 0 < np.linalg.norm(a - b) / np.linalg.norm(a) < 0.1
+
+
+def test_dequantize_e4m3_kmajor_is_the_transpose():
+    rng = np.random.default_rng(45)
+    qb = rng.integers(0, 126, size=(2, 5, 7)).astype(np.uint8)   # [S, K, n], finite codes
+    sc = rng.uniform(0.5, 2, (2, 7))
+    a = O.dequantize_e4m3(qb, sc)
+    b = O.dequantize_e4m3(np.ascontiguousarray(np.swapaxes(qb, 1, 2)), sc, kmajor=True)
+    assert np.array_equal(a, b)
+    assert a[1, 3, 6] == O.e4m3_value(qb[1, 3, 6]) * sc[1, 6]
+
+
 # ------------------------------------------------- device-level capacity (§2③)
 
 def test_device_capacity_values():
