@@ -180,7 +180,7 @@ class OracleSampler:
         inp = W.make_inputs(w)
         f = lambda t: None if t is None else t.float().numpy()  # noqa: E731
         if w.weights == "e4m3":  # the experts the library multiplies
-            Wx = [O.dequantize_e4m3(inp[n + "q"].numpy(), inp[n + "s"].numpy())
+            Wx = [O.dequantize_e4m3(inp[n + "q"].numpy(), inp[n + "s"].numpy(), kmajor=True)
                   for n in ("W1", "W3", "W2")]
         else:
             Wx = [f(inp[n]) for n in ("W1", "W3", "W2")]
@@ -196,7 +196,7 @@ class OracleSampler:
         self.O.layer_forward(*self.args, mode=w.mode, k=w.k, gamma=w.gamma, m=w.m,
                              group_size=w.group_size, renorm=w.renorm, dtype=w.dtype,
                              Ws1=self.shared[0], Ws3=self.shared[1], Ws2=self.shared[2],
-                             tokens=tokens)
+                             tokens=tokens, act_e4m3=w.weights == "e4m3")
         return len(tokens), time.perf_counter() - t0
 
     def calibrate(self, target_s: float) -> int:
@@ -334,8 +334,8 @@ def measure_layer(M, w, d, args, dev, world, rank, fuse_gather=False):
     import torch.distributed as td
     dist = world > 1
     cfg = M.config_from_workload(w, fuse_gather=fuse_gather)
-    sz = M.sizes(cfg)
-    ws = torch.zeros(sz.workspace, dtype=torch.uint8, device=dev)
+    wsz = M.workspace_size_e4m3(cfg) if w.weights == "e4m3" else M.sizes(cfg).workspace
+    ws = torch.zeros(wsz, dtype=torch.uint8, device=dev)
     dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     y = torch.empty((w.T, w.d), dtype=dt, device=dev)
     stats = torch.zeros(M.MOE_STATS_LEN, dtype=torch.float64, device=dev)
@@ -485,7 +485,18 @@ def coverage_summary(cov):
 # capacity limit and at capacity factor 1.5, the fine-grained layer with its
 # shared expert, the expert-choice layer and the decode batch.
 EXTRA_CONFIGS = ("mixtral_bf16", "mixtral_bf16_gamma1.5", "finegrained_bf16",
-                 "expert_choice_bf16", "decode_bf16")
+                 "expert_choice_bf16", "decode_bf16", "decode_e4m3")
+
+
+def e4m3_from_bf16(d):
+    """The e4m3 experts of a workload whose bf16 draws are already on the
+    device (the recipe's per-column quantization, done on the GPU here, stored
+    K-major); the bf16 routed experts are dropped."""
+    out = {k: v for k, v in d.items() if k not in ("W1", "W3", "W2")}
+    for name in ("W1", "W3", "W2"):
+        q, sc = W.quantize_e4m3(d[name])
+        out[name + "q"], out[name + "s"] = q.transpose(-1, -2).contiguous(), sc
+    return out
 
 
 def config_entry(w, r, args, world, peaks, peak_src):
@@ -613,6 +624,13 @@ def run_ours(args, rank, world, local_rank):
                           (wx.T, wx.d, wx.N, wx.f, wx.f_shared, wx.zipf_s, wx.dtype, wx.weights)]
             if same_draws:  # the same draws (only the routing mode differs)
                 dx = cache[same_draws[0]]
+            elif wx.weights == "e4m3" and \
+                    any(W.ALL[k] == wx.replace(name=k, weights="same") for k in cache):
+                # e4m3 experts quantized from the bf16 draws already on the device
+                k0 = next(k for k in cache if W.ALL[k] == wx.replace(name=k, weights="same"))
+                dx = e4m3_from_bf16(cache.pop(k0))
+                torch.cuda.empty_cache()
+                cache[name] = dx
             else:
                 cache.clear()
                 torch.cuda.empty_cache()
@@ -733,7 +751,9 @@ def run_stage(args):
         "combine": lambda: M.moe_combine(cfg, op, row_gate, tok_rows, None, y),
     }
     if args.kernel == "ffn":
-        fws = torch.zeros(M.ffn_workspace_size(R, w.f, w.dtype), dtype=torch.uint8, device=dev)
+        fsz = M.ffn_workspace_size_e4m3(R, w.d, w.f) if w.weights == "e4m3" else \
+            M.ffn_workspace_size(R, w.f, w.dtype)
+        fws = torch.zeros(fsz, dtype=torch.uint8, device=dev)
         if w.weights == "e4m3":
             ex = M.e4m3_experts(d["W1q"], d["W3q"], d["W2q"], d["W1s"], d["W3s"], d["W2s"])
             fns["ffn"] = lambda: M.moe_expert_ffn_e4m3(cfg, xp, offs, w.N, R, w.f, ex, op, fws)

@@ -327,29 +327,48 @@ int moe_expert_ffn_noalloc(const moe_config* cfg, const void* xp, const int32_t*
                            void* stream);
 
 /*
- * Routed experts stored in FP8 (e4m3: 1 sign, 4 exponent bits with bias 7, 3
- * mantissa bits), one fp32 scale per output column: W1[e][k][n] =
- * value(W1q[e][k][n]) * s1[e][n], likewise W3 with s3 and W2 with s2. Halves
- * the bytes a weight-bound (decode) step streams; activations stay bf16 and
- * accumulation fp32. ("From personas to MoE 02", section "dense was honestly
- * heavy": quantising the weights, NVFP4 for instance, lightens the weight
- * side; the e4m3 format with column scales is this library's choice.)
+ * Routed experts in FP8 ("From personas to MoE 02", section "dense was
+ * honestly heavy": quantising the weights, NVFP4 for instance, lightens the
+ * weight side of a bandwidth-bound step; the e4m3 format and its scales are
+ * this library's choice). e4m3: 1 sign, 4 exponent bits with bias 7, 3
+ * mantissa bits, largest magnitude 448.
+ *
+ * Weights are stored K-major, one fp32 scale per output column:
+ *   W1[e][k][n] = value(W1q[e][n][k]) * s1[e][n], likewise W3 with s3, and
+ *   W2[e][j][c] = value(W2q[e][c][j]) * s2[e][c] (j < f, c < d).
+ * Both operands of every expert product are e4m3 on the tensor cores
+ * (tcgen05 kind::f8f6f4, fp32 accumulate): the token rows before W1/W3 and
+ * the SwiGLU hidden rows (stored bf16) before W2 are quantised per row on the
+ * GPU, scale = max|row| / 448 (fp32; 1 for a zero row) and each element the
+ * e4m3 value nearest to element / scale (ties to even, saturating). The row
+ * scale times the column scale multiplies each fp32 sum in the epilogue. The
+ * expert output op, h and y stay bf16.
  */
 typedef struct moe_e4m3_experts {
-  const uint8_t* W1;   /* [N, d, f] e4m3 bytes */
-  const uint8_t* W3;   /* [N, d, f] */
-  const uint8_t* W2;   /* [N, f, d] */
+  const uint8_t* W1;   /* [N, f, d] e4m3 bytes (K-major) */
+  const uint8_t* W3;   /* [N, f, d] */
+  const uint8_t* W2;   /* [N, d, f] */
   const float*   s1;   /* [N, f] */
   const float*   s3;   /* [N, f] */
   const float*   s2;   /* [N, d] */
 } moe_e4m3_experts;
 
+/* Workspace bytes of moe_expert_ffn_e4m3 for rows_max rows, width d and
+ * hidden width f: the control block, then (each 256-byte aligned) the bf16
+ * hidden rows [rows_max, f], the e4m3 token rows [rows_max, d] and their
+ * scales [rows_max] fp32, the e4m3 hidden rows [rows_max, f] and their scales
+ * [rows_max] fp32. */
+size_t moe_ffn_workspace_size_e4m3(int64_t rows_max, int32_t d, int32_t f);
+
+/* Workspace bytes of moe_layer_forward_e4m3: moe_workspace_size plus the
+ * e4m3 rows and scales above (0 if the config is invalid). */
+size_t moe_workspace_size_e4m3(const moe_config* cfg);
+
 /*
  * moe_expert_ffn with e4m3 experts (struct above; its pointers are device
- * pointers, the struct itself is read on the host). bf16 only, d and f
- * multiples of 128; MOE_ERR_UNSUPPORTED for fp32 configs. The e4m3 bytes are
- * widened to bf16 in shared memory (exactly) and the column scales multiply
- * the fp32 accumulators. ws as for moe_expert_ffn.
+ * pointers, the struct itself is read on the host). xp stays bf16 and is
+ * quantised per row inside the call. bf16 configs only, d and f multiples of
+ * 128; MOE_ERR_UNSUPPORTED for fp32 configs. ws >= moe_ffn_workspace_size_e4m3.
  */
 int moe_expert_ffn_e4m3(const moe_config* cfg, const void* xp, const int32_t* offsets,
                         int32_t n_segments, int64_t rows_max, int32_t f,
@@ -359,6 +378,7 @@ int moe_expert_ffn_e4m3(const moe_config* cfg, const void* xp, const int32_t* of
 /*
  * moe_layer_forward with e4m3 routed experts; the router, the shared expert
  * (Ws1, Ws3, Ws2, bf16) and everything else as in moe_layer_forward.
+ * ws >= moe_workspace_size_e4m3(cfg).
  */
 int moe_layer_forward_e4m3(const moe_config* cfg, const void* x, const void* W_router,
                            const float* bias, const moe_e4m3_experts* experts, const void* Ws1,

@@ -15,8 +15,10 @@ Recipe (one fixed draw order per workload, ``torch.Generator().manual_seed``):
   Ws2  ~ N(0, 1/fs)         [fs, d]      cost with MoE routing", §"how routing
                                           allocates the compute budget")
 Values are drawn in fp32; bf16 workloads round each value once to bf16
-(round-to-nearest-even). The optional router bias is the log of a Zipf(s)
-distribution over experts, expert 0 the most popular, to skew the load the way
+(round-to-nearest-even). Workloads with e4m3 routed experts quantize W1, W3
+and W2 per output column (quantize_e4m3) and store the bytes K-major,
+W1q [N, f, d], W3q [N, f, d], W2q [N, d, f], with scales [N, f] and [N, d].
+The optional router bias is the log of a Zipf(s) distribution over experts, expert 0 the most popular, to skew the load the way
 the straggler discussion of "Capacity-Aware Inference: Mitigating the
 Straggler Effect in MoE" (§1) describes.
 """
@@ -78,7 +80,7 @@ class Workload:
         if self.zipf_s is not None:
             s += f" zipf_s={self.zipf_s}"
         if self.weights == "e4m3":
-            s += " expert weights e4m3 (per-column scales)"
+            s += " routed experts in e4m3 (weights per-column, activations per-row scales)"
         return s
 
 
@@ -91,8 +93,8 @@ MIXTRAL_BF16 = Workload("mixtral_bf16", T=4096, d=4096, N=8, f=14336, k=2,
 FINE_BF16 = Workload("finegrained_bf16", T=8192, d=2048, N=64, f=1408, k=6,
                      mode=CAPACITY_DROP, gamma=1.25, f_shared=2816, zipf_s=1.0)
 DECODE_BF16 = Workload("decode_bf16", T=32, d=4096, N=8, f=14336, k=2)
-# the decode step with its routed experts' weights stored in FP8
-DECODE_W8 = DECODE_BF16.replace(name="decode_bf16_w8", weights="e4m3")
+# the decode step with its routed experts in FP8 (e4m3 weights and activations)
+DECODE_W8 = DECODE_BF16.replace(name="decode_e4m3", weights="e4m3")
 
 
 def mixtral(gamma: float) -> Workload:
@@ -147,9 +149,10 @@ def make_inputs(w: Workload, with_experts: bool = True) -> Dict[str, torch.Tenso
     out["W1"] = _draw(g, (w.N, w.d, w.f), w.d ** -0.5).to(dt)
     out["W3"] = _draw(g, (w.N, w.d, w.f), w.d ** -0.5).to(dt)
     out["W2"] = _draw(g, (w.N, w.f, w.d), w.f ** -0.5).to(dt)
-    if w.weights == "e4m3":
+    if w.weights == "e4m3":  # stored K-major: [N, n, K] bytes, [N, n] scales
         for name in ("W1", "W3", "W2"):
-            out[name + "q"], out[name + "s"] = quantize_e4m3(out[name])
+            q, sc = quantize_e4m3(out[name])
+            out[name + "q"], out[name + "s"] = q.transpose(-1, -2).contiguous(), sc
     if w.f_shared:
         fs = w.f_shared
         out["Ws1"] = _draw(g, (w.d, fs), w.d ** -0.5).to(dt)

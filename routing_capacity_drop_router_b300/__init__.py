@@ -84,6 +84,9 @@ SIGNATURES = {
     "moe_workspace_size": (ctypes.c_size_t, [_CFG]),
     "moe_ffn_workspace_size": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32]),
     "moe_route_workspace_size": (ctypes.c_size_t, [_CFG]),
+    "moe_ffn_workspace_size_e4m3": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int32,
+                                                      ctypes.c_int32]),
+    "moe_workspace_size_e4m3": (ctypes.c_size_t, [_CFG]),
     "moe_route": (ctypes.c_int, [_CFG, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                  ctypes.c_size_t, _VP]),
     "moe_capacity_drop": (ctypes.c_int, [_CFG, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
@@ -206,6 +209,14 @@ def workspace_size(cfg: moe_config) -> int:
 
 def ffn_workspace_size(rows_max: int, f: int, dtype) -> int:
     return int(lib().moe_ffn_workspace_size(rows_max, f, DTYPES.get(dtype, dtype)))
+
+
+def ffn_workspace_size_e4m3(rows_max: int, d: int, f: int) -> int:
+    return int(lib().moe_ffn_workspace_size_e4m3(rows_max, d, f))
+
+
+def workspace_size_e4m3(cfg: moe_config) -> int:
+    return int(lib().moe_workspace_size_e4m3(ctypes.byref(cfg)))
 
 
 def route_workspace_size(cfg: moe_config) -> int:

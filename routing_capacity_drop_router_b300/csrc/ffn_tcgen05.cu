@@ -43,6 +43,11 @@
 //   Tiles run segment by segment, n-tile by n-tile, m fastest, so units that
 //   run at the same time share the weight tile in L2. Segment sizes are read
 //   on the device: no host synchronisation.
+//   FP8 form: A is e4m3 [rows, K] with one fp32 scale per row, B is e4m3
+//   stored K-major ([n_out, K] per segment) with one fp32 scale per column;
+//   a 128-byte k-block then holds 128 k, B tiles are K-major like A, the MMAs
+//   are kind::f8f6f4 (e4m3 x e4m3, fp32 accumulate) and the epilogue scales
+//   each accumulator by its row's and column's scales before the SwiGLU.
 //   Every mbarrier wait is bounded (1 s of globaltimer); on expiry the CTA
 //   raises a shared abort flag, every role leaves its loop, outstanding TMA
 //   copies and MMAs are drained (bounded), TMEM is freed and
@@ -147,15 +152,29 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t base) {
                  : "memory");
 }
 
-template <bool SWIGLU, bool PAIR, bool GATHER>
+// Instruction descriptor of the FP8 form, kind::f8f6f4: D fp32 (bits 4-5 =
+// 1), A and B e4m3 (bits 7-9 and 10-12 = 0), both K-major (bits 15, 16 = 0),
+// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+template <bool PAIR>
+constexpr uint32_t fp8_idesc() {
+  return (1u << 4) | (static_cast<uint32_t>(kBN >> 3) << 17) |
+         (static_cast<uint32_t>(Geo<PAIR>::kTileRows >> 4) << 24);
+}
+
+template <bool SWIGLU, bool PAIR, bool GATHER, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
     const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB1,
     const __grid_constant__ CUtensorMap tmB3, const int32_t* __restrict__ offsets, int S, int K,
     int n_out, int rows_max, __nv_bfloat16* __restrict__ out, int32_t* __restrict__ status,
     int withhold_kb, const __nv_bfloat16* __restrict__ xg, const int32_t* __restrict__ row_src,
-    int x_rows) {
+    int x_rows, const float* __restrict__ a_scale, const float* __restrict__ b1_scale,
+    const float* __restrict__ b3_scale) {
+  static_assert(!(GATHER && FP8), "the row gather reads bf16 token rows");
   using G = Geo<PAIR>;
   constexpr int kStages = G::kStages;
+  // elements of k per 128-byte k-block
+  constexpr int kKE = FP8 ? 2 * kBK : kBK;
+  constexpr uint32_t kIdesc = FP8 ? fp8_idesc<PAIR>() : G::kIdesc;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -169,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
   const int n_units = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   const int tile_n = SWIGLU ? kBN / 2 : kBN;  // output columns per tile
   const int n_tiles = (n_out + tile_n - 1) / tile_n;
-  const int num_kb = (K + kBK - 1) / kBK;
+  const int num_kb = (K + kKE - 1) / kKE;
 
   // ---- set-up: barriers, tile table, TMEM ----
   if (threadIdx.x == 0) {
@@ -251,6 +270,21 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
   // B tiles of one k-block: CTA 0 of a pair W1 (or B) columns col0.., CTA 1
   // W3 columns col0.. (or B columns col0 + 128..); one CTA: all of them
   auto load_b = [&](uint32_t sb, uint32_t fb, int seg, int col0, int kb) {
+    if (FP8) {  // K-major boxes of 128 k x 128 columns (16 KiB)
+      constexpr int kBox8 = 128 * 128;
+      if (PAIR) {
+        const CUtensorMap* mb = (SWIGLU && rank == 1) ? &tmB3 : &tmB1;
+        const int c = SWIGLU ? col0 : col0 + static_cast<int>(rank) * 128;
+        tma_load_3d_pair(sb, mb, kb * kKE, c, seg, fb);
+      } else if (SWIGLU) {
+        tma_load_3d(sb, &tmB1, kb * kKE, col0, seg, fb);
+        tma_load_3d(sb + kBox8, &tmB3, kb * kKE, col0, seg, fb);
+      } else {
+        tma_load_3d(sb, &tmB1, kb * kKE, col0, seg, fb);
+        tma_load_3d(sb + kBox8, &tmB1, kb * kKE, col0 + 128, seg, fb);
+      }
+      return;
+    }
     if (PAIR) {
       const CUtensorMap* mb = (SWIGLU && rank == 1) ? &tmB3 : &tmB1;
       const int c = SWIGLU ? col0 : col0 + static_cast<int>(rank) * 128;
@@ -369,8 +403,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
           // (failure-detection self-test: the withheld k-block is announced
           // but never loaded, so the MMA issuer's bounded wait expires)
           const uint32_t sa = stage0 + stage * G::kStageBytes;
-          if (PAIR) tma_load_2d_pair(sa, &tmA, kb * kBK, arow, fb);
-          else tma_load_2d(sa, &tmA, kb * kBK, arow, fb);
+          if (PAIR) tma_load_2d_pair(sa, &tmA, kb * kKE, arow, fb);
+          else tma_load_2d(sa, &tmA, kb * kKE, arow, fb);
           load_b(sa + kABytes, fb, seg, col0, kb);
         }
         if (++stage == kStages) {
@@ -425,11 +459,17 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
         const uint32_t sa = stage0 + stage * G::kStageBytes;
         const uint32_t sb = sa + kABytes;
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk) {
-          const uint64_t ad = kmajor_desc(sa, kk), bd = mnmajor_desc(sb, kk, kBoxBytes);
+        for (int kk = 0; kk < 4; ++kk) {  // 32 bytes of k per MMA
+          const uint64_t ad = kmajor_desc(sa, kk);
+          const uint64_t bd = FP8 ? kmajor_desc(sb, kk) : mnmajor_desc(sb, kk, kBoxBytes);
           const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
-          if (PAIR) tc_mma_pair(d_tmem, ad, bd, G::kIdesc, acc);
-          else tc_mma(d_tmem, ad, bd, G::kIdesc, acc);
+          if (FP8) {
+            if (PAIR) tc_mma_pair_f8(d_tmem, ad, bd, kIdesc, acc);
+            else tc_mma_f8(d_tmem, ad, bd, kIdesc, acc);
+          } else {
+            if (PAIR) tc_mma_pair(d_tmem, ad, bd, kIdesc, acc);
+            else tc_mma(d_tmem, ad, bd, kIdesc, acc);
+          }
         }
         if (PAIR) tc_commit_pair_mc(smem_u32(&ctrl->empty[stage]), 0x3);
         else tc_commit(smem_u32(&ctrl->empty[stage]));
@@ -470,6 +510,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
       const bool valid = row >= 0 && row < row_end && row < rows_max;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * kBN);
       __nv_bfloat16* orow = out + static_cast<size_t>(row) * n_out;
+      // FP8: the row's scale times each column's scale multiplies the sum of
+      // the code products
+      const float sa = (FP8 && valid) ? a_scale[row] : 1.f;
+      const float* sc1 = FP8 ? b1_scale + static_cast<size_t>(seg) * n_out + col0 : nullptr;
+      const float* sc3 = (FP8 && SWIGLU) ? b3_scale + static_cast<size_t>(seg) * n_out + col0 : nullptr;
       if (SWIGLU) {
 #pragma unroll 1
         for (int c = 0; c < kBN / 2; c += 32) {
@@ -478,6 +523,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
           tc_ld32(taddr + kBN / 2 + c, g);
           tc_wait_ld();
           if (valid && col0 + c < n_out) {
+            if (FP8) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                a[i] = __float_as_uint(__uint_as_float(a[i]) * sa * __ldg(sc1 + c + i));
+                g[i] = __float_as_uint(__uint_as_float(g[i]) * sa * __ldg(sc3 + c + i));
+              }
+            }
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -497,6 +549,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
           tc_ld32(taddr + c, a);
           tc_wait_ld();
           if (valid && col0 + c < n_out) {
+            if (FP8) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                a[i] = __float_as_uint(__uint_as_float(a[i]) * sa * __ldg(sc1 + c + i));
+            }
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
@@ -532,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
 
 // Clusters of 2 of the kernel that will be launched (its shared-memory
 // attribute already set) that can be resident at once (0: pairs unavailable).
-template <bool SWIGLU, bool GATHER>
+template <bool SWIGLU, bool GATHER, bool FP8>
 int pair_slots(int dev) {
   static int cached[64] = {};
   static bool done[64] = {};
@@ -550,7 +607,7 @@ int pair_slots(int dev) {
   cfg.dynamicSmemBytes = smem_bytes<true>();
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_tc_kernel<SWIGLU, true, GATHER>, &cfg) !=
+  if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_tc_kernel<SWIGLU, true, GATHER, FP8>, &cfg) !=
       cudaSuccess) {
     (void)cudaGetLastError();
     n = 0;
@@ -560,29 +617,30 @@ int pair_slots(int dev) {
   return n;
 }
 
-template <bool SWIGLU, bool PAIR, bool GATHER>
+template <bool SWIGLU, bool PAIR, bool GATHER, bool FP8>
 cudaError_t set_smem_attr(int dev) {
   static bool attr_set[64] = {};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (attr_set[dev]) return cudaSuccess;
-  const cudaError_t err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<SWIGLU, PAIR, GATHER>,
+  const cudaError_t err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<SWIGLU, PAIR, GATHER, FP8>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                smem_bytes<PAIR>());
   if (err == cudaSuccess) attr_set[dev] = true;
   return err;
 }
 
-template <bool SWIGLU, bool GATHER>
+template <bool SWIGLU, bool GATHER, bool FP8 = false>
 cudaError_t launch_gemm(const CUtensorMap& mA, const CUtensorMap& mB1, const CUtensorMap& mB3,
                         const int32_t* offsets, int S, int64_t rows_max, int K, int n_out,
                         __nv_bfloat16* o, int32_t* status, cudaStream_t s, int withhold_kb,
                         int max_sms, const __nv_bfloat16* xg, const int32_t* row_src,
-                        int x_rows) {
+                        int x_rows, const float* a_scale = nullptr,
+                        const float* b1_scale = nullptr, const float* b3_scale = nullptr) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  if ((err = set_smem_attr<SWIGLU, true, GATHER>(dev)) != cudaSuccess) return err;
-  if ((err = set_smem_attr<SWIGLU, false, GATHER>(dev)) != cudaSuccess) return err;
+  if ((err = set_smem_attr<SWIGLU, true, GATHER, FP8>(dev)) != cudaSuccess) return err;
+  if ((err = set_smem_attr<SWIGLU, false, GATHER, FP8>(dev)) != cudaSuccess) return err;
   // Pairs pay off once segments average a 256-row tile; below that (decode
   // batches) half of every pair tile would be padding. The row-gather form
   // runs one CTA per tile: its pairs wait on two CTAs' copies per k-block and
@@ -591,7 +649,7 @@ cudaError_t launch_gemm(const CUtensorMap& mA, const CUtensorMap& mB1, const CUt
   const bool want_pairs = env ? env[0] != '0' : (!GATHER && rows_max >= 2LL * kBM * S);
   int sms = device_sm_count();
   if (max_sms > 0 && max_sms < sms) sms = max_sms;  // confined to a slice of the GPU
-  int slots = want_pairs ? pair_slots<SWIGLU, GATHER>(dev) : 0;
+  int slots = want_pairs ? pair_slots<SWIGLU, GATHER, FP8>(dev) : 0;
   if (slots > sms / 2) slots = sms / 2;
   const bool pair = slots > 0;
   const int tile_rows = pair ? 2 * kBM : kBM;
@@ -618,12 +676,12 @@ cudaError_t launch_gemm(const CUtensorMap& mA, const CUtensorMap& mB1, const CUt
   cfg.attrs = attr;
   cfg.numAttrs = pair ? 2 : 1;
   if (pair)
-    return cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<SWIGLU, true, GATHER>, mA, mB1, mB3,
-                              offsets, S, K, n_out, rmax, o, status, withhold_kb, xg, row_src,
-                              x_rows);
-  return cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<SWIGLU, false, GATHER>, mA, mB1, mB3,
-                            offsets, S, K, n_out, rmax, o, status, withhold_kb, xg, row_src,
-                            x_rows);
+    return cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<SWIGLU, true, GATHER, FP8>, mA, mB1,
+                              mB3, offsets, S, K, n_out, rmax, o, status, withhold_kb, xg, row_src,
+                              x_rows, a_scale, b1_scale, b3_scale);
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<SWIGLU, false, GATHER, FP8>, mA, mB1,
+                            mB3, offsets, S, K, n_out, rmax, o, status, withhold_kb, xg, row_src,
+                            x_rows, a_scale, b1_scale, b3_scale);
 }
 
 }  // namespace
@@ -659,6 +717,34 @@ cudaError_t launch_grouped_gemm_tc_bf16(const void* A, const int32_t* offsets, i
                                     withhold_kb, max_sms, nullptr, nullptr, 0);
   return launch_gemm<false, false>(mA, mB1, mB3, offsets, S, rows_max, K, n_out, o, status, s,
                                    withhold_kb, max_sms, nullptr, nullptr, 0);
+}
+
+cudaError_t launch_grouped_gemm_tc_fp8(const void* A, const float* a_scale,
+                                       const int32_t* offsets, int S, int64_t rows_max, int K,
+                                       int n_out, const void* B1, const float* sc1,
+                                       const void* B3, const float* sc3, void* out, bool swiglu,
+                                       int32_t* status, cudaStream_t s) {
+  if (S == 0 || rows_max == 0) return cudaSuccess;
+  if (S > kMaxSegments || K % 128 || n_out % 128) return cudaErrorInvalidValue;
+  if (!a_scale || !sc1 || (swiglu && (!B3 || !sc3))) return cudaErrorInvalidValue;
+  CUtensorMap mA, mB1, mB3;
+  // A: [rows_max, K] bytes in 128 x 128 boxes; B: [S, n_out, K] bytes, boxes
+  // of 128 k x 128 columns
+  if (!make_tmap_2d_u8(&mA, A, static_cast<uint64_t>(rows_max), static_cast<uint64_t>(K), 128,
+                       kBM))
+    return cudaErrorInvalidValue;
+  if (!make_tmap_3d_u8(&mB1, B1, S, n_out, K, 128, 128)) return cudaErrorInvalidValue;
+  if (swiglu) {
+    if (!make_tmap_3d_u8(&mB3, B3, S, n_out, K, 128, 128)) return cudaErrorInvalidValue;
+  } else {
+    mB3 = mB1;
+  }
+  __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
+  if (swiglu)
+    return launch_gemm<true, false, true>(mA, mB1, mB3, offsets, S, rows_max, K, n_out, o, status,
+                                          s, -1, 0, nullptr, nullptr, 0, a_scale, sc1, sc3);
+  return launch_gemm<false, false, true>(mA, mB1, mB3, offsets, S, rows_max, K, n_out, o, status,
+                                         s, -1, 0, nullptr, nullptr, 0, a_scale, sc1, nullptr);
 }
 
 }  // namespace moe

@@ -108,13 +108,24 @@ cudaError_t launch_dispatch(int dtype, const void* x, const int32_t* cand_idx,
                             int32_t* expert_offsets, int32_t* row_token, float* row_gate,
                             int32_t* tok_rows, int32_t* coverage, void* xp, cudaStream_t s);
 
-// Grouped GEMM with e4m3 weights and per-column fp32 scales (sc1 [S, n_out],
-// sc3 likewise for SwiGLU): out = silu(A (B1*sc1)) * (A (B3*sc3)) or A (B1*sc1);
-// A bf16, out bf16.
-cudaError_t launch_grouped_gemm_tc_w8(const void* A, const int32_t* offsets, int S,
-                                      int64_t rows_max, int K, int n_out, const void* B1,
-                                      const float* sc1, const void* B3, const float* sc3,
-                                      void* out, bool swiglu, int32_t* status, cudaStream_t s);
+// Grouped GEMM on e4m3 operands (tcgen05 kind::f8f6f4): A [rows_max, K]
+// e4m3 bytes with one fp32 scale per row (a_scale [rows_max]); B1, B3
+// [S, n_out, K] e4m3 bytes, K-major, with one fp32 scale per output column
+// (sc1, sc3 [S, n_out]). The products of the codes are summed in fp32 and
+// scaled in the epilogue: out = silu(sa*sc1*(A B1)) * (sa*sc3*(A B3)) or
+// sa*sc1*(A B1); out bf16. K and n_out multiples of 128.
+cudaError_t launch_grouped_gemm_tc_fp8(const void* A, const float* a_scale,
+                                       const int32_t* offsets, int S, int64_t rows_max, int K,
+                                       int n_out, const void* B1, const float* sc1,
+                                       const void* B3, const float* sc3, void* out, bool swiglu,
+                                       int32_t* status, cudaStream_t s);
+
+// Rows r < offsets[S] of the bf16 matrix X [rows_max, K] to e4m3 with one
+// fp32 scale per row: scale = max|X[r]| / 448 (1 for a zero row), Q[r][j] =
+// nearest e4m3 of X[r][j] / scale (ties to even, saturating). K % 8 == 0.
+cudaError_t launch_quantize_rows_e4m3(const void* X, const int32_t* offsets, int S,
+                                      int64_t rows_max, int K, uint8_t* Q, float* scale,
+                                      cudaStream_t s);
 
 // Grouped GEMMs. SwiGLU variant: out = silu(A B1) * (A B3); plain: out = A B1.
 cudaError_t launch_grouped_gemm_simt_f32(const float* A, const int32_t* offsets, int S,
@@ -147,7 +158,10 @@ bool make_tmap_2d_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t 
                        uint32_t box_cols, uint32_t box_rows);
 bool make_tmap_3d_bf16(CUtensorMap* m, const void* ptr, uint64_t S, uint64_t K, uint64_t n,
                        uint32_t box_n, uint32_t box_k);
-// [S, K, n] bytes (e4m3 weights), 128-byte swizzle.
+// Byte tensors (e4m3), 128-byte swizzle. 2-D: [rows, cols] row-major, box
+// box_cols x box_rows. 3-D: [S, K, n] row-major, box box_n x box_k x 1.
+bool make_tmap_2d_u8(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols,
+                     uint32_t box_cols, uint32_t box_rows);
 bool make_tmap_3d_u8(CUtensorMap* m, const void* ptr, uint64_t S, uint64_t K, uint64_t n,
                      uint32_t box_n, uint32_t box_k);
 

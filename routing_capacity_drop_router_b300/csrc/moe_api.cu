@@ -214,10 +214,11 @@ int run_router(const moe_config& c, bool ec, const void* x, const void* W_r, con
 struct Layout {
   size_t ctrl, logits, scores, cand_idx, cand_gate, slot, keep, demand, kept, offsets,
       shared_offsets, row_token, row_gate, tok_rows, coverage, xp, hp, op, shared_out, colsum,
-      total;
+      // e4m3 experts only: e4m3 token rows and scales, e4m3 hidden rows and scales
+      xq, xs, hq, hs, total;
 };
 
-Layout layout(const moe_config& c, const Derived& d) {
+Layout layout(const moe_config& c, const Derived& d, bool e4m3 = false) {
   Layout L{};
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -247,6 +248,33 @@ Layout layout(const moe_config& c, const Derived& d) {
   L.op = take(R * dd * d.sx);
   L.shared_out = take(c.f_shared > 0 ? T * dd * d.sx : 0);
   L.colsum = take(colsum_bytes(c.T, c.N));
+  L.xq = take(e4m3 ? R * dd : 0);
+  L.xs = take(e4m3 ? R * 4 : 0);
+  L.hq = take(e4m3 ? R * static_cast<size_t>(c.f) : 0);
+  L.hs = take(e4m3 ? R * 4 : 0);
+  L.total = off;
+  return L;
+}
+
+// The e4m3 expert FFN's workspace after the control block: bf16 hidden rows,
+// e4m3 token rows and scales, e4m3 hidden rows and scales.
+struct FfnE4m3Layout {
+  size_t hp, xq, xs, hq, hs, total;
+};
+FfnE4m3Layout ffn_e4m3_layout(int64_t rows_max, int d, int f) {
+  FfnE4m3Layout L{};
+  const size_t R = static_cast<size_t>(rows_max);
+  size_t off = kCtrlBytes;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align256(off + bytes);
+    return o;
+  };
+  L.hp = take(R * f * 2);
+  L.xq = take(R * d);
+  L.xs = take(R * 4);
+  L.hq = take(R * f);
+  L.hs = take(R * 4);
   L.total = off;
   return L;
 }
@@ -286,15 +314,22 @@ int run_ffn(int dtype, const void* xp, const int32_t* offsets, int S, int64_t ro
   return MOE_OK;
 }
 
-// Expert FFN with e4m3 weights and per-column scales (bf16 activations).
+// Expert FFN with e4m3 experts: the bf16 rows xp are quantised per row (xq,
+// xs), GEMM1 on e4m3 operands writes the bf16 hidden rows hp, which are
+// quantised per row (hq, hs) for GEMM2. Trace marks: the first quantisation
+// and GEMM1 count as GEMM1, the second quantisation and GEMM2 as GEMM2.
 int run_ffn_e4m3(const void* xp, const int32_t* offsets, int S, int64_t rows_max, int d, int f,
-                 const moe_e4m3_experts& w, void* hp, void* op, int32_t* status, cudaStream_t s,
-                 Tracer* tr = nullptr) {
-  cudaError_t e = launch_grouped_gemm_tc_w8(xp, offsets, S, rows_max, d, f, w.W1, w.s1, w.W3,
-                                            w.s3, hp, true, status, s);
+                 const moe_e4m3_experts& w, void* hp, uint8_t* xq, float* xs, uint8_t* hq,
+                 float* hs, void* op, int32_t* status, cudaStream_t s, Tracer* tr = nullptr) {
+  cudaError_t e = launch_quantize_rows_e4m3(xp, offsets, S, rows_max, d, xq, xs, s);
+  if (e == cudaSuccess)
+    e = launch_grouped_gemm_tc_fp8(xq, xs, offsets, S, rows_max, d, f, w.W1, w.s1, w.W3, w.s3, hp,
+                                   true, status, s);
   if (e != cudaSuccess || (tr && !tr->mark())) return MOE_ERR_LAUNCH;
-  e = launch_grouped_gemm_tc_w8(hp, offsets, S, rows_max, f, d, w.W2, w.s2, nullptr, nullptr, op,
-                                false, status, s);
+  e = launch_quantize_rows_e4m3(hp, offsets, S, rows_max, f, hq, hs, s);
+  if (e == cudaSuccess)
+    e = launch_grouped_gemm_tc_fp8(hq, hs, offsets, S, rows_max, f, d, w.W2, w.s2, nullptr,
+                                   nullptr, op, false, status, s);
   if (e != cudaSuccess || (tr && !tr->mark())) return MOE_ERR_LAUNCH;
   return MOE_OK;
 }
@@ -338,6 +373,17 @@ size_t moe_ffn_workspace_size(int64_t rows_max, int32_t f, int32_t dtype) {
   if (rows_max < 0 || f < 0) return 0;
   const size_t sx = dtype == MOE_BF16 ? 2 : 4;
   return kCtrlBytes + align256(static_cast<size_t>(rows_max) * static_cast<size_t>(f) * sx);
+}
+
+size_t moe_ffn_workspace_size_e4m3(int64_t rows_max, int32_t d, int32_t f) {
+  if (rows_max < 0 || d < 0 || f < 0) return 0;
+  return ffn_e4m3_layout(rows_max, d, f).total;
+}
+
+size_t moe_workspace_size_e4m3(const moe_config* cfg) {
+  Derived d;
+  if (validate(cfg, &d) != MOE_OK) return 0;
+  return layout(*cfg, d, true).total;
 }
 
 size_t moe_route_workspace_size(const moe_config* cfg) {
@@ -550,7 +596,7 @@ int layer_forward(const moe_config* cfg, const void* x, const void* W_router, co
       (reinterpret_cast<uintptr_t>(ws) & 255u) || (!given && !aligned16(W_router)))
     return MOE_ERR_ALIGN;
   if (c.f_shared > 0 && (!aligned16(Ws1) || !aligned16(Ws3) || !aligned16(Ws2))) return MOE_ERR_ALIGN;
-  const Layout L = layout(c, d);
+  const Layout L = layout(c, d, w8 != nullptr);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
 
   cudaStream_t s = as_stream(stream);
@@ -595,7 +641,9 @@ int layer_forward(const moe_config* cfg, const void* x, const void* W_router, co
       !tr.mark(1))
     return MOE_ERR_LAUNCH;
   if (w8)
-    st = run_ffn_e4m3(xp, offsets, c.N, d.rows_max, c.d, c.f, *w8, hp, op, status, s, &tr);
+    st = run_ffn_e4m3(xp, offsets, c.N, d.rows_max, c.d, c.f, *w8, hp, at<uint8_t>(ws, L.xq),
+                      at<float>(ws, L.xs), at<uint8_t>(ws, L.hq), at<float>(ws, L.hs), op, status,
+                      s, &tr);
   else if (fuse)
     st = run_ffn(c.dtype, x, offsets, c.N, d.rows_max, c.d, c.f, W1, W3, W2, hp, op, status, s,
                  &tr, 0, row_token, c.T);
@@ -656,11 +704,13 @@ int moe_expert_ffn_e4m3(const moe_config* cfg, const void* xp, const int32_t* of
   if (st != MOE_OK) return st;
   if (n_segments > kMaxN) return MOE_ERR_UNSUPPORTED;
   if (!xp || !offsets || !op || !ws) return MOE_ERR_NULL;
-  if (!aligned16(xp) || !aligned16(op) || !aligned16(ws)) return MOE_ERR_ALIGN;
-  if (ws_bytes < moe_ffn_workspace_size(rows_max, f, MOE_BF16)) return MOE_ERR_WORKSPACE;
-  void* hp = static_cast<unsigned char*>(ws) + kCtrlBytes;
-  return run_ffn_e4m3(xp, offsets, n_segments, rows_max, cfg->d, f, *experts, hp, op,
-                      static_cast<int32_t*>(ws), as_stream(stream));
+  if (!aligned16(xp) || !aligned16(op) || (reinterpret_cast<uintptr_t>(ws) & 255u))
+    return MOE_ERR_ALIGN;
+  const FfnE4m3Layout L = ffn_e4m3_layout(rows_max, cfg->d, f);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  return run_ffn_e4m3(xp, offsets, n_segments, rows_max, cfg->d, f, *experts, at<void>(ws, L.hp),
+                      at<uint8_t>(ws, L.xq), at<float>(ws, L.xs), at<uint8_t>(ws, L.hq),
+                      at<float>(ws, L.hs), op, static_cast<int32_t*>(ws), as_stream(stream));
 }
 
 int moe_layer_stages(const moe_config* cfg, const char** names, int max_names) {

@@ -125,7 +125,8 @@ def layer_gpu(w: W.Workload, inp: Dict[str, torch.Tensor], logits: Optional[np.n
     ``fuse_gather`` -> MOE_FUSE_GATHER."""
     cfg = M.config_from_workload(w, logits_given=logits is not None, fuse_gather=fuse_gather)
     dev = torch.device("cuda")
-    ws = torch.zeros(M.workspace_size(cfg), dtype=torch.uint8, device=dev)  # status word = 0
+    wsz = M.workspace_size_e4m3(cfg) if w.weights == "e4m3" else M.workspace_size(cfg)
+    ws = torch.zeros(wsz, dtype=torch.uint8, device=dev)  # status word = 0
     dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     y = torch.empty((w.T, w.d), dtype=dt, device=dev)
     stats = torch.zeros(M.MOE_STATS_LEN, dtype=torch.float64, device=dev)
@@ -158,7 +159,7 @@ def layer_gpu(w: W.Workload, inp: Dict[str, torch.Tensor], logits: Optional[np.n
 def oracle_layer(w: W.Workload, inp: Dict[str, torch.Tensor], logits: Optional[np.ndarray] = None,
                  tokens=None, home_group=None):
     if w.weights == "e4m3":  # the experts the GPU multiplies: e4m3 values times column scales
-        W1, W3, W2 = (O.dequantize_e4m3(inp[n + "q"].numpy(), inp[n + "s"].numpy())
+        W1, W3, W2 = (O.dequantize_e4m3(inp[n + "q"].numpy(), inp[n + "s"].numpy(), kmajor=True)
                       for n in ("W1", "W3", "W2"))
     else:
         W1, W3, W2 = np32(inp["W1"]), np32(inp["W3"]), np32(inp["W2"])
@@ -167,7 +168,7 @@ def oracle_layer(w: W.Workload, inp: Dict[str, torch.Tensor], logits: Optional[n
                            m=w.m, group_size=w.group_size, renorm=w.renorm, dtype=w.dtype,
                            Ws1=np32(inp.get("Ws1")), Ws3=np32(inp.get("Ws3")),
                            Ws2=np32(inp.get("Ws2")), logits=logits, tokens=tokens,
-                           home_group=home_group)
+                           home_group=home_group, act_e4m3=w.weights == "e4m3")
 
 
 def tile_edge_tokens(w: W.Workload, L: np.ndarray, tile: int = 128) -> np.ndarray:

@@ -203,7 +203,7 @@ def test_e4m3_experts_host_checks():
     lib = M.lib()
     fake = ctypes.c_void_p(1 << 20)
     ex = M.moe_e4m3_experts(*([1 << 20] * 6))
-    need = M.ffn_workspace_size(8, 128, "bf16")
+    need = M.ffn_workspace_size_e4m3(8, 128, 128)
     args = lambda cfg, f, e: (ctypes.byref(cfg), fake, fake, 2, 8, f, e, fake, fake, need, None)  # noqa: E731
     bf = M.make_config(T=8, d=128, N=2, f=128, k=1, dtype="bf16")
     f32 = M.make_config(T=8, d=128, N=2, f=128, k=1, dtype="f32")
@@ -214,6 +214,19 @@ def test_e4m3_experts_host_checks():
     assert lib.moe_expert_ffn_e4m3(*args(bf, 128, ctypes.byref(bad))) == M.MOE_ERR_NULL
     assert lib.moe_layer_forward_e4m3(ctypes.byref(bf), *([None] * 3), None, *([None] * 8), 0,
                                       None) == M.MOE_ERR_NULL
+
+
+def test_e4m3_workspace_sizes():
+    # control block, bf16 hidden rows, e4m3 token rows + scales, e4m3 hidden rows + scales
+    a = lambda n: (n + 255) // 256 * 256  # noqa: E731
+    R, d, f = 1000, 4096, 14336
+    assert M.ffn_workspace_size_e4m3(R, d, f) == \
+        M.MOE_CTRL_BYTES + a(R * f * 2) + a(R * d) + a(R * 4) + a(R * f) + a(R * 4)
+    cfg = M.make_config(T=64, d=256, N=8, f=512, k=2)
+    R = M.sizes(cfg).rows_max
+    assert M.workspace_size_e4m3(cfg) == M.workspace_size(cfg) + a(R * 256) + a(R * 4) + \
+        a(R * 512) + a(R * 4)
+    assert M.workspace_size_e4m3(M.make_config(T=64, d=256, N=300, f=512, k=2)) == 0
 
 
 def test_status_strings():

@@ -29,7 +29,7 @@ def test_routed_weight_bytes_count_the_experts_hit():
     w = W.ALL["decode_bf16"]
     kept = np.array([3, 0, 9, 1, 0, 0, 7, 2])
     assert bench.routed_weight_bytes(w, kept) == 5 * 3 * w.d * w.f * 2
-    q = W.ALL["decode_bf16_w8"]
+    q = W.ALL["decode_e4m3"]
     per = 3 * q.d * q.f + 4 * (2 * q.f + q.d)  # e4m3 bytes + fp32 column scales
     assert bench.routed_weight_bytes(q, kept) == 5 * per
 

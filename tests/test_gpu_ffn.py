@@ -222,14 +222,27 @@ def test_expert_ffn_on_a_slice_of_the_gpu():
     assert not op[:a].any() and not op[b:].any()
 
 
+def _e4m3_codes(values) -> np.ndarray:
+    """Byte codes of values that are e4m3 values (exact conversion)."""
+    t = torch.from_numpy(np.ascontiguousarray(values, dtype=np.float32))
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def _a256(n):
+    return (n + 255) // 256 * 256
+
+
 @pytest.mark.parametrize("sizes,d,f", [
     ([130, 0, 170, 1, 249], 256, 384),
     ([8, 8, 7, 9, 8, 8, 8, 8], 512, 1408),     # decode-like: a handful of rows per expert
     ([300, 400], 128, 256),
+    ([600, 0, 513], 256, 512),                  # several 256-row pair tiles, ragged tails
 ])
-def test_expert_ffn_e4m3_against_oracle(sizes, d, f):
-    """e4m3 experts with per-column scales: the GPU result against the oracle
-    run on the dequantized weights (values times scales, exact)."""
+def test_expert_ffn_e4m3_against_oracle(sizes, d, f, gemm_form):
+    """FP8 experts (e4m3 x e4m3 on the tensor cores): the token rows' e4m3
+    codes and row scales bit for bit against the oracle's quantization, and the
+    output against the oracle's FP8 expert (weights dequantized, operand rows
+    quantized per row) within the bf16 tolerance."""
     S = len(sizes)
     off = _segments(sizes)
     P = int(off[-1])
@@ -238,23 +251,37 @@ def test_expert_ffn_e4m3_against_oracle(sizes, d, f):
     Wb = {n: _rand(shape, seed, scale) for n, shape, seed, scale in (
         ("W1", (S, d, f), 22, d ** -0.5), ("W3", (S, d, f), 23, d ** -0.5),
         ("W2", (S, f, d), 24, f ** -0.5))}
-    q = {n: W.quantize_e4m3(Wb[n]) for n in Wb}
-    deq = {n: O.dequantize_e4m3(q[n][0].numpy(), q[n][1].numpy()) for n in q}
+    q = {}
+    for n in Wb:  # per-column quantization, stored K-major
+        qb, sc = W.quantize_e4m3(Wb[n])
+        q[n] = (qb.transpose(-1, -2).contiguous(), sc)
+    deq = {n: O.dequantize_e4m3(q[n][0].numpy(), q[n][1].numpy(), kmajor=True) for n in q}
     cfg = M.make_config(T=1, d=d, N=S, f=f, k=1, dtype="bf16")
     dev = torch.device("cuda")
     qd = {n: (q[n][0].cuda(), q[n][1].cuda()) for n in q}
     ex = M.e4m3_experts(qd["W1"][0], qd["W3"][0], qd["W2"][0], qd["W1"][1], qd["W3"][1],
                         qd["W2"][1])
     op = torch.zeros((rows_max, d), dtype=torch.bfloat16, device=dev)
-    ws = torch.zeros(M.ffn_workspace_size(rows_max, f, "bf16"), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(M.ffn_workspace_size_e4m3(rows_max, d, f), dtype=torch.uint8, device=dev)
     M.moe_expert_ffn_e4m3(cfg, xp.cuda(), torch.from_numpy(off).cuda(), S, rows_max, f, ex, op, ws)
     torch.cuda.synchronize()
     assert M.moe_get_device_status(ws) == M.MOE_OK
+    # the workspace layout of moe_ffn_workspace_size_e4m3: control block, bf16
+    # hidden rows, e4m3 token rows, their scales, ...
+    o_xq = M.MOE_CTRL_BYTES + _a256(rows_max * f * 2)
+    o_xs = o_xq + _a256(rows_max * d)
+    w_h = ws.cpu().numpy()
+    xq = w_h[o_xq:o_xq + P * d].reshape(P, d)
+    xs = w_h[o_xs:o_xs + 4 * P].view(np.float32)
+    vals, scale = O.quantize_rows_e4m3(G.np32(xp[:P]))
+    assert np.array_equal(xs.view(np.uint32), scale.view(np.uint32)), "row scales differ"
+    assert np.array_equal(xq, _e4m3_codes(vals)), "e4m3 codes of the token rows differ"
     got = op.float().cpu().numpy()
     for s in range(S):
         a, b = int(off[s]), int(off[s + 1])
         if a < b:
-            ref = O.swiglu(G.np32(xp[a:b]), deq["W1"][s], deq["W3"][s], deq["W2"][s], "bf16")
+            ref = O.swiglu(G.np32(xp[a:b]), deq["W1"][s], deq["W3"][s], deq["W2"][s], "bf16",
+                           act_e4m3=True)
             G.assert_output_close(got[a:b], ref, "bf16", f"segment {s}")
     assert not op[P:].any()
 

@@ -215,7 +215,7 @@ def test_gamma_inf_equals_token_choice_bitwise():
     ("finegrained_bf16", 64),
     ("finegrained_bf16_expanded", 64),
     ("finegrained_bf16_device", 64),
-    ("decode_bf16_w8", None),
+    ("decode_e4m3", None),
 ])
 def test_benchmark_workloads_full_size(name, sample):
     """Full size. Sampled workloads check a random token sample plus every
