@@ -132,11 +132,10 @@ size_t moe_workspace_size(const moe_config* cfg);
 
 /* Every workspace (moe_layer_forward, moe_route, moe_expert_ffn,
  * moe_grouped_gemm) begins with a 1024-byte control block: the sticky status
- * word and the arrival counter of the selection kernel, whose last block
- * finishes the load statistics. The control block must be zero before the
+ * word, then reserved bytes. The control block must be zero before the
  * workspace's first use (allocate it zeroed, or call
- * moe_clear_device_status); every call leaves the counter at zero again.
- * Calls that share a workspace must not overlap on the GPU. */
+ * moe_clear_device_status). Calls that share a workspace must not overlap on
+ * the GPU. */
 #define MOE_CTRL_BYTES 1024
 
 /* Bytes of workspace moe_route needs (the control block). */
@@ -529,8 +528,8 @@ int moe_workspace_views(const moe_config* cfg, void* ws, moe_views_t* out);
  * first 4 bytes of its control block. */
 int moe_get_device_status(const void* ws, void* stream, int32_t* out_host);
 
-/* Enqueue a reset of ws's control block (MOE_CTRL_BYTES: status word and
- * arrival counters) to zero. */
+/* Enqueue a reset of ws's control block (MOE_CTRL_BYTES, starting with the
+ * status word) to zero. */
 int moe_clear_device_status(void* ws, void* stream);
 
 /* Static description of a status code. */

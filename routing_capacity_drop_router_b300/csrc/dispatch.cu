@@ -13,12 +13,16 @@
 //   x[t] is read once, 16 bytes per lane, and written to each of its rows
 //   (skipped when xp is null: the expert GEMM then gathers the rows itself
 //   through row_token).
+// With load statistics requested, one extra block (after the token blocks)
+// computes them from the selection's demand/kept and the router's column
+// sums while the others copy rows.
 #include <climits>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "device_common.cuh"
 #include "internal.h"
+#include "stats_final.cuh"
 
 namespace moe {
 namespace {
@@ -62,11 +66,16 @@ __global__ void __launch_bounds__(kDispThreads) dispatch_kernel(
     int rows_max,
     int32_t* __restrict__ expert_offsets, int32_t* __restrict__ row_token,
     float* __restrict__ row_gate, int32_t* __restrict__ tok_rows,
-    int32_t* __restrict__ coverage, E* __restrict__ xp) {
+    int32_t* __restrict__ coverage, E* __restrict__ xp, int token_blocks,
+    const int32_t* __restrict__ demand, const StatsArgs st) {
   __shared__ int s_off[257];
   __shared__ int s_rows[kDispWarps][kMaxRowsPerToken];
   pdl_launch_dependents();
   pdl_wait();
+  if (static_cast<int>(blockIdx.x) >= token_blocks) {  // the load-statistics block
+    stats_final_block(demand, kept, st.colsum, st.rows, T, N, st.stats);
+    return;
+  }
   scan_offsets(kept, N, s_off);
   if (blockIdx.x == 0)
     for (int e = threadIdx.x; e <= N; e += blockDim.x) expert_offsets[e] = s_off[e];
@@ -75,7 +84,7 @@ __global__ void __launch_bounds__(kDispThreads) dispatch_kernel(
   const int wib = threadIdx.x >> 5;
   int* rows = s_rows[wib];
   const int nvec = d * static_cast<int>(sizeof(E)) / 16;  // 16-byte vectors per row
-  const int warps_total = kDispWarps * gridDim.x;
+  const int warps_total = kDispWarps * token_blocks;
 
   for (int t = blockIdx.x * kDispWarps + wib; t < T; t += warps_total) {
     int nrows = 0;
@@ -153,22 +162,26 @@ cudaError_t launch_dispatch(int dtype, const void* x, const int32_t* cand_idx,
                             const float* cand_gate, const int32_t* slot, const int32_t* kept,
                             int T, int d, int N, int kc, int expert_choice, int64_t rows_max,
                             int32_t* expert_offsets, int32_t* row_token, float* row_gate,
-                            int32_t* tok_rows, int32_t* coverage, void* xp, cudaStream_t s) {
+                            int32_t* tok_rows, int32_t* coverage, void* xp, const int32_t* demand,
+                            const StatsArgs& st, cudaStream_t s) {
   const int rmax = rows_max > 0x7fffffff ? 0x7fffffff : static_cast<int>(rows_max);
   int blocks = (T + kDispWarps - 1) / kDispWarps;
   const int cap = device_sm_count() * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;  // still writes expert_offsets when T == 0
+  if (st.stats && (!demand || N > 256)) return cudaErrorInvalidValue;
+  const int grid = blocks + (st.stats ? 1 : 0);
+  static_assert(kDispThreads >= 256, "the statistics block needs 256 threads");
   if (dtype == 1) {
-    return launch_pdl(dispatch_kernel<__nv_bfloat16>, blocks, kDispThreads, 0, s,
+    return launch_pdl(dispatch_kernel<__nv_bfloat16>, grid, kDispThreads, 0, s,
                       static_cast<const __nv_bfloat16*>(x), cand_idx, cand_gate, slot, kept, T, d,
                       N, kc, expert_choice, rmax, expert_offsets, row_token, row_gate, tok_rows,
-                      coverage, static_cast<__nv_bfloat16*>(xp));
+                      coverage, static_cast<__nv_bfloat16*>(xp), blocks, demand, st);
   }
-  return launch_pdl(dispatch_kernel<float>, blocks, kDispThreads, 0, s,
+  return launch_pdl(dispatch_kernel<float>, grid, kDispThreads, 0, s,
                     static_cast<const float*>(x), cand_idx, cand_gate, slot, kept, T, d, N, kc,
                     expert_choice, rmax, expert_offsets, row_token, row_gate, tok_rows,
-                    coverage, static_cast<float*>(xp));
+                    coverage, static_cast<float*>(xp), blocks, demand, st);
 }
 
 }  // namespace moe

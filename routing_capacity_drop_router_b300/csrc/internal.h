@@ -32,12 +32,10 @@ cudaError_t launch_pdl(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem,
 cudaError_t launch_router_logits(int dtype, const void* x, const void* W_r, const float* bias,
                                  float* L, int T, int d, int N, cudaStream_t s);
 
-// The first kCtrlBytes of every workspace: the sticky status word, then the
-// arrival counter of the selection kernel's last-block statistics step (it
-// must start at zero: the workspace is zeroed, or moe_clear_device_status is
-// called, before first use; the last block resets it).
+// The first kCtrlBytes of every workspace: the sticky status word (it must
+// start at zero: the workspace is zeroed, or moe_clear_device_status is
+// called, before first use); the rest is reserved.
 constexpr size_t kCtrlBytes = 1024;
-constexpr int kCtrlSelectCounter = 1;    // int32 index in the control block
 constexpr int kRouteTile = 128;          // tokens per router tile (tensor-core M)
 
 // Per-token routing (route_token.cuh) inputs and outputs.
@@ -91,22 +89,21 @@ cudaError_t launch_stats_final(const int32_t* demand, const int32_t* kept,
 
 // Per-expert selection (token choice: rank only; capacity drop: top-cap by
 // gate; expert choice: top-cap tokens by score; group_size > 0: the experts of
-// each group of group_size share the capacity cap). With st.stats set, the
-// last block to finish also writes the load statistics (counter: the control
-// block's select counter).
+// each group of group_size share the capacity cap).
 cudaError_t launch_select(const int32_t* cand_idx, const float* cand_gate, int T, int kc, int N,
                           int expert_choice, int cap, int group_size, int32_t* slot, uint8_t* keep,
-                          int32_t* demand, int32_t* kept, const StatsArgs& st,
-                          uint32_t* counter, cudaStream_t s);
+                          int32_t* demand, int32_t* kept, cudaStream_t s);
 int select_max_tokens();
 
 // Offsets, row maps, token rows, per-token coverage (nullable) and the
-// gather of x into xp.
+// gather of x into xp; with st.stats set, one extra block writes the load
+// statistics from demand, kept and the column sums.
 cudaError_t launch_dispatch(int dtype, const void* x, const int32_t* cand_idx,
                             const float* cand_gate, const int32_t* slot, const int32_t* kept,
                             int T, int d, int N, int kc, int expert_choice, int64_t rows_max,
                             int32_t* expert_offsets, int32_t* row_token, float* row_gate,
-                            int32_t* tok_rows, int32_t* coverage, void* xp, cudaStream_t s);
+                            int32_t* tok_rows, int32_t* coverage, void* xp,
+                            const int32_t* demand, const StatsArgs& st, cudaStream_t s);
 
 // Grouped GEMM on e4m3 operands (tcgen05 kind::f8f6f4): A [rows_max, K]
 // e4m3 bytes with one fp32 scale per row (a_scale [rows_max]); B1, B3

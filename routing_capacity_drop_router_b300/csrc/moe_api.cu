@@ -419,8 +419,7 @@ int moe_capacity_drop(const moe_config* cfg, const int32_t* cand_idx, const floa
   if (!have(cand_gate, T) || !have(slot, T) || !demand || !kept || (!d.ec && !have(cand_idx, T)))
     return MOE_ERR_NULL;
   return status_from(launch_select(cand_idx, cand_gate, cfg->T, d.kc, cfg->N, d.ec ? 1 : 0, d.cap, d.device_group,
-                                   slot, keep, demand, kept, StatsArgs{}, nullptr,
-                                   as_stream(stream)));
+                                   slot, keep, demand, kept, as_stream(stream)));
 }
 
 int moe_dispatch(const moe_config* cfg, const void* x, const int32_t* cand_idx,
@@ -438,7 +437,8 @@ int moe_dispatch(const moe_config* cfg, const void* x, const int32_t* cand_idx,
   if (!aligned16(x) || !aligned16(xp)) return MOE_ERR_ALIGN;
   return status_from(launch_dispatch(cfg->dtype, x, cand_idx, cand_gate, slot, kept, cfg->T,
                                      cfg->d, cfg->N, d.kc, d.ec ? 1 : 0, d.rows_max, expert_offsets, row_token,
-                                     row_gate, tok_rows, coverage, xp, as_stream(stream)));
+                                     row_gate, tok_rows, coverage, xp, nullptr, StatsArgs{},
+                                     as_stream(stream)));
 }
 
 int moe_expert_ffn(const moe_config* cfg, const void* xp, const int32_t* offsets,
@@ -631,13 +631,13 @@ int layer_forward(const moe_config* cfg, const void* x, const void* W_router, co
   sa.rows = colsum_rows;
   sa.stats = stats;
   if (launch_select(cand_idx, cand_gate, c.T, d.kc, c.N, d.ec ? 1 : 0, d.cap, d.device_group, slot, keep, demand,
-                    kept, sa, reinterpret_cast<uint32_t*>(ctrl + kCtrlSelectCounter),
-                    s) != cudaSuccess ||
+                    kept, s) != cudaSuccess ||
       !tr.mark(1))
     return MOE_ERR_LAUNCH;
   if (launch_dispatch(c.dtype, x, cand_idx, cand_gate, slot, kept, c.T, c.d, c.N, d.kc,
                       d.ec ? 1 : 0, d.rows_max, offsets, row_token, row_gate, tok_rows,
-                      at<int32_t>(ws, L.coverage), fuse ? nullptr : xp, s) != cudaSuccess ||
+                      at<int32_t>(ws, L.coverage), fuse ? nullptr : xp, demand, sa, s) !=
+          cudaSuccess ||
       !tr.mark(1))
     return MOE_ERR_LAUNCH;
   if (w8)

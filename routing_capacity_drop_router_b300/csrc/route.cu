@@ -126,31 +126,28 @@ constexpr int kRouteWarpsPerBlock = 8;
 
 template <int W, int PER>
 __global__ void __launch_bounds__(kRouteWarpsPerBlock * 32) route_tokens_kernel(const RouteArgs a) {
-  __shared__ unsigned long long s_cs[256];
+  constexpr int kTokensPerBlock = kRouteWarpsPerBlock * (32 / W);
+  // p of the block's tokens for the column sums: kTokensPerBlock * W * PER <= 2048
+  __shared__ float s_p[kTokensPerBlock * W * PER];
   pdl_launch_dependents();
   pdl_wait();
-  constexpr int kTokensPerBlock = kRouteWarpsPerBlock * (32 / W);
   const int N = a.N;
-  unsigned long long* cs = a.colsum ? s_cs : nullptr;
-  if (cs) {
-    for (int e = threadIdx.x; e < N; e += blockDim.x) cs[e] = 0ull;
-    __syncthreads();
-  }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int ls = lane % W;
-  const int t = blockIdx.x * kTokensPerBlock + warp * (32 / W) + lane / W;
+  const int slot = warp * (32 / W) + lane / W;
+  const int t = blockIdx.x * kTokensPerBlock + slot;
   const bool valid = t < a.T;
   float l[PER];
 #pragma unroll
   for (int j = 0; j < PER; ++j) {
-    const int e = ls + W * j;
+    const int e = ls * PER + j;  // a lane's experts are contiguous
     l[j] = (valid && e < N) ? a.logits[static_cast<size_t>(t) * N + e] : 0.f;
   }
-  route_token_seg<W, PER>(a, t, valid, l, cs);
-  if (cs) {
+  route_token_seg<W, PER>(a, t, valid, l, a.colsum ? s_p + slot * N : nullptr);
+  if (a.colsum) {
     __syncthreads();
-    for (int e = threadIdx.x; e < N; e += blockDim.x)
-      a.colsum[static_cast<size_t>(blockIdx.x) * N + e] = cs[e];
+    const int rows = max(0, min(kTokensPerBlock, a.T - static_cast<int>(blockIdx.x) * kTokensPerBlock));
+    colsum_rows(s_p, rows, N, a.colsum + static_cast<size_t>(blockIdx.x) * N);
   }
 }
 
@@ -180,11 +177,12 @@ int route_tokens_colsum_rows(int T, int N) {
 
 cudaError_t launch_route_tokens(const RouteArgs& a, cudaStream_t s) {
   if (a.T == 0) return cudaSuccess;
+  // (W, PER) = (route_seg_width(N), route_seg_per(N))
   if (a.N <= 8) return route_launch<8, 1>(a, s);
-  if (a.N <= 16) return route_launch<16, 1>(a, s);
-  if (a.N <= 32) return route_launch<32, 1>(a, s);
-  if (a.N <= 64) return route_launch<32, 2>(a, s);
-  if (a.N <= 128) return route_launch<32, 4>(a, s);
+  if (a.N <= 16) return route_launch<8, 2>(a, s);
+  if (a.N <= 32) return route_launch<8, 4>(a, s);
+  if (a.N <= 64) return route_launch<8, 8>(a, s);
+  if (a.N <= 128) return route_launch<16, 8>(a, s);
   if (a.N <= 256) return route_launch<32, 8>(a, s);
   return cudaErrorInvalidValue;
 }

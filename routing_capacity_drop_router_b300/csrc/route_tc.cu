@@ -16,9 +16,11 @@
 // row i of its partial logits into the stage buffer of the CTA that routes
 // token i (CTA i / (128/C)), at the slot of its own rank; after a second
 // cluster barrier each CTA adds, for its 128/C tokens, the C partials in rank
-// order (= k order) and the bias, and routes them (route_token.cuh). So the
-// logits and every decision are deterministic, and no partial goes through
-// global memory.
+// order (= k order) and the bias (all threads, coalesced logit stores), then
+// routes them with W-lane warp segments, 256 / W tokens per pass
+// (route_token.cuh; 8 lanes of 8 contiguous experts each for N = 64, so the
+// ordered softmax sum crosses 8 lanes, not 64). So the logits and every
+// decision are deterministic, and no partial goes through global memory.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -80,7 +82,6 @@ __global__ void __launch_bounds__(kRThreads) router_tc_kernel(
   constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
                               ((kCols >> 3) << 17) | (static_cast<uint32_t>(kRM >> 4) << 24);
   extern __shared__ unsigned char smem_raw[];
-  __shared__ unsigned long long s_cs[256];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   unsigned char* smem = smem_raw + (base - raw);
@@ -108,7 +109,6 @@ __global__ void __launch_bounds__(kRThreads) router_tc_kernel(
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
-  for (int e = threadIdx.x; e < 256; e += blockDim.x) s_cs[e] = 0ull;  // blockDim >= 256
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(&ctrl->tmem_base)),
@@ -232,34 +232,40 @@ __global__ void __launch_bounds__(kRThreads) router_tc_kernel(
                  : "memory");
   }
 
-  // ---- routing of this CTA's tokens: rank*tpc + i, i < tpc, one W-lane
-  //      segment per token ----
-  const float* recv = reinterpret_cast<const float*>(smem);
+  // ---- routing of this CTA's tokens t0 + i, i < tpc ----
+  // (a) every thread: logits = the C partials added in rank order, plus the
+  //     bias, stored to global memory and in place into rank 0's slot
+  float* recv = reinterpret_cast<float*>(smem);
+  const int t0 = tile * kRM + static_cast<int>(rank) * tpc;
+  for (int idx = static_cast<int>(threadIdx.x); idx < tpc * N; idx += kRThreads) {
+    const int i = idx / N, e = idx - (idx / N) * N;
+    float v = recv[idx];
+    for (int src = 1; src < cl; ++src) v = __fadd_rn(v, recv[(src * tpc + i) * N + e]);
+    if (ra.bias) v = __fadd_rn(v, ra.bias[e]);
+    const int t = t0 + i;
+    if (ra.logits_out && t < T) ra.logits_out[static_cast<size_t>(t) * N + e] = v;
+    recv[idx] = v;
+  }
+  __syncthreads();
+  // (b) one W-lane segment per token, 256 / W tokens per pass
   const int ls = lane % W;
-  constexpr int kSegs = kRThreads / W;  // tokens per pass
+  constexpr int kSegs = kRThreads / W;
   for (int i0 = 0; i0 < tpc; i0 += kSegs) {
-    const int i = i0 + (static_cast<int>(threadIdx.x) / W);
-    const int t = tile * kRM + static_cast<int>(rank) * tpc + i;
+    const int i = i0 + static_cast<int>(threadIdx.x) / W;
+    const int t = t0 + i;
     const bool valid = i < tpc && t < T;
     float l[PER];
 #pragma unroll
     for (int j = 0; j < PER; ++j) {
-      const int e = ls + W * j;
-      float v = 0.f;
-      if (valid && e < N) {
-        v = recv[(0 * tpc + i) * N + e];
-        for (int src = 1; src < cl; ++src) v = __fadd_rn(v, recv[(src * tpc + i) * N + e]);
-        if (ra.bias) v = __fadd_rn(v, ra.bias[e]);
-        if (ra.logits_out) ra.logits_out[static_cast<size_t>(t) * N + e] = v;
-      }
-      l[j] = v;
+      const int e = ls * PER + j;
+      l[j] = (valid && e < N) ? recv[i * N + e] : 0.f;
     }
-    route_token_seg<W, PER>(ra, t, valid, l, ra.colsum ? s_cs : nullptr);
+    // p replaces the token's logits in its own row (read above by this segment)
+    route_token_seg<W, PER>(ra, t, valid, l, ra.colsum ? recv + i * N : nullptr);
   }
   if (ra.colsum) {
     __syncthreads();
-    for (int e = threadIdx.x; e < N; e += blockDim.x)
-      ra.colsum[static_cast<size_t>(blockIdx.x) * N + e] = s_cs[e];
+    colsum_rows(recv, max(0, min(tpc, T - t0)), N, ra.colsum + static_cast<size_t>(blockIdx.x) * N);
   }
 }
 
@@ -326,11 +332,12 @@ cudaError_t launch_router_tc(const void* x, const void* W_r, int d, const Router
   if (!make_tmap_2d_bf16(&mW, W_r, static_cast<uint64_t>(d), static_cast<uint64_t>(N), 64, kRK))
     return cudaErrorInvalidValue;
   const int nkb = d / kRK;
+  // (W, PER) = (route_seg_width(N), route_seg_per(N))
   if (N <= 8) return launch_router<1, 8, 1>(mX, mW, plan, nkb, ra, status, s);
-  if (N <= 16) return launch_router<1, 16, 1>(mX, mW, plan, nkb, ra, status, s);
-  if (N <= 32) return launch_router<1, 32, 1>(mX, mW, plan, nkb, ra, status, s);
-  if (N <= 64) return launch_router<1, 32, 2>(mX, mW, plan, nkb, ra, status, s);
-  if (N <= 128) return launch_router<2, 32, 4>(mX, mW, plan, nkb, ra, status, s);
+  if (N <= 16) return launch_router<1, 8, 2>(mX, mW, plan, nkb, ra, status, s);
+  if (N <= 32) return launch_router<1, 8, 4>(mX, mW, plan, nkb, ra, status, s);
+  if (N <= 64) return launch_router<1, 8, 8>(mX, mW, plan, nkb, ra, status, s);
+  if (N <= 128) return launch_router<2, 16, 8>(mX, mW, plan, nkb, ra, status, s);
   if (N <= 256) return launch_router<4, 32, 8>(mX, mW, plan, nkb, ra, status, s);
   return cudaErrorInvalidValue;
 }

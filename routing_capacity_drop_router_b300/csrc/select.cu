@@ -13,8 +13,9 @@
 //     over the 32-bit gate keys finds the capacity-th largest key K* and how
 //     many candidates equal to K* survive (the first ones in token order);
 //  3. an ordered pass writes each candidate's rank among the kept (ascending
-//     token) or -1;
-//  4. optionally, the last CTA to finish writes the layer's load statistics.
+//     token) or -1.
+// (The layer's load statistics are written by the dispatch kernel, which
+// runs next and overlaps them with its row copies.)
 //
 // Device-level capacity ("Capacity-Aware Inference", section 2 (3)): the
 // experts of a device, a group of group_size consecutive experts, share one
@@ -32,7 +33,6 @@
 
 #include "device_common.cuh"
 #include "internal.h"
-#include "stats_final.cuh"
 #include "tc_ptx.cuh"
 
 namespace moe {
@@ -118,15 +118,14 @@ __device__ __forceinline__ void radix_pick(const unsigned* hist, int need, int* 
 __global__ void __launch_bounds__(kSelThreads) select_kernel(
     const int32_t* __restrict__ cand_idx, const float* __restrict__ cand_gate, int T, int kc,
     int N, int expert_choice, int cap, int group_size, int clustered, int32_t* __restrict__ slot,
-    uint8_t* __restrict__ keep, int32_t* __restrict__ demand, int32_t* __restrict__ kept,
-    const StatsArgs st, uint32_t* __restrict__ counter) {
+    uint8_t* __restrict__ keep, int32_t* __restrict__ demand, int32_t* __restrict__ kept) {
   extern __shared__ __align__(16) unsigned char sel_smem[];
   int32_t* lflat = reinterpret_cast<int32_t*>(sel_smem);
   uint32_t* lkey = reinterpret_cast<uint32_t*>(lflat + T);
   __shared__ int warp_sums[32];
   __shared__ unsigned hist[256];
   __shared__ unsigned hsum[256];
-  __shared__ int s_bin, s_need, s_last, s_bound, s_fits, s_count, s_over;
+  __shared__ int s_bin, s_need, s_bound, s_fits, s_count, s_over;
 
   const int e = blockIdx.x;
   const int lane = threadIdx.x & 31;
@@ -524,25 +523,6 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
     kept[e] = k_e;
   }
 
-  // 4. load statistics: the last block to finish reads every expert's counts
-  if (st.stats) {
-    // thread 0 wrote demand/kept: it alone publishes them before arriving
-    if (threadIdx.x == 0) {
-      __threadfence();
-      const uint32_t old = atomicAdd(counter, 1u);
-      s_last = old == gridDim.x - 1;
-      if (s_last) {
-        // acquire side: the fence after observing the final count orders this
-        // block's reads of every other block's demand/kept after their
-        // release (fence, then arrival); the block barrier below carries the
-        // order to the block's other threads
-        __threadfence();
-        *counter = 0u;
-      }
-    }
-    __syncthreads();
-    if (s_last) stats_final_block(demand, kept, st.colsum, st.rows, T, N, st.stats);
-  }
 }
 
 }  // namespace
@@ -587,9 +567,7 @@ bool group_cluster_ok(int dev, int gs) {
 
 cudaError_t launch_select(const int32_t* cand_idx, const float* cand_gate, int T, int kc, int N,
                           int expert_choice, int cap, int group_size, int32_t* slot, uint8_t* keep,
-                          int32_t* demand, int32_t* kept, const StatsArgs& st, uint32_t* counter,
-                          cudaStream_t s) {
-  if (st.stats && !counter) return cudaErrorInvalidValue;
+                          int32_t* demand, int32_t* kept, cudaStream_t s) {
   static bool attr_set[64] = {};  // per device; setting it twice is harmless
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -618,7 +596,7 @@ cudaError_t launch_select(const int32_t* cand_idx, const float* cand_gate, int T
   cfg.attrs = attr;
   cfg.numAttrs = clustered ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, select_kernel, cand_idx, cand_gate, T, kc, N, expert_choice, cap,
-                            group_size, clustered, slot, keep, demand, kept, st, counter);
+                            group_size, clustered, slot, keep, demand, kept);
 }
 
 }  // namespace moe

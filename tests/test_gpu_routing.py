@@ -179,3 +179,46 @@ def test_router_workspace_reused_across_shapes():
         _assert_routing_of(w, *_route_own_logits(w, inp, rws))
     ctrl = rws[:G.M.MOE_CTRL_BYTES].view(torch.int32).cpu().numpy()
     assert (ctrl == 0).all(), "control block not back at zero"
+
+
+ROUTER_TAIL = [
+    # one CTA per tile (3 k-blocks of 64 do not split in two): 128 tokens per
+    # CTA, 256 experts, renormalised top-8
+    W.Workload("tail_c1_n256", T=300, d=192, N=256, f=64, k=8, renorm=True, zipf_s=1.0),
+    # 128 experts, expanded candidates from groups of 16, capacity drop
+    W.Workload("tail_n128_expanded", T=1000, d=512, N=128, f=64, k=4, m=4, group_size=16,
+               mode=W.CAPACITY_DROP, gamma=1.25),
+    # N not a power of two, expert choice, ragged last tile
+    W.Workload("tail_n24_ec", T=777, d=1024, N=24, f=64, k=3, mode=W.EXPERT_CHOICE),
+]
+
+
+@pytest.mark.parametrize("w", ROUTER_TAIL, ids=[w.name for w in ROUTER_TAIL])
+def test_router_tail_shapes_bit_exact(w):
+    """The router tail (partials summed in rank order, one thread per token)
+    routes its own logits exactly as the oracle does, at the shapes where the
+    tail's chunking and row rotation change: one CTA per tile, N = 256, N not
+    a power of two, a ragged last tile."""
+    inp = W.make_inputs(w, with_experts=False)
+    L, scores, idx, gate = _route_own_logits(w, inp)
+    bound = G.logit_bound(G.np32(inp["x"]), G.np32(inp["W_r"]),
+                          O.router_logits(G.np32(inp["x"]), G.np32(inp["W_r"]),
+                                          G.np32(inp["bias"])))
+    ref = O.router_logits(G.np32(inp["x"]), G.np32(inp["W_r"]), G.np32(inp["bias"]))
+    assert np.all(np.abs(L.astype(np.float64) - ref) <= bound)
+    _assert_routing_of(w, L, scores, idx, gate)
+
+
+def test_router_tail_ties_bit_exact():
+    """Integer-valued x and W_r make the logits exact and full of ties, so the
+    tail's tie-breaks (lower expert first) decide most of the top-k."""
+    w = W.Workload("tail_ties", T=513, d=256, N=64, f=64, k=6, renorm=True)
+    g = torch.Generator().manual_seed(77)
+    x = torch.randint(-1, 2, (w.T, w.d), generator=g).to(torch.bfloat16)
+    W_r = (torch.randint(-1, 2, (w.d, w.N), generator=g).float() / 4).to(torch.bfloat16)
+    inp = {"x": x, "W_r": W_r, "bias": None}
+    L, scores, idx, gate = _route_own_logits(w, inp)
+    ref = O.router_logits(G.np32(x), G.np32(W_r), None)
+    assert np.array_equal(L, ref)  # exact: small integers times quarters
+    assert (np.sort(L, axis=1)[:, 1:] == np.sort(L, axis=1)[:, :-1]).any(axis=1).mean() > 0.9
+    _assert_routing_of(w, L, scores, idx, gate)
