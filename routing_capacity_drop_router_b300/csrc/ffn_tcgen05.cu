@@ -28,12 +28,13 @@
 //              their bytes on CTA 0's full barrier.
 //              Row-gather form (GATHER): A row r is row row_src[r] of the
 //              token matrix x, so the dispatched copy of x is never written.
-//              All 32 lanes copy the A tile with 16-byte cp.async into the
-//              same swizzled layout TMA would produce (lane: chunk lane % 8 of
-//              rows 4i + lane / 8); a k-block's rows are announced on the full
-//              barrier (one arrival per CTA, after the copies land and a proxy
-//              fence) while up to stages - 1 later k-blocks are in flight;
-//              lane 0 still loads B by TMA.
+//              Four copy warps (warp 0 and warps 6-8) each copy 32 rows of
+//              the A tile with 16-byte cp.async into the same swizzled layout
+//              TMA would produce (lane: chunk lane % 8 of rows 32w + 4i +
+//              lane / 8); each warp announces a k-block's rows on the full
+//              barrier (one arrival per copy warp, after its copies land and a
+//              proxy fence) while up to stages - 1 later k-blocks are in
+//              flight; lane 0 of warp 0 still loads B by TMA.
 //   warp 1   : allocates 512 TMEM columns (two 256-column accumulators);
 //              lane 0 of CTA 0 issues tcgen05.mma and tcgen05.commit, whose
 //              arrivals are multicast to both CTAs' barriers.
@@ -76,6 +77,10 @@ constexpr int kABytes = kBM * kBK * 2;
 constexpr int kBoxBytes = 64 * kBK * 2;  // one 64-column TMA box of B
 constexpr int kTmemCols = 512;
 constexpr int kThreads = 192;
+constexpr int kCopyWarps = 4;  // row-gather form: warp 0 and warps 6..8 copy A rows
+constexpr int kThreadsGather = kThreads + 32 * (kCopyWarps - 1);
+template <bool GATHER>
+constexpr int threads_of() { return GATHER ? kThreadsGather : kThreads; }
 constexpr int kEpiWarps = 4;
 constexpr int kMaxSegments = 256;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
@@ -162,7 +167,7 @@ constexpr uint32_t fp8_idesc() {
 }
 
 template <bool SWIGLU, bool PAIR, bool GATHER, bool FP8>
-__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
+__global__ void __launch_bounds__(threads_of<GATHER>(), 1) grouped_gemm_tc_kernel(
     const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB1,
     const __grid_constant__ CUtensorMap tmB3, const int32_t* __restrict__ offsets, int S, int K,
     int n_out, int rows_max, __nv_bfloat16* __restrict__ out, int32_t* __restrict__ status,
@@ -193,8 +198,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
   // ---- set-up: barriers, tile table, TMEM ----
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      // GATHER: the expect_tx arrival plus one per CTA once its rows landed
-      mbar_init(smem_u32(&ctrl->full[s]), GATHER ? (PAIR ? 3 : 2) : 1);
+      // GATHER: the expect_tx arrival plus one per copy warp of each CTA
+      // once its rows landed
+      mbar_init(smem_u32(&ctrl->full[s]), GATHER ? 1 + kCopyWarps * (PAIR ? 2 : 1) : 1);
       mbar_init(smem_u32(&ctrl->empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -301,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
         tma_load_3d(sb + j * kBoxBytes, &tmB1, col0 + 64 * j, kb * kBK, seg, fb);
     }
   };
-  if (warp == 0 && (GATHER || lane == 0)) {
+  if ((warp == 0 && (GATHER || lane == 0)) || (GATHER && warp >= 2 + kEpiWarps)) {
     // ---------------- producer ----------------
     int stage = 0;
     uint32_t phase = 0;
@@ -311,7 +317,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
     bool ok = true;
     if constexpr (GATHER) {
       constexpr int kDepth = kStages - 1;  // k-blocks whose rows may still be in flight
-      constexpr int kRowsPerLane = kBM / 4;
+      constexpr int kRowsPerLane = kBM / (4 * kCopyWarps);
+      const int cw = warp == 0 ? 0 : warp - (1 + kEpiWarps);  // copy warp 0..3
+      const int rbase = 32 * cw;                                // its 32 rows of the tile
       const int rsub = lane >> 3, ch = lane & 7;
       const int lim = min(ctrl->seg_row[S], rows_max);  // rows that have a token
       int pend = 0, pend_stage = 0;  // k-blocks copied but not yet announced; the oldest
@@ -334,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
         bool bad = false;
 #pragma unroll
         for (int i = 0; i < kRowsPerLane; ++i) {
-          const int r = arow + 4 * i + rsub;
+          const int r = arow + rbase + 4 * i + rsub;
           int t = -1;
           if (r < lim) {
             t = row_src[r];
@@ -355,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
             break;
           }
           const uint32_t sa = stage0 + stage * G::kStageBytes;
-          if (lane == 0) {
+          if (cw == 0 && lane == 0) {
             const uint32_t fb_local = smem_u32(&ctrl->full[stage]);
             if (rank == 0) mbar_expect_tx(fb_local, G::kTxBytesB);
             issued[stage] = 1;
@@ -365,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
           const __nv_bfloat16* xk = xg + kb * kBK + ch * 8;
 #pragma unroll
           for (int i = 0; i < kRowsPerLane; ++i) {
-            const int r = 4 * i + rsub;
+            const int r = rbase + 4 * i + rsub;
             const int t = tok[i];
             cp_async16(sa + r * 128 + ((ch ^ (r & 7)) << 4),
                        xk + static_cast<size_t>(t < 0 ? 0 : t) * K, t < 0 ? 0u : 16u);
@@ -491,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(
         *abort_flag = 1;
         break;
       }
-  } else if (warp >= 2) {
+  } else if (warp >= 2 && warp < 2 + kEpiWarps) {
     // ---------------- epilogue ----------------
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     const uint32_t tempty0 = PAIR ? map_to_rank(smem_u32(&ctrl->tempty[0]), 0) : smem_u32(&ctrl->tempty[0]);
@@ -603,7 +611,7 @@ int pair_slots(int dev) {
   attr[0].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(device_sm_count() & ~1));
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(threads_of<GATHER>());
   cfg.dynamicSmemBytes = smem_bytes<true>();
   cfg.attrs = attr;
   cfg.numAttrs = 1;
@@ -670,7 +678,7 @@ cudaError_t launch_gemm(const CUtensorMap& mA, const CUtensorMap& mB1, const CUt
   attr[1].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(pair ? 2 * units : units));
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(threads_of<GATHER>());
   cfg.dynamicSmemBytes = pair ? smem_bytes<true>() : smem_bytes<false>();
   cfg.stream = s;
   cfg.attrs = attr;

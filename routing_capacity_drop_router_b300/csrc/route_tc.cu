@@ -191,9 +191,13 @@ __global__ void __launch_bounds__(kRThreads) router_tc_kernel(
       }
   }
   __syncwarp();
-  int acc_ok = 1;
-  if (lane == 0) acc_ok = mbar_wait(smem_u32(&ctrl->acc_full), 0u, abort_flag, kRWaitNs);
-  acc_ok = __shfl_sync(0xffffffffu, acc_ok, 0);
+  // one thread waits for the accumulator; the others wait at the block
+  // barrier, which takes no issue slots from the producer and the MMA issuer
+  __shared__ int s_acc_ok;
+  if (warp == 2 && lane == 0)
+    s_acc_ok = mbar_wait(smem_u32(&ctrl->acc_full), 0u, abort_flag, kRWaitNs) ? 1 : 0;
+  __syncthreads();
+  const int acc_ok = s_acc_ok;
   // the stage buffers (written by TMA, read by the tensor cores) are about to
   // receive generic stores from the cluster
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -211,14 +215,26 @@ __global__ void __launch_bounds__(kRThreads) router_tc_kernel(
     const uint32_t dst_local = base + static_cast<uint32_t>(((rank * tpc) + (r % tpc)) * N * 4);
     const uint32_t dst = map_to_rank(dst_local, owner);
     const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    for (int c = 0; c < N; c += 16) {
-      uint32_t v[16];
-      tc_ld16(taddr + c, v);
+    for (int c0 = 0; c0 < N; c0 += 64) {  // up to four 16-column loads, then one wait
+      uint32_t v[64];
+      const int nchunk = min(4, (N - c0 + 15) / 16);  // warp-uniform
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (q < nchunk) tc_ld16(taddr + c0 + 16 * q, v + 16 * q);
       tc_wait_ld();
-      const int nv = (N - c) >= 16 ? 4 : (N - c) / 4;  // N % 8 == 0
-      for (int i = 0; i < nv; ++i)
-        st_cluster_v4(dst + (c + 4 * i) * 4, __uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                      __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int c = c0 + 16 * q;
+        if (q >= nchunk) break;
+        const int nv = (N - c) >= 16 ? 4 : (N - c) / 4;  // N % 8 == 0
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (i < nv)
+            st_cluster_v4(dst + (c + 4 * i) * 4, __uint_as_float(v[16 * q + 4 * i]),
+                          __uint_as_float(v[16 * q + 4 * i + 1]),
+                          __uint_as_float(v[16 * q + 4 * i + 2]),
+                          __uint_as_float(v[16 * q + 4 * i + 3]));
+      }
     }
   }
   tc_fence_before();
