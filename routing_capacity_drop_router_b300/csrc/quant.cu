@@ -12,9 +12,10 @@
 // so X[r][j] ~ value(Q[r][j]) * scale[r]. Both roundings are fixed IEEE
 // operations, so the codes are a fixed function of the bf16 inputs.
 //
-// One warp per row; the row is read twice (the maximum, then the codes; the
-// second read hits L2). Only rows below offsets[S] (the kept rows, read on the
-// device) are written.
+// One block per row (grid-stride over the rows); the row is read twice (the
+// maximum, a block reduction, then the codes; the second read hits L2), so a
+// few long rows (a decode batch's hidden rows) still spread over many SMs.
+// Only rows below offsets[S] (the kept rows, read on the device) are written.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
@@ -32,15 +33,16 @@ constexpr float kE4m3Max = 448.0f;
 __global__ void __launch_bounds__(kQThreads) quantize_rows_e4m3_kernel(
     const __nv_bfloat16* __restrict__ X, const int32_t* __restrict__ offsets, int S, int rows_max,
     int K, uint8_t* __restrict__ Q, float* __restrict__ scale) {
+  __shared__ float s_max[kQWarps];
   pdl_launch_dependents();
   pdl_wait();
   const int P = min(max(offsets[S], 0), rows_max);
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nvec = K / 8;  // 16-byte vectors of 8 bf16
-  for (int r = blockIdx.x * kQWarps + (threadIdx.x >> 5); r < P; r += gridDim.x * kQWarps) {
+  for (int r = blockIdx.x; r < P; r += gridDim.x) {
     const uint4* src = reinterpret_cast<const uint4*>(X + static_cast<size_t>(r) * K);
     float amax = 0.f;
-    for (int c = lane; c < nvec; c += 32) {
+    for (int c = threadIdx.x; c < nvec; c += kQThreads) {
       const uint4 q = __ldg(src + c);
       const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
 #pragma unroll
@@ -51,9 +53,14 @@ __global__ void __launch_bounds__(kQThreads) quantize_rows_e4m3_kernel(
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if (lane == 0) s_max[warp] = amax;
+    __syncthreads();
+    amax = s_max[0];
+#pragma unroll
+    for (int w = 1; w < kQWarps; ++w) amax = fmaxf(amax, s_max[w]);
     const float sc = amax > 0.f ? __fdiv_rn(amax, kE4m3Max) : 1.0f;
     uint2* dst = reinterpret_cast<uint2*>(Q + static_cast<size_t>(r) * K);
-    for (int c = lane; c < nvec; c += 32) {
+    for (int c = threadIdx.x; c < nvec; c += kQThreads) {
       const uint4 q = __ldg(src + c);
       const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
       uint32_t w[2];
@@ -69,7 +76,8 @@ __global__ void __launch_bounds__(kQThreads) quantize_rows_e4m3_kernel(
       }
       dst[c] = make_uint2(w[0], w[1]);
     }
-    if (lane == 0) scale[r] = sc;
+    if (threadIdx.x == 0) scale[r] = sc;
+    __syncthreads();  // s_max is reused by the next row
   }
 }
 
@@ -81,9 +89,8 @@ cudaError_t launch_quantize_rows_e4m3(const void* X, const int32_t* offsets, int
   if (S == 0 || rows_max == 0) return cudaSuccess;
   if (K <= 0 || K % 8) return cudaErrorInvalidValue;
   const int rmax = rows_max > 0x7fffffff ? 0x7fffffff : static_cast<int>(rows_max);
-  int blocks = static_cast<int>((rows_max + kQWarps - 1) / kQWarps);
-  const int cap = device_sm_count() * 8;
-  if (blocks > cap) blocks = cap;
+  const long long cap = device_sm_count() * 8;
+  const int blocks = static_cast<int>(rows_max < cap ? rows_max : cap);
   return launch_pdl(quantize_rows_e4m3_kernel, blocks, kQThreads, 0, s,
                     static_cast<const __nv_bfloat16*>(X), offsets, S, rmax, K, Q, scale);
 }
