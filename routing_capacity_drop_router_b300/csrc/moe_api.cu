@@ -704,8 +704,7 @@ int moe_expert_ffn_e4m3(const moe_config* cfg, const void* xp, const int32_t* of
   if (st != MOE_OK) return st;
   if (n_segments > kMaxN) return MOE_ERR_UNSUPPORTED;
   if (!xp || !offsets || !op || !ws) return MOE_ERR_NULL;
-  if (!aligned16(xp) || !aligned16(op) || (reinterpret_cast<uintptr_t>(ws) & 255u))
-    return MOE_ERR_ALIGN;
+  if (!aligned16(xp) || !aligned16(op) || !aligned16(ws)) return MOE_ERR_ALIGN;
   const FfnE4m3Layout L = ffn_e4m3_layout(rows_max, cfg->d, f);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
   return run_ffn_e4m3(xp, offsets, n_segments, rows_max, cfg->d, f, *experts, at<void>(ws, L.hp),

@@ -8,8 +8,8 @@
 // section 2 (2) Expanded Drop: m extra candidates from the token's own device.
 //
 // Lane l of the segment holds the contiguous experts e = l*PER ... l*PER +
-// PER - 1 (route_seg_shape picks W and PER for N: 8 lanes up to 64 experts,
-// so one warp routes 4 tokens at once).
+// PER - 1 (route_seg_width and route_seg_per pick W and PER for N: 8 lanes up
+// to 64 experts, so one warp routes 4 tokens at once).
 //   scores: m = max L; u_e = score_exp(L_e - m); Z = u_0 + u_1 + ... in
 //           ascending e: each lane adds its own run of experts to the running
 //           sum it receives from the lane before (W shuffles, PER adds each);

@@ -522,7 +522,6 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
     demand[e] = expert_choice ? k_e : n_all;
     kept[e] = k_e;
   }
-
 }
 
 }  // namespace

@@ -1,6 +1,7 @@
 // Final step of the load statistics (see stats.cu), run by one block of at
-// least 256 threads; reads demand/kept through L2, since in the selection
-// kernel's tail they were written by other blocks of the same launch.
+// least 256 threads (the dispatch kernel's extra block in the layer, the
+// statistics kernel for moe_load_stats); reads demand, kept and the column
+// sums through L2 (__ldcg), as earlier kernels of the stream wrote them.
 // Everything up to the last few divisions is integer arithmetic: this part's
 // fp64 pipe is narrow, and one thread does the handful of fp64 operations.
 #pragma once
