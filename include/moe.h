@@ -443,7 +443,8 @@ int moe_combine(const moe_config* cfg, const void* op, const float* row_gate,
  * doubles; layout above). scores [T, N] are the router probabilities; their
  * column sums are taken in fixed point (units of 2^-40, exact u64 sums), so
  * P_i does not depend on the order of the additions.
- * ws >= 8 * N * ceil(T / 8) bytes, 16-byte aligned (scratch).
+ * ws >= 8 * N * ceil(T / 32) bytes, 16-byte aligned (scratch: one row of N
+ * column sums per 32 tokens; it has no control block).
  */
 int moe_load_stats(const moe_config* cfg, const int32_t* demand, const int32_t* kept,
                    const float* scores, double* stats, void* ws, size_t ws_bytes, void* stream);

@@ -555,7 +555,9 @@ int moe_load_stats(const moe_config* cfg, const int32_t* demand, const int32_t* 
   int st = validate(cfg, &d);
   if (st != MOE_OK) return st;
   if (!demand || !kept || !have(scores, cfg->T) || !stats || !ws) return MOE_ERR_NULL;
-  if (ws_bytes < colsum_bytes(cfg->T, cfg->N)) return MOE_ERR_WORKSPACE;
+  const size_t need = static_cast<size_t>(colsum_kernel_rows(cfg->T)) *
+                      static_cast<size_t>(cfg->N) * sizeof(unsigned long long);
+  if (ws_bytes < need) return MOE_ERR_WORKSPACE;
   if (!aligned16(ws)) return MOE_ERR_ALIGN;
   cudaStream_t s = as_stream(stream);
   auto* colsum = static_cast<unsigned long long*>(ws);

@@ -8,8 +8,9 @@
 // fixed point (units of 2^-40, u64), which the routing kernels write as they
 // compute p; integer sums are exact, so the result does not depend on the
 // order of the additions. B itself is formed as one exact integer,
-// sum_i demand_i * colsum_i, divided once in fp64. The final step (stats_final.cuh) also runs as the
-// last-block tail of the selection kernel.
+// sum_i demand_i * colsum_i, divided once in fp64. Inside the layer the final
+// step (stats_final.cuh) runs in an extra block of the dispatch kernel; the
+// kernels here serve moe_load_stats.
 #include <cuda_runtime.h>
 
 #include "internal.h"

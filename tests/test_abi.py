@@ -149,6 +149,13 @@ def test_misaligned_and_small_workspace_rejected_before_any_launch():
         M.MOE_ERR_WORKSPACE
     assert lib.moe_grouped_gemm(M.MOE_BF16, fake, fake, 8, 64, 100, 128, fake, fake, fake, 1 << 20,
                                 None) == M.MOE_ERR_SHAPE
+    # moe_load_stats: 8 * N * ceil(T / 32) scratch bytes; a misaligned scratch of
+    # exactly that size passes the size check and fails the alignment one
+    stats_need = 8 * cfg.N * -(-cfg.T // 32)
+    assert lib.moe_load_stats(r, fake, fake, fake, fake, fake, stats_need - 1, None) == \
+        M.MOE_ERR_WORKSPACE
+    assert lib.moe_load_stats(r, fake, fake, fake, fake, fake + 8, stats_need, None) == \
+        M.MOE_ERR_ALIGN
 
 
 def test_expert_ffn_on_sms_host_checks():
