@@ -20,6 +20,16 @@
 //   48 KiB, and 6 stages of buffering fit in shared memory. SwiGLU tiles put
 //   128 columns of W1 (CTA 0) next to the same 128 columns of W3 (CTA 1), so
 //   one M=256, N=256 MMA produces both halves of a SwiGLU output tile.
+//   A segment's last tile, when it has fewer than 256 rows, runs transposed
+//   (out^T = W^T A^T): the weight columns become the MMA's M = 256 (MN-major,
+//   loaded as before) and the tile's n token rows its N, n rounded up to 32
+//   and split N/2 : N/2 over the pair, so the tail costs n/256 of a tile
+//   instead of a whole one. Each product is the same sum over the same k, and
+//   the outputs equal the padded form's bit for bit. The epilogue then reads
+//   a TMEM lane per output column and stores rows transposed, neighbouring
+//   lanes trading one value so each writes 32-bit words; under SwiGLU the
+//   gate and up halves of a column sit in different lane quadrants and meet
+//   through a small shared-memory exchange.
 //   Where clusters cannot be formed the same kernel runs one CTA per tile
 //   (128 rows, both B halves, cta_group::1, 4 stages).
 //   warp 0   : TMA producer of its CTA's operand tiles (128-byte swizzle); A
@@ -106,12 +116,29 @@ struct Geo {
                                      (static_cast<uint32_t>(kTileRows >> 4) << 24);
 };
 
+// Transposed tail tile of a pair (see the file comment): the weight columns
+// are the MMA's A operand (M = 256, MN-major as stored), the tile's n token
+// rows its B operand (N = n rounded up to 32, the step of N for a CTA-pair
+// MMA; K-major), so the accumulator holds out^T: TMEM lane = output column,
+// TMEM column = token row.
+__host__ __device__ constexpr uint32_t swap_idesc(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | (0u << 16) |
+         (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>((2 * kBM) >> 4) << 24);
+}
+// SwiGLU epilogue of a transposed tile: gate and up values of one output
+// column sit in different TMEM lane quadrants, so the epilogue warps swap
+// half of each 32-token chunk through shared memory (two buffers of
+// [2 column groups][2 directions][16 tokens][32 lanes] fp32).
+constexpr int kXchgFloats = 2 * 2 * 16 * 32;
+constexpr int kXchgBytes = 2 * kXchgFloats * 4;
+
 template <int STAGES>
 struct __align__(8) Ctrl {
   unsigned long long full[STAGES];
   unsigned long long empty[STAGES];
   unsigned long long tfull[2];
   unsigned long long tempty[2];
+  unsigned long long xchg[2];  // transposed SwiGLU exchange, one per buffer
   unsigned long long drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -121,9 +148,11 @@ struct __align__(8) Ctrl {
   int seg_row[kMaxSegments + 1];    // offsets[], so a tile decodes from shared memory
 };
 template <bool PAIR>
+constexpr int xchg_bytes() { return PAIR ? kXchgBytes : 0; }
+template <bool PAIR>
 constexpr int smem_bytes() {
   return 1024 /*alignment slack*/ + Geo<PAIR>::kStages * Geo<PAIR>::kStageBytes +
-         static_cast<int>(sizeof(Ctrl<Geo<PAIR>::kStages>));
+         xchg_bytes<PAIR>() + static_cast<int>(sizeof(Ctrl<Geo<PAIR>::kStages>));
 }
 static_assert(smem_bytes<true>() <= 227 * 1024, "shared memory");
 static_assert(smem_bytes<false>() <= 227 * 1024, "shared memory");
@@ -131,6 +160,28 @@ static_assert(smem_bytes<false>() <= 227 * 1024, "shared memory");
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Transposed-tile store: lane l of the warp holds column col (= c_base + l) of
+// rows t0 .. t0 + CNT - 1 in v[]. Neighbouring lanes trade one value, so that
+// the even lane writes columns (col, col + 1) of row t0 + i and the odd lane
+// the same two columns of row t0 + i + 1, each as one 32-bit word. Rows at
+// or beyond lim and columns at or beyond n_out (even) are not written.
+template <int CNT>
+__device__ __forceinline__ void store_transposed(const float* v, int t0, int col, int lim,
+                                                 int n_out, __nv_bfloat16* __restrict__ out,
+                                                 int lane) {
+  const int odd = lane & 1;
+  const int c = col & ~1;
+#pragma unroll
+  for (int i = 0; i < CNT; i += 2) {
+    const float send = odd ? v[i] : v[i + 1];
+    const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+    const int t = t0 + i + odd;
+    const uint32_t w = odd ? pack_bf16x2(recv, v[i + 1]) : pack_bf16x2(v[i], recv);
+    if (t < lim && c < n_out)
+      *reinterpret_cast<uint32_t*>(out + static_cast<size_t>(t) * n_out + c) = w;
+  }
 }
 
 template <bool PAIR>
@@ -173,9 +224,11 @@ __global__ void __launch_bounds__(threads_of<GATHER>(), 1) grouped_gemm_tc_kerne
     int n_out, int rows_max, __nv_bfloat16* __restrict__ out, int32_t* __restrict__ status,
     int withhold_kb, const __nv_bfloat16* __restrict__ xg, const int32_t* __restrict__ row_src,
     int x_rows, const float* __restrict__ a_scale, const float* __restrict__ b1_scale,
-    const float* __restrict__ b3_scale) {
+    const float* __restrict__ b3_scale, int swap_tails) {
   static_assert(!(GATHER && FP8), "the row gather reads bf16 token rows");
   using G = Geo<PAIR>;
+  // segment tails of a bf16 pair run transposed (swap_tails != 0)
+  constexpr bool kSwap = PAIR && !GATHER && !FP8;
   constexpr int kStages = G::kStages;
   // elements of k per 128-byte k-block
   constexpr int kKE = FP8 ? 2 * kBK : kBK;
@@ -184,7 +237,9 @@ __global__ void __launch_bounds__(threads_of<GATHER>(), 1) grouped_gemm_tc_kerne
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   unsigned char* smem = smem_raw + (base - raw);
-  Ctrl<kStages>* ctrl = reinterpret_cast<Ctrl<kStages>*>(smem + kStages * G::kStageBytes);
+  float* xchg = reinterpret_cast<float*>(smem + kStages * G::kStageBytes);
+  Ctrl<kStages>* ctrl =
+      reinterpret_cast<Ctrl<kStages>*>(smem + kStages * G::kStageBytes + xchg_bytes<PAIR>());
   volatile int* abort_flag = &ctrl->abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -206,6 +261,7 @@ __global__ void __launch_bounds__(threads_of<GATHER>(), 1) grouped_gemm_tc_kerne
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&ctrl->tfull[b]), 1);
       mbar_init(smem_u32(&ctrl->tempty[b]), (PAIR ? 2 : 1) * kEpiWarps);
+      mbar_init(smem_u32(&ctrl->xchg[b]), 32 * kEpiWarps);  // every epilogue thread
     }
     mbar_init(smem_u32(&ctrl->drain), 1);
     ctrl->abort_flag = 0;
@@ -271,11 +327,21 @@ __global__ void __launch_bounds__(threads_of<GATHER>(), 1) grouped_gemm_tc_kerne
     row_end = ctrl->seg_row[seg + 1];
     col0 = n_idx * tile_n;
   };
+  // A segment's last tile with fewer rows than a pair tile runs transposed,
+  // N = its rows rounded up to 32 (nsw), instead of padding the rows to 256.
+  auto transposed = [&](int row0, int row_end, int& nsw) {
+    const int n = min(row_end, rows_max) - row0;
+    nsw = (n + 31) & ~31;
+    return kSwap && swap_tails != 0 && n > 0 && n < G::kTileRows;
+  };
 
   const uint32_t stage0 = base;
   // B tiles of one k-block: CTA 0 of a pair W1 (or B) columns col0.., CTA 1
   // W3 columns col0.. (or B columns col0 + 128..); one CTA: all of them
-  auto load_b = [&](uint32_t sb, uint32_t fb, int seg, int col0, int kb) {
+  // A transposed SwiGLU tile gives each CTA 64 columns of W1 and the same 64
+  // of W3 (col0 + 64 * rank ..), so one CTA's TMEM holds gate and up of the
+  // same output columns.
+  auto load_b = [&](uint32_t sb, uint32_t fb, int seg, int col0, int kb, bool sw) {
     if (FP8) {  // K-major boxes of 128 k x 128 columns (16 KiB)
       constexpr int kBox8 = 128 * 128;
       if (PAIR) {
@@ -291,7 +357,11 @@ __global__ void __launch_bounds__(threads_of<GATHER>(), 1) grouped_gemm_tc_kerne
       }
       return;
     }
-    if (PAIR) {
+    if (PAIR && SWIGLU && sw) {
+      const int c = col0 + 64 * static_cast<int>(rank);
+      tma_load_3d_pair(sb, &tmB1, c, kb * kBK, seg, fb);
+      tma_load_3d_pair(sb + kBoxBytes, &tmB3, c, kb * kBK, seg, fb);
+    } else if (PAIR) {
       const CUtensorMap* mb = (SWIGLU && rank == 1) ? &tmB3 : &tmB1;
       const int c = SWIGLU ? col0 : col0 + static_cast<int>(rank) * 128;
       tma_load_3d_pair(sb, mb, c, kb * kBK, seg, fb);
@@ -368,7 +438,7 @@ __global__ void __launch_bounds__(threads_of<GATHER>(), 1) grouped_gemm_tc_kerne
             if (rank == 0) mbar_expect_tx(fb_local, G::kTxBytesB);
             issued[stage] = 1;
             issued_phase[stage] = phase;
-            load_b(sa + kABytes, PAIR ? map_to_rank(fb_local, 0) : fb_local, seg, col0, kb);
+            load_b(sa + kABytes, PAIR ? map_to_rank(fb_local, 0) : fb_local, seg, col0, kb, false);
           }
           const __nv_bfloat16* xk = xg + kb * kBK + ch * 8;
 #pragma unroll
@@ -393,9 +463,11 @@ __global__ void __launch_bounds__(threads_of<GATHER>(), 1) grouped_gemm_tc_kerne
       while (pend > 0) announce();
     } else {
     for (int tile = unit; ok && tile < total; tile += n_units) {
-      int seg, row0, row_end, col0;
+      int seg, row0, row_end, col0, nsw;
       decode(tile, seg, row0, row_end, col0);
-      const int arow = row0 + static_cast<int>(rank) * kBM;
+      const bool sw = transposed(row0, row_end, nsw);
+      // a transposed tile's rows are the B operand, split N/2 : N/2 over the pair
+      const int arow = row0 + static_cast<int>(rank) * (sw ? nsw / 2 : kBM);
       for (int kb = 0; kb < num_kb; ++kb) {
         const uint32_t fb_local = smem_u32(&ctrl->full[stage]);
         if (!mbar_wait(smem_u32(&ctrl->empty[stage]), phase ^ 1u, abort_flag, kWaitLimitNs)) {
@@ -413,7 +485,7 @@ __global__ void __launch_bounds__(threads_of<GATHER>(), 1) grouped_gemm_tc_kerne
           const uint32_t sa = stage0 + stage * G::kStageBytes;
           if (PAIR) tma_load_2d_pair(sa, &tmA, kb * kKE, arow, fb);
           else tma_load_2d(sa, &tmA, kb * kKE, arow, fb);
-          load_b(sa + kABytes, fb, seg, col0, kb);
+          load_b(sa + kABytes, fb, seg, col0, kb, sw);
         }
         if (++stage == kStages) {
           stage = 0;
@@ -453,6 +525,10 @@ __global__ void __launch_bounds__(threads_of<GATHER>(), 1) grouped_gemm_tc_kerne
       }
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * kBN);
+      int seg, row0, row_end, col0, nsw;
+      decode(tile, seg, row0, row_end, col0);
+      const bool sw = transposed(row0, row_end, nsw);
+      const uint32_t idesc = sw ? swap_idesc(nsw) : kIdesc;
       for (int kb = 0; kb < num_kb; ++kb) {
         // (row gather in a pair: CTA 1's rows are released at cluster scope)
         const bool got =
@@ -468,15 +544,17 @@ __global__ void __launch_bounds__(threads_of<GATHER>(), 1) grouped_gemm_tc_kerne
         const uint32_t sb = sa + kABytes;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {  // 32 bytes of k per MMA
-          const uint64_t ad = kmajor_desc(sa, kk);
-          const uint64_t bd = FP8 ? kmajor_desc(sb, kk) : mnmajor_desc(sb, kk, kBoxBytes);
+          // token rows (K-major) and weight columns; a transposed tile swaps them
+          const uint64_t rd = kmajor_desc(sa, kk);
+          const uint64_t wd = FP8 ? kmajor_desc(sb, kk) : mnmajor_desc(sb, kk, kBoxBytes);
+          const uint64_t ad = sw ? wd : rd, bd = sw ? rd : wd;
           const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
           if (FP8) {
-            if (PAIR) tc_mma_pair_f8(d_tmem, ad, bd, kIdesc, acc);
-            else tc_mma_f8(d_tmem, ad, bd, kIdesc, acc);
+            if (PAIR) tc_mma_pair_f8(d_tmem, ad, bd, idesc, acc);
+            else tc_mma_f8(d_tmem, ad, bd, idesc, acc);
           } else {
-            if (PAIR) tc_mma_pair(d_tmem, ad, bd, kIdesc, acc);
-            else tc_mma(d_tmem, ad, bd, kIdesc, acc);
+            if (PAIR) tc_mma_pair(d_tmem, ad, bd, idesc, acc);
+            else tc_mma(d_tmem, ad, bd, idesc, acc);
           }
         }
         if (PAIR) tc_commit_pair_mc(smem_u32(&ctrl->empty[stage]), 0x3);
@@ -504,6 +582,7 @@ __global__ void __launch_bounds__(threads_of<GATHER>(), 1) grouped_gemm_tc_kerne
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     const uint32_t tempty0 = PAIR ? map_to_rank(smem_u32(&ctrl->tempty[0]), 0) : smem_u32(&ctrl->tempty[0]);
     int local = 0;
+    int xuse = 0;  // exchange rounds so far (transposed SwiGLU tiles)
     for (int tile = unit; tile < total; tile += n_units, ++local) {
       const int buf = local & 1;
       const uint32_t use = static_cast<uint32_t>(local >> 1);
@@ -512,8 +591,76 @@ __global__ void __launch_bounds__(threads_of<GATHER>(), 1) grouped_gemm_tc_kerne
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      int seg, row0, row_end, col0;
+      int seg, row0, row_end, col0, nsw;
       decode(tile, seg, row0, row_end, col0);
+      const uint32_t taddr_t =
+          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * kBN);
+      if (transposed(row0, row_end, nsw)) {
+        // TMEM lane = output column, TMEM column = token row row0 + column
+        const int lim = min(row_end, rows_max);
+        const int ntok = lim - row0;
+        if (SWIGLU) {
+          // lanes 0-63: W1 (gate) columns col0 + 64 * rank ..; lanes 64-127:
+          // W3 (up) of the same columns. Warp q and warp q ^ 2 hold gate and
+          // up of 32 columns; per 32-token chunk each keeps 16 tokens and
+          // passes the other 16 to its partner.
+          const int grp = q & 1;
+          const bool gate = q < 2;
+          const int col = col0 + 64 * static_cast<int>(rank) + 32 * grp + lane;
+          const int keep0 = gate ? 0 : 16;  // tokens of the chunk this warp stores
+          for (int c0 = 0; c0 < ntok; c0 += 32) {
+            uint32_t a[32];
+            tc_ld32(taddr_t + c0, a);
+            tc_wait_ld();
+            const int b = xuse & 1;
+            const uint32_t par = static_cast<uint32_t>(xuse >> 1) & 1u;
+            ++xuse;
+            float* xb = xchg + b * kXchgFloats + grp * 1024;
+            float* put = xb + (gate ? 0 : 512);
+            const float* take = xb + (gate ? 512 : 0);
+            float mine[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float lo = __uint_as_float(a[i]), hi = __uint_as_float(a[16 + i]);
+              put[i * 32 + lane] = gate ? hi : lo;
+              mine[i] = gate ? lo : hi;
+            }
+            mbar_arrive(smem_u32(&ctrl->xchg[b]));
+            const int got = mbar_wait(smem_u32(&ctrl->xchg[b]), par, abort_flag, kWaitLimitNs);
+            if (!__all_sync(0xffffffffu, got)) {
+              ok = 0;
+              break;
+            }
+            float h[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float other = take[i * 32 + lane];
+              h[i] = gate ? silu_fast(mine[i]) * other : silu_fast(other) * mine[i];
+            }
+            store_transposed<16>(h, row0 + c0 + keep0, col, lim, n_out, out, lane);
+          }
+        } else {
+          const int col = col0 + 128 * static_cast<int>(rank) + 32 * q + lane;
+          for (int c0 = 0; c0 < ntok; c0 += 32) {
+            uint32_t a[32];
+            tc_ld32(taddr_t + c0, a);
+            tc_wait_ld();
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(a[i]);
+            store_transposed<32>(v, row0 + c0, col, lim, n_out, out, lane);
+          }
+        }
+        if (!ok) break;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          const uint32_t te = tempty0 + static_cast<uint32_t>(buf * sizeof(unsigned long long));
+          if (PAIR) mbar_arrive_cluster(te);
+          else mbar_arrive(te);
+        }
+        continue;
+      }
       const int row = row0 + static_cast<int>(rank) * kBM + q * 32 + lane;
       const bool valid = row >= 0 && row < row_end && row < rows_max;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * kBN);
@@ -668,6 +815,9 @@ cudaError_t launch_gemm(const CUtensorMap& mA, const CUtensorMap& mB1, const CUt
   const long long cap = pair ? slots : sms;
   if (units > cap) units = cap;
   const int rmax = rows_max > 0x7fffffff ? 0x7fffffff : static_cast<int>(rows_max);
+  // segment tails of the pair form run transposed unless MOE_GEMM_SWAP_TAILS=0
+  const char* sw_env = getenv("MOE_GEMM_SWAP_TAILS");
+  const int swap_tails = sw_env ? (sw_env[0] != '0') : 1;
 
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -686,10 +836,10 @@ cudaError_t launch_gemm(const CUtensorMap& mA, const CUtensorMap& mB1, const CUt
   if (pair)
     return cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<SWIGLU, true, GATHER, FP8>, mA, mB1,
                               mB3, offsets, S, K, n_out, rmax, o, status, withhold_kb, xg, row_src,
-                              x_rows, a_scale, b1_scale, b3_scale);
+                              x_rows, a_scale, b1_scale, b3_scale, swap_tails);
   return cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<SWIGLU, false, GATHER, FP8>, mA, mB1,
                             mB3, offsets, S, K, n_out, rmax, o, status, withhold_kb, xg, row_src,
-                            x_rows, a_scale, b1_scale, b3_scale);
+                            x_rows, a_scale, b1_scale, b3_scale, swap_tails);
 }
 
 }  // namespace

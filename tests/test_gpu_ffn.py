@@ -19,12 +19,38 @@ def _segments(sizes):
     return off
 
 
-@pytest.fixture(params=["cta_pairs", "single_cta"])
+@pytest.fixture(params=["cta_pairs", "cta_pairs_padded", "single_cta"])
 def gemm_form(request, monkeypatch):
-    """Run a bf16 case through both forms of the tcgen05 grouped GEMM: CTA
-    pairs (cta_group::2, 256-row tiles) and one CTA per 128-row tile."""
-    monkeypatch.setenv("MOE_GEMM_CTA_PAIRS", "1" if request.param == "cta_pairs" else "0")
+    """Run a bf16 case through every form of the tcgen05 grouped GEMM: CTA
+    pairs (cta_group::2, 256-row tiles) whose segment tails run transposed
+    (the default), the same pairs with the tails padded to 256 rows, and one
+    CTA per 128-row tile."""
+    monkeypatch.setenv("MOE_GEMM_CTA_PAIRS", "0" if request.param == "single_cta" else "1")
+    monkeypatch.setenv("MOE_GEMM_SWAP_TAILS", "0" if request.param == "cta_pairs_padded" else "1")
     return request.param
+
+
+# one segment per tail class of a 256-row pair tile: tails of 1..255 rows
+# (a transposed tile's N = 32..256 after rounding up to 32; tails that end in
+# either half of the pair's N/2 : N/2 token split), whole tiles, and a tile
+# plus a tail
+TAIL_SIZES = [1, 7, 8, 9, 15, 16, 17, 31, 33, 100, 127, 128, 129, 200, 240, 255, 256, 257, 513]
+
+
+@pytest.mark.parametrize("K,n_out", [(192, 320), (1024, 256)])
+def test_grouped_gemm_every_tail_class(K, n_out, gemm_form):
+    """The grouped GEMM over segments of every tail size against fp64
+    products; n_out = 320 leaves the last n-tile of each segment a quarter
+    full. Rows past the last segment stay untouched."""
+    _grouped_gemm_case(TAIL_SIZES, K, n_out)
+
+
+@pytest.mark.parametrize("d,f", [(320, 192), (256, 1408)])
+def test_expert_ffn_every_tail_class(d, f, gemm_form):
+    """The SwiGLU expert over segments of every tail size against the oracle;
+    f = 192 leaves GEMM1's last n-tile half full (a transposed tile's second
+    CTA then holds no output column)."""
+    _expert_ffn_case(TAIL_SIZES, d, f)
 
 
 def _rand(shape, seed, scale=1.0, dtype=torch.bfloat16):
@@ -41,6 +67,10 @@ def _rand(shape, seed, scale=1.0, dtype=torch.bfloat16):
     ([77, 300, 5], 2048, 512),    # few tiles, long K, ragged rows
 ])
 def test_grouped_gemm_bf16_against_torch(sizes, K, n_out, gemm_form):
+    _grouped_gemm_case(sizes, K, n_out)
+
+
+def _grouped_gemm_case(sizes, K, n_out):
     S = len(sizes)
     off = _segments(sizes)
     P = int(off[-1])
@@ -70,6 +100,10 @@ def test_grouped_gemm_bf16_against_torch(sizes, K, n_out, gemm_form):
     ([77], 2048, 1408),
 ])
 def test_expert_ffn_bf16_against_oracle(sizes, d, f, gemm_form):
+    _expert_ffn_case(sizes, d, f)
+
+
+def _expert_ffn_case(sizes, d, f):
     S = len(sizes)
     off = _segments(sizes)
     P = int(off[-1])
