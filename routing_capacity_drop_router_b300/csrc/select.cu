@@ -115,6 +115,50 @@ __device__ __forceinline__ void radix_pick(const unsigned* hist, int need, int* 
   }
 }
 
+// Warp-level pick over a 256-bin histogram (bin and need lane-uniform).
+// Lane l reads bins l, l + 32, ... (no bank conflicts): the 32-bin block
+// holding the need-th largest key is found from the top by warp sums, then
+// the bin inside it by a suffix scan over the lanes.
+__device__ __forceinline__ void radix_pick_warp(const unsigned* hist, int need, int& bin_out,
+                                                int& need_out) {
+  const int lane = threadIdx.x & 31;
+  unsigned c[8], t[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) t[q] = c[q] = hist[32 * q + lane];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {  // the eight block sums side by side
+#pragma unroll
+    for (int q = 0; q < 8; ++q) t[q] += __shfl_xor_sync(0xffffffffu, t[q], o);
+  }
+  unsigned above = 0u;  // keys in the blocks above the chosen one
+  int q = 0;
+  unsigned cb = c[0];  // this lane's count in the chosen block
+  bool found = false;
+#pragma unroll
+  for (int j = 7; j >= 0; --j) {
+    if (!found && above + t[j] >= static_cast<unsigned>(need)) {
+      found = true;
+      q = j;
+      cb = c[j];
+    } else if (!found) {
+      above += t[j];
+    }
+  }
+  // inclusive suffix over lanes >= lane inside block q
+  unsigned suf = cb;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned v = __shfl_down_sync(0xffffffffu, suf, o);
+    if (lane + o < 32) suf += v;
+  }
+  const unsigned a = above + suf - cb;  // keys in higher bins
+  const bool hit = a < static_cast<unsigned>(need) && static_cast<unsigned>(need) <= a + cb;
+  const unsigned hb = __ballot_sync(0xffffffffu, hit);
+  const int src = __ffs(hb) - 1;
+  bin_out = 32 * q + src;
+  need_out = need - static_cast<int>(__shfl_sync(0xffffffffu, a, src));
+}
+
 __global__ void __launch_bounds__(kSelThreads) select_kernel(
     const int32_t* __restrict__ cand_idx, const float* __restrict__ cand_gate, int T, int kc,
     int N, int expert_choice, int cap, int group_size, int clustered, int32_t* __restrict__ slot,
@@ -125,6 +169,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
   __shared__ int warp_sums[32];
   __shared__ unsigned hist[256];
   __shared__ unsigned hsum[256];
+  __shared__ unsigned hist3[3 * 256];  // per-expert radix: three rotating histograms
   __shared__ int s_bin, s_need, s_bound, s_fits, s_count, s_over;
 
   const int e = blockIdx.x;
@@ -446,9 +491,18 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
     uint32_t prefix = 0u, pmask = 0u;
     int need = cap;
     if (cap > 0) {
-      for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int b = threadIdx.x; b < 256; b += blockDim.x) hist[b] = 0u;
-        __syncthreads();
+      // Two barriers per pass: pass p fills histogram p % 3 and clears (p+1)
+      // % 3 for the next pass (last read by the pick of pass p - 2, before
+      // the barriers of pass p - 1); warp 0 finds the bin and hands it over
+      // at the second barrier (read by every warp before the next pass's
+      // first barrier, after which warp 0 writes it again).
+      for (int b = threadIdx.x; b < 256; b += blockDim.x) hist3[b] = 0u;
+      __syncthreads();
+      int pass = 0;
+      for (int shift = 24; shift >= 0; shift -= 8, ++pass) {
+        unsigned* h = hist3 + 256 * (pass % 3);
+        unsigned* h_next = hist3 + 256 * ((pass + 1) % 3);
+        for (int b = threadIdx.x; b < 256; b += blockDim.x) h_next[b] = 0u;
         for (int i0 = 0; i0 < n; i0 += blockDim.x) {  // uniform trip count per warp
           const int i = i0 + static_cast<int>(threadIdx.x);
           int bin = -1;
@@ -456,16 +510,28 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
             const uint32_t kk = lkey[i];
             if ((kk & pmask) == prefix) bin = static_cast<int>((kk >> shift) & 255u);
           }
-          const unsigned peers = __match_any_sync(0xffffffffu, bin);
-          if (bin >= 0 && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+          if (pass == 0) {
+            // the top byte is shared by most gates of one expert: one
+            // atomic per distinct bin of the warp
+            const unsigned peers = __match_any_sync(0xffffffffu, bin);
+            if (bin >= 0 && lane == __ffs(peers) - 1) atomicAdd(&h[bin], __popc(peers));
+          } else if (bin >= 0) {  // lower bytes spread over the bins
+            atomicAdd(&h[bin], 1u);
+          }
         }
         __syncthreads();
-        if (threadIdx.x < 32) radix_pick(hist, need, &s_bin, &s_need);
+        if (threadIdx.x < 32) {
+          int bin, left;
+          radix_pick_warp(h, need, bin, left);
+          if (lane == 0) {
+            s_bin = bin;
+            s_need = left;
+          }
+        }
         __syncthreads();
         prefix |= static_cast<uint32_t>(s_bin) << shift;
         pmask |= 255u << shift;
         need = s_need;
-        __syncthreads();
       }
     }
     const uint32_t thr = prefix;
