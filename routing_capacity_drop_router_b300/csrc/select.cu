@@ -79,6 +79,29 @@ __device__ __forceinline__ int warp_exclusive_offset(int warp_total, int* warp_s
   return excl;
 }
 
+// The same with two barriers: `warp_sums` must alternate between two
+// 32-int buffers on consecutive calls (the call after next reuses a buffer
+// only after every warp has passed the intervening call's first barrier, so
+// after it has read this call's sums).
+__device__ __forceinline__ int warp_exclusive_offset2(int warp_total, int* warp_sums, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  if (lane == 0) warp_sums[warp] = warp_total;
+  __syncthreads();
+  if (warp == 0) {
+    int w = (lane < nwarps) ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += n;
+    }
+    warp_sums[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  total = warp_sums[nwarps - 1];
+  return warp ? warp_sums[warp - 1] : 0;
+}
+
 // Warp 0: given a 256-bin histogram and `need` (>= 1) keys still to place,
 // find the bin that holds the need-th largest key and how many of the keys to
 // place fall in it (s_bin, s_need).
@@ -167,6 +190,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
   int32_t* lflat = reinterpret_cast<int32_t*>(sel_smem);
   uint32_t* lkey = reinterpret_cast<uint32_t*>(lflat + T);
   __shared__ int warp_sums[32];
+  __shared__ int warp_sums2[2 * 32];  // alternating buffers of warp_exclusive_offset2
+  int scan_use = 0;
   __shared__ unsigned hist[256];
   __shared__ unsigned hsum[256];
   __shared__ unsigned hist3[3 * 256];  // per-expert radix: three rotating histograms
@@ -224,7 +249,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
         }
       }
       int tot;
-      int pos = n + warp_exclusive_offset(cnt, warp_sums, tot);
+      int pos = n + warp_exclusive_offset2(cnt, warp_sums2 + 32 * (scan_use++ & 1), tot);
 #pragma unroll
       for (int j = 0; j < kSelRounds; ++j) {
         const int i = w0 + 32 * j;
@@ -558,7 +583,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
       // one scan carries both warp counts (above in the high half, equal in
       // the low half; each < 2^16)
       int tot;
-      const int ex = warp_exclusive_offset((gt_w << 16) | eq_w, warp_sums, tot);
+      const int ex =
+          warp_exclusive_offset2((gt_w << 16) | eq_w, warp_sums2 + 32 * (scan_use++ & 1), tot);
       int gt_before = (ex >> 16), eq_before = eq_base + (ex & 0xffff);
       // kept before an entry = above-thr before it + min(equal before it, need_eq)
 #pragma unroll
