@@ -343,3 +343,34 @@ def test_expert_ffn_f32_against_oracle(sizes, d, f):
             continue
         ref = O.swiglu(xp[a:b].numpy(), W1[s].numpy(), W3[s].numpy(), W2[s].numpy(), "f32")
         G.assert_output_close(got[a:b], ref, "f32", f"segment {s}")
+
+
+def test_transposed_tails_equal_padded_bit_for_bit(monkeypatch):
+    """A segment's last tile computed transposed (the default in pair form)
+    gives the same bits as the padded 256-row tile (MOE_GEMM_SWAP_TAILS=0):
+    each output is the same sum over the same k."""
+    monkeypatch.setenv("MOE_GEMM_CTA_PAIRS", "1")
+    sizes, d, f = TAIL_SIZES, 320, 192
+    S = len(sizes)
+    off = torch.from_numpy(_segments(sizes)).cuda()
+    rows_max = int(sum(sizes)) + 5
+    dev = torch.device("cuda")
+    xp = _rand((rows_max, d), 51).cuda()
+    W1 = _rand((S, d, f), 52, d ** -0.5).cuda()
+    W3 = _rand((S, d, f), 53, d ** -0.5).cuda()
+    W2 = _rand((S, f, d), 54, f ** -0.5).cuda()
+    B = _rand((S, d, 320), 55, d ** -0.5).cuda()
+    cfg = M.make_config(T=1, d=d, N=S, f=f, k=1, dtype="bf16")
+    outs = []
+    for swap in ("1", "0"):
+        monkeypatch.setenv("MOE_GEMM_SWAP_TAILS", swap)
+        op = torch.zeros((rows_max, d), dtype=torch.bfloat16, device=dev)
+        ws = torch.zeros(M.ffn_workspace_size(rows_max, f, "bf16"), dtype=torch.uint8, device=dev)
+        M.moe_expert_ffn(cfg, xp, off, S, rows_max, f, W1, W3, W2, op, ws)
+        g = torch.zeros((rows_max, 320), dtype=torch.bfloat16, device=dev)
+        M.moe_grouped_gemm("bf16", xp, off, S, rows_max, d, 320, B, g, ws)
+        torch.cuda.synchronize()
+        assert M.moe_get_device_status(ws) == M.MOE_OK
+        outs.append((op.cpu(), g.cpu()))
+    assert torch.equal(outs[0][0], outs[1][0]), "expert FFN: transposed and padded tails differ"
+    assert torch.equal(outs[0][1], outs[1][1]), "grouped GEMM: transposed and padded tails differ"
