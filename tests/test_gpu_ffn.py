@@ -37,11 +37,13 @@ def gemm_form(request, monkeypatch):
 TAIL_SIZES = [1, 7, 8, 9, 15, 16, 17, 31, 33, 100, 127, 128, 129, 200, 240, 255, 256, 257, 513]
 
 
-@pytest.mark.parametrize("K,n_out", [(192, 320), (1024, 256)])
+@pytest.mark.parametrize("K,n_out", [(192, 320), (1024, 256), (64, 64), (64, 448)])
 def test_grouped_gemm_every_tail_class(K, n_out, gemm_form):
     """The grouped GEMM over segments of every tail size against fp64
     products; n_out = 320 leaves the last n-tile of each segment a quarter
-    full. Rows past the last segment stay untouched."""
+    full, n_out = 64 is a single weight box (the second CTA of a pair holds no
+    output column), K = 64 a single k-block. Rows past the last segment stay
+    untouched."""
     _grouped_gemm_case(TAIL_SIZES, K, n_out)
 
 
