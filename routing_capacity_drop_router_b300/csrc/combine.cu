@@ -3,10 +3,12 @@
 // MoE differs from the Transformer").
 //
 // One warp per token; the token's rows (ascending expert) and gates are staged
-// in shared memory, then each lane walks 16-byte column vectors (two per
-// pass, the loads of two rows issued before their FMAs): for every row
-// an FMA into fp32 accumulators in a fixed order (ascending expert, shared
-// expert last), one rounding to the output dtype at the end.
+// in shared memory, the shared expert's row last with gate 1 (fma(1, v, acc)
+// rounds v + acc once, as an add would), then each lane walks 16-byte column
+// vectors (two per pass, the loads of RB rows issued before their FMAs: 2 for
+// top-2 tokens, 4 when a token may have more rows): for every row an FMA into
+// fp32 accumulators in a fixed order (ascending expert, shared expert last),
+// one rounding to the output dtype at the end.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -18,9 +20,9 @@ namespace {
 
 constexpr int kCombThreads = 256;
 constexpr int kCombWarps = kCombThreads / 32;
-constexpr int kCombMaxRows = 256;
+constexpr int kCombMaxRows = 257;  // up to 256 routed rows, then the shared expert's
+constexpr int kShared = -2;        // row marker: the shared expert's output row
 constexpr int kU = 2;   // 16-byte column vectors per lane per pass
-constexpr int kRB = 2;  // rows loaded per batch (k = 2 in one batch)
 // few registers, so that 32+ warps per SM keep enough 16-byte loads in flight
 constexpr int kCombMinBlocks = 4;
 
@@ -56,8 +58,9 @@ template <> struct Pack<float> {
   }
 };
 
-template <typename E>
-__global__ void __launch_bounds__(kCombThreads, kCombMinBlocks) combine_kernel(
+template <typename E, int kRB>
+__global__ void __launch_bounds__(kCombThreads, kRB > 2 ? kCombMinBlocks - 1 : kCombMinBlocks)
+    combine_kernel(
     const E* __restrict__ op, const float* __restrict__ row_gate,
     const int32_t* __restrict__ tok_rows, const E* __restrict__ shared_out, E* __restrict__ y,
     int T, int d, int kc, int rows_max) {
@@ -83,9 +86,15 @@ __global__ void __launch_bounds__(kCombThreads, kCombMinBlocks) combine_kernel(
       }
       nrows += __popc(b);
     }
+    if (shared_out) {  // the shared expert's row, last, gate 1
+      if (lane == 0) {
+        s_row[wib][nrows] = kShared;
+        s_gate[wib][nrows] = 1.0f;
+      }
+      ++nrows;
+    }
     __syncwarp();
-    const uint4* sh = shared_out ? reinterpret_cast<const uint4*>(shared_out + static_cast<size_t>(t) * d)
-                                 : nullptr;
+    const E* sh = shared_out ? shared_out + static_cast<size_t>(t) * d : nullptr;
     uint4* dst = reinterpret_cast<uint4*>(y + static_cast<size_t>(t) * d);
     // kU column vectors per lane and up to kRB rows loaded before their FMAs,
     // so each lane keeps kU * kRB 16-byte loads in flight
@@ -100,8 +109,9 @@ __global__ void __launch_bounds__(kCombThreads, kCombMinBlocks) combine_kernel(
 #pragma unroll
         for (int rr = 0; rr < kRB; ++rr) {
           if (r0 + rr < nrows) {
-            const uint4* src =
-                reinterpret_cast<const uint4*>(op + static_cast<size_t>(s_row[wib][r0 + rr]) * d);
+            const int row = s_row[wib][r0 + rr];
+            const uint4* src = reinterpret_cast<const uint4*>(
+                row == kShared ? sh : op + static_cast<size_t>(row) * d);
 #pragma unroll
             for (int u = 0; u < kU; ++u)
               if (c0 + 32 * u < nvec) q[rr][u] = __ldg(src + c0 + 32 * u);
@@ -126,15 +136,7 @@ __global__ void __launch_bounds__(kCombThreads, kCombMinBlocks) combine_kernel(
 #pragma unroll
       for (int u = 0; u < kU; ++u) {
         const int c = c0 + 32 * u;
-        if (c < nvec) {
-          if (sh) {
-            float v[V];
-            Pack<E>::unpack(__ldg(sh + c), v);
-#pragma unroll
-            for (int i = 0; i < V; ++i) acc[u][i] += v[i];
-          }
-          dst[c] = Pack<E>::pack(acc[u]);
-        }
+        if (c < nvec) dst[c] = Pack<E>::pack(acc[u]);
       }
     }
     __syncwarp();
@@ -151,16 +153,19 @@ cudaError_t launch_combine(int dtype, const void* op, const float* row_gate,
   int blocks = (T + kCombWarps - 1) / kCombWarps;
   const int cap = device_sm_count() * 8;
   if (blocks > cap) blocks = cap;
+  // rows loaded per batch: a top-2 token's rows in one batch; more rows
+  // (top-k > 2, expanded candidates, expert choice, a shared expert) in 4s
+  const bool wide = kc + (shared_out ? 1 : 0) > 2;
   if (dtype == 1) {
-    return launch_pdl(combine_kernel<__nv_bfloat16>, blocks, kCombThreads, 0, s,
-                      static_cast<const __nv_bfloat16*>(op), row_gate, tok_rows,
-                      static_cast<const __nv_bfloat16*>(shared_out),
+    auto k = wide ? combine_kernel<__nv_bfloat16, 4> : combine_kernel<__nv_bfloat16, 2>;
+    return launch_pdl(k, blocks, kCombThreads, 0, s, static_cast<const __nv_bfloat16*>(op),
+                      row_gate, tok_rows, static_cast<const __nv_bfloat16*>(shared_out),
                       static_cast<__nv_bfloat16*>(y), T, d, kc, rmax);
   } else {
-    return launch_pdl(combine_kernel<float>, blocks, kCombThreads, 0, s,
-                      static_cast<const float*>(op), row_gate, tok_rows,
-                      static_cast<const float*>(shared_out), static_cast<float*>(y), T, d, kc,
-                      rmax);
+    auto k = wide ? combine_kernel<float, 4> : combine_kernel<float, 2>;
+    return launch_pdl(k, blocks, kCombThreads, 0, s, static_cast<const float*>(op), row_gate,
+                      tok_rows, static_cast<const float*>(shared_out), static_cast<float*>(y), T,
+                      d, kc, rmax);
   }
   return cudaGetLastError();
 }
