@@ -257,8 +257,10 @@ int moe_dispatch(const moe_config* cfg, const void* x, const int32_t* cand_idx,
  * the choice: "0" one CTA per tile, anything else pairs. In pair form an
  * expert's last tile with fewer than 256 rows is computed transposed (the
  * weight columns as the MMA's 256 rows, the tile's rows as its columns), so
- * it costs its rows instead of a padded tile; the outputs are the same bits.
- * MOE_GEMM_SWAP_TAILS=0, read at every launch, pads those tiles instead.
+ * it costs its rows instead of a padded tile; the second GEMM (and
+ * moe_grouped_gemm) computes every tile that way. The outputs are the same
+ * bits. MOE_GEMM_SWAP_TAILS=0, read at every launch, computes every tile
+ * untransposed, padding the last ones.
  */
 int moe_expert_ffn(const moe_config* cfg, const void* xp, const int32_t* offsets,
                    int32_t n_segments, int64_t rows_max, int32_t f,

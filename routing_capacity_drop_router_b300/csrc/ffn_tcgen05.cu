@@ -29,7 +29,12 @@
 //   a TMEM lane per output column and stores rows transposed, neighbouring
 //   lanes trading one value so each writes 32-bit words; under SwiGLU the
 //   gate and up halves of a column sit in different lane quadrants and meet
-//   through a small shared-memory exchange.
+//   through a small shared-memory exchange. Without SwiGLU (the second GEMM)
+//   every pair tile runs transposed, full ones with N = 256: the same
+//   products, and the transposed epilogue's stores (64 contiguous bytes of a
+//   row per half-warp) load the memory system less than one 16-byte store
+//   per row per lane; under SwiGLU full tiles keep the untransposed form,
+//   whose epilogue needs no exchange.
 //   Where clusters cannot be formed the same kernel runs one CTA per tile
 //   (128 rows, both B halves, cta_group::1, 4 stages).
 //   warp 0   : TMA producer of its CTA's operand tiles (128-byte swizzle); A
@@ -59,6 +64,9 @@
 //   a 128-byte k-block then holds 128 k, B tiles are K-major like A, the MMAs
 //   are kind::f8f6f4 (e4m3 x e4m3, fp32 accumulate) and the epilogue scales
 //   each accumulator by its row's and column's scales before the SwiGLU.
+//   The producers' waits for a free stage and the epilogue's waits for a
+//   full accumulator suspend in the barrier (try_wait with a time hint)
+//   rather than spin; the MMA issuer, on the critical path, spins.
 //   Every mbarrier wait is bounded (1 s of globaltimer); on expiry the CTA
 //   raises a shared abort flag, every role leaves its loop, outstanding TMA
 //   copies and MMAs are drained (bounded), TMEM is freed and
@@ -328,11 +336,12 @@ __global__ void __launch_bounds__(threads_of<GATHER>(), 1) grouped_gemm_tc_kerne
     col0 = n_idx * tile_n;
   };
   // A segment's last tile with fewer rows than a pair tile runs transposed,
-  // N = its rows rounded up to 32 (nsw), instead of padding the rows to 256.
+  // N = its rows rounded up to 32 (nsw), instead of padding the rows to 256;
+  // without SwiGLU every tile does (full ones with N = 256).
   auto transposed = [&](int row0, int row_end, int& nsw) {
-    const int n = min(row_end, rows_max) - row0;
+    const int n = min(min(row_end, rows_max) - row0, G::kTileRows);
     nsw = (n + 31) & ~31;
-    return kSwap && swap_tails != 0 && n > 0 && n < G::kTileRows;
+    return kSwap && swap_tails != 0 && n > 0 && (!SWIGLU || n < G::kTileRows);
   };
 
   const uint32_t stage0 = base;
@@ -427,7 +436,7 @@ __global__ void __launch_bounds__(threads_of<GATHER>(), 1) grouped_gemm_tc_kerne
         for (int kb = 0; kb < num_kb; ++kb) {
           int w = 1;
           if (lane == 0)
-            w = mbar_wait(smem_u32(&ctrl->empty[stage]), phase ^ 1u, abort_flag, kWaitLimitNs);
+            w = mbar_wait_suspend(smem_u32(&ctrl->empty[stage]), phase ^ 1u, abort_flag, kWaitLimitNs);
           if (!__shfl_sync(0xffffffffu, w, 0)) {
             ok = false;
             break;
@@ -470,7 +479,7 @@ __global__ void __launch_bounds__(threads_of<GATHER>(), 1) grouped_gemm_tc_kerne
       const int arow = row0 + static_cast<int>(rank) * (sw ? nsw / 2 : kBM);
       for (int kb = 0; kb < num_kb; ++kb) {
         const uint32_t fb_local = smem_u32(&ctrl->full[stage]);
-        if (!mbar_wait(smem_u32(&ctrl->empty[stage]), phase ^ 1u, abort_flag, kWaitLimitNs)) {
+        if (!mbar_wait_suspend(smem_u32(&ctrl->empty[stage]), phase ^ 1u, abort_flag, kWaitLimitNs)) {
           ok = false;
           break;
         }
@@ -587,7 +596,8 @@ __global__ void __launch_bounds__(threads_of<GATHER>(), 1) grouped_gemm_tc_kerne
       const int buf = local & 1;
       const uint32_t use = static_cast<uint32_t>(local >> 1);
       int ok = 1;
-      if (lane == 0) ok = mbar_wait(smem_u32(&ctrl->tfull[buf]), use & 1u, abort_flag, kWaitLimitNs);
+      if (lane == 0)
+        ok = mbar_wait_suspend(smem_u32(&ctrl->tfull[buf]), use & 1u, abort_flag, kWaitLimitNs);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
@@ -597,7 +607,7 @@ __global__ void __launch_bounds__(threads_of<GATHER>(), 1) grouped_gemm_tc_kerne
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * kBN);
       if (transposed(row0, row_end, nsw)) {
         // TMEM lane = output column, TMEM column = token row row0 + column
-        const int lim = min(row_end, rows_max);
+        const int lim = min(min(row_end, rows_max), row0 + G::kTileRows);
         const int ntok = lim - row0;
         if (SWIGLU) {
           // lanes 0-63: W1 (gate) columns col0 + 64 * rank ..; lanes 64-127:
@@ -815,7 +825,7 @@ cudaError_t launch_gemm(const CUtensorMap& mA, const CUtensorMap& mB1, const CUt
   const long long cap = pair ? slots : sms;
   if (units > cap) units = cap;
   const int rmax = rows_max > 0x7fffffff ? 0x7fffffff : static_cast<int>(rows_max);
-  // segment tails of the pair form run transposed unless MOE_GEMM_SWAP_TAILS=0
+  // pair tiles run transposed (see transposed()) unless MOE_GEMM_SWAP_TAILS=0
   const char* sw_env = getenv("MOE_GEMM_SWAP_TAILS");
   const int swap_tails = sw_env ? (sw_env[0] != '0') : 1;
 

@@ -44,6 +44,39 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
   }
 }
+// try_wait with a suspend-time hint: a thread whose phase is not complete
+// sleeps in the barrier until the phase completes or the hint (ns) elapses,
+// instead of spinning. For waits that are usually long and not on the
+// tensor-core issue path (a producer whose ring is full, an epilogue waiting
+// for its accumulator), where spinning only takes issue slots and power.
+constexpr uint32_t kSuspendHintNs = 20000;
+__device__ __forceinline__ bool mbar_try_suspend(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
+      : "memory");
+  return ok != 0u;
+}
+// mbar_wait with suspend-hinted tries; bounded the same way (the limit is
+// checked after every try, so at most limit_ns + the hint).
+__device__ __forceinline__ bool mbar_wait_suspend(uint32_t bar, uint32_t parity,
+                                                  volatile int* abort_flag,
+                                                  unsigned long long limit_ns) {
+  if (mbar_try(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  while (true) {
+    if (mbar_try_suspend(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_ns() - t0 > limit_ns) {
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }

@@ -22,9 +22,10 @@ def _segments(sizes):
 @pytest.fixture(params=["cta_pairs", "cta_pairs_padded", "single_cta"])
 def gemm_form(request, monkeypatch):
     """Run a bf16 case through every form of the tcgen05 grouped GEMM: CTA
-    pairs (cta_group::2, 256-row tiles) whose segment tails run transposed
-    (the default), the same pairs with the tails padded to 256 rows, and one
-    CTA per 128-row tile."""
+    pairs (cta_group::2, 256-row tiles) whose segment tails run transposed,
+    and every tile of the second GEMM (the default), the same pairs with no
+    tile transposed and the tails padded to 256 rows, and one CTA per
+    128-row tile."""
     monkeypatch.setenv("MOE_GEMM_CTA_PAIRS", "0" if request.param == "single_cta" else "1")
     monkeypatch.setenv("MOE_GEMM_SWAP_TAILS", "0" if request.param == "cta_pairs_padded" else "1")
     return request.param
@@ -348,9 +349,11 @@ def test_expert_ffn_f32_against_oracle(sizes, d, f):
 
 
 def test_transposed_tails_equal_padded_bit_for_bit(monkeypatch):
-    """A segment's last tile computed transposed (the default in pair form)
-    gives the same bits as the padded 256-row tile (MOE_GEMM_SWAP_TAILS=0):
-    each output is the same sum over the same k."""
+    """Tiles computed transposed (the default in pair form: every segment's
+    last tile, and every tile of the second GEMM and of the plain grouped
+    GEMM) give the same bits as the untransposed form with the tails padded
+    to 256 rows (MOE_GEMM_SWAP_TAILS=0): each output is the same sum over the
+    same k."""
     monkeypatch.setenv("MOE_GEMM_CTA_PAIRS", "1")
     sizes, d, f = TAIL_SIZES, 320, 192
     S = len(sizes)
