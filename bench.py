@@ -2,6 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference ...     # the CPU oracle, timed on host cores
+    python bench.py --vs-cublas --steps 10   # plain grouped GEMM beside cuBLAS bmm
 
 A step is one moe_layer_forward (router GEMM + softmax/top-k, per-expert
 capacity selection, dispatch, grouped SwiGLU expert GEMMs, combine, load
@@ -282,10 +283,10 @@ def gemm_traffic(w):
 # keyed by the sha256 prefix of the kernel source it was taken on.
 GEMM_TRAFFIC = {
     # the CTA-pair grouped GEMM on the Mixtral-shaped layer at gamma 1: GEMM1+SwiGLU
-    # 1.966183 GB read + 0.140524 GB written, GEMM2 1.181313 GB + 0.039829 GB
-    "mixtral_bf16_gamma1": {"kernel_sha": "3aee9bad50da7f7f",
-                            "bytes_per_launch_pair": 1.966183e9 + 0.140524e9 +
-                            1.181313e9 + 0.039829e9},
+    # 2.009582 GB read + 0.140430 GB written, GEMM2 1.181581 GB + 0.039514 GB
+    "mixtral_bf16_gamma1": {"kernel_sha": "9ea6ad912332f037",
+                            "bytes_per_launch_pair": 2.009582e9 + 0.140430e9 +
+                            1.181581e9 + 0.039514e9},
 }
 
 
@@ -795,6 +796,61 @@ def run_stage(args):
     print(json.dumps(out), flush=True)
 
 
+# (segments, rows per segment, K, n_out): the Mixtral-shaped expert GEMMs at
+# 1024 rows per expert (GEMM1 as one plain GEMM of width 2f, then GEMM2), and
+# GEMM1's width on 614-row segments, whose last tiles are ragged
+VS_CUBLAS_SHAPES = [(8, 1024, 4096, 28672), (8, 1024, 14336, 4096), (8, 614, 4096, 28672)]
+
+
+def run_vs_cublas(args):
+    """--vs-cublas: the plain grouped GEMM (moe_grouped_gemm, bf16) against
+    cuBLAS's batched GEMM (torch.bmm) on the same equal-sized segments, the
+    L2 flushed before every launch; prints both rates and the largest
+    difference between the two outputs. A library yardstick for the expert
+    GEMMs, not part of the layer."""
+    import routing_capacity_drop_router_b300 as M
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    gen = torch.Generator(device=dev).manual_seed(7)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            flush.zero_()
+            fn()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for a, b in evs:
+            flush.zero_()
+            a.record()
+            fn()
+            b.record()
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in evs)
+
+    rows_out = []
+    for S, n, K, n_out in VS_CUBLAS_SHAPES:
+        R = S * n
+        A = (torch.randn((R, K), device=dev, generator=gen) * 0.05).to(torch.bfloat16)
+        B = (torch.randn((S, K, n_out), device=dev, generator=gen) * 0.05).to(torch.bfloat16)
+        out = torch.empty((R, n_out), dtype=torch.bfloat16, device=dev)
+        ref = torch.empty_like(out)
+        offs = torch.arange(0, R + 1, n, dtype=torch.int32, device=dev)
+        ws = torch.zeros(M.ffn_workspace_size(0, 0, "bf16"), dtype=torch.uint8, device=dev)
+        ms_ours = timed(lambda: M.moe_grouped_gemm("bf16", A, offs, S, R, K, n_out, B, out, ws))
+        ms_lib = timed(lambda: torch.bmm(A.view(S, n, K), B, out=ref.view(S, n, n_out)))
+        flops = 2.0 * R * K * n_out
+        rows_out.append({"segments": S, "rows_per_segment": n, "K": K, "n_out": n_out,
+                         "ours_ms": ms_ours, "ours_tflops": flops / (ms_ours * 1e-3) / 1e12,
+                         "cublas_ms": ms_lib, "cublas_tflops": flops / (ms_lib * 1e-3) / 1e12,
+                         "ours_over_cublas": ms_lib / ms_ours,
+                         "max_abs_diff": (out.float() - ref.float()).abs().max().item()})
+        del A, B, out, ref
+    print(json.dumps({"metric": "grouped GEMM against cuBLAS batched GEMM", "unit": "TFLOP/s",
+                      "steps": args.steps, "warmup": args.warmup,
+                      "l2": "flushed before every launch", "rows": rows_out}), flush=True)
+
+
 def run_ep_sim(args):
     """--ep-sim: expert parallelism simulated on one GPU ("Capacity-Aware
     Inference", section 1: under expert parallelism the layer waits for the
@@ -898,6 +954,9 @@ def main():
     ap.add_argument("--ep-sim", action="store_true",
                     help="simulate expert parallelism: time each device group's experts on "
                          "its share of the SMs and report the straggler")
+    ap.add_argument("--vs-cublas", action="store_true",
+                    help="time the plain grouped GEMM beside cuBLAS's batched GEMM on the "
+                         "same segments")
     ap.add_argument("--ep-devices", type=int, default=8)
     ap.add_argument("--ep-reps", type=int, default=10)
     args = ap.parse_args()
@@ -906,6 +965,9 @@ def main():
         return
     if args.ep_sim:
         run_ep_sim(args)
+        return
+    if args.vs_cublas:
+        run_vs_cublas(args)
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
