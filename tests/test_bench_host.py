@@ -50,3 +50,17 @@ def test_oracle_sampler_takes_a_bounded_sample(target_s):
     got, dt = smp.run(n)
     assert got == n and dt > 0
     assert "full-batch routing" in smp.describe(got, dt)
+
+
+def test_vs_cublas_shapes_meet_the_grouped_gemm_shape_rules():
+    """--vs-cublas runs moe_grouped_gemm, which takes bf16 K and n_out in
+    multiples of 64 and at most 256 segments, and cuBLAS's batched form,
+    which needs equal segments: every shape must satisfy both, and the
+    first two must be the expert GEMMs of the Mixtral-shaped workload."""
+    w = W.ALL["mixtral_bf16"]
+    for S, n, K, n_out in bench.VS_CUBLAS_SHAPES:
+        assert 1 <= S <= 256 and n >= 1
+        assert K % 64 == 0 and n_out % 64 == 0
+    (S1, n1, K1, o1), (S2, n2, K2, o2) = bench.VS_CUBLAS_SHAPES[:2]
+    assert (S1, K1, o1) == (w.N, w.d, 2 * w.f) and (S2, K2, o2) == (w.N, w.f, w.d)
+    assert n1 == n2 == w.k * w.T // w.N  # rows per expert with no capacity limit, on average
